@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of the fused MoE forward on GB300.
+
+One step = one full forward (route -> layout -> quantise/gather -> grouped
+GEMM with fused weighted scatter -> bf16 finalize) over one batch of seeded
+synthetic inputs resident in HBM.  Default workload: the 128-token /
+256-expert FP8 shape (M=128, K=2048, N=512, E=256, top-8, softcap 30).
+Metric: TFLOPS on compact routed rows (2*R*N*K per forward, R = M*top_k);
+µs per forward and the fraction of the roofline are reported beside it.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(token data-parallel, no collective on the data path); rank 0 prints the
+aggregate.  ``--impl reference`` times the CPU oracle (the only reference
+implementation this workload has) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_forward_gb300 import inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FLUSH_BYTES = 256 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="qwen_small_batch_fp8",
+                    choices=list(inputs.FP8_CONFIGS) + list(inputs.BF16_CONFIGS))
+    ap.add_argument("--routing", default="uniform")
+    ap.add_argument("--rho", type=float, default=1.0)
+    ap.add_argument("--block-m", type=int, default=0)
+    ap.add_argument("--k-splits", type=int, default=0)
+    ap.add_argument("--sched", choices=["queue", "static"], default="queue")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def all_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- workload facts
+def workload(cfg_name, args, seed):
+    if cfg_name in inputs.FP8_CONFIGS:
+        d = inputs.make_fp8_inputs(cfg_name, seed=seed)
+        c = d["cfg"]
+        desc = (f"{cfg_name} M={c['M']} K={c['K']} N={c['N']} E={c['E']} top{c['k']} "
+                f"softcap={c['softcap']:g} fp8-e4m3 128x128/1x128 blocks")
+        return "fp8", d, desc
+    d = inputs.make_bf16_inputs(cfg_name, routing=args.routing, rho=args.rho, seed=seed)
+    c = d["cfg"]
+    desc = (f"{cfg_name} T={c['T']} H={c['H']} I={c['I']} E={c['E']} top{c['k']} "
+            f"routing={args.routing} rho={args.rho:g} bf16 gated FFN")
+    return "bf16", d, desc
+
+
+def flops_per_step(kind, c):
+    if kind == "fp8":
+        return 2.0 * c["M"] * c["k"] * c["N"] * c["K"]
+    R = c["T"] * c["k"]
+    return 2.0 * R * (2 * c["I"]) * c["H"] + 2.0 * R * c["H"] * c["I"]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        self.path = tempfile.mktemp(suffix=".csv")
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def bench_ours(args, rank, world, local):
+    from mixture_experts_forward_gb300 import _lib as L
+    from mixture_experts_forward_gb300 import build as moe_build
+    moe_build.build()
+    L.lib()
+    dev = torch.device("cuda", local)
+    kind, d, desc = workload(args.config, args, args.seed + rank)
+    c = d["cfg"]
+    sched = L.SCHED_QUEUE if args.sched == "queue" else L.SCHED_STATIC
+    if kind == "fp8":
+        logits, x = d["logits"].to(dev), d["x"].to(dev)
+        w, ws_ = d["w_q"].to(dev), d["w_scales"].to(dev)
+        M, K, N, E, k = c["M"], c["K"], c["N"], c["E"], c["k"]
+        fa = L.forward_args(dtype=L.DTYPE_FP8, M=M, K=K, N=N, E=E, top_k=k, softcap=c["softcap"],
+                            logits=logits, x=x, w=w, w_scales=ws_, block_m=args.block_m,
+                            sched=sched, k_splits=args.k_splits, use_graph=1)
+        out_cols = N
+    else:
+        logits, x = d["logits"].to(dev), d["x"].to(dev)
+        w, w2 = d["w_up"].to(dev), d["w_dn"].to(dev)
+        M, K, N, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+        fa = L.forward_args(dtype=L.DTYPE_BF16, M=M, K=K, N=N, E=E, top_k=k, softcap=0.0,
+                            logits=logits, x=x, w=w, w2=w2, block_m=args.block_m, sched=sched,
+                            use_graph=1)
+        out_cols = K
+    ws = L.new_workspace(L.workspace_size(fa), device=dev)
+    out = torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    block_m, k_splits = L.forward_plan(fa)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        L.forward(fa, out, ws)
+    torch.cuda.synchronize()
+    assert L.get_error(ws) == L.MOE_OK
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                          # L2 flushed between steps (untimed)
+        starts[i].record(stream)
+        L.forward(fa, out, ws)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    status = L.get_error(ws)
+    assert status == L.MOE_OK, L.status_string(status)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = all_max(sum(step_ms), world)
+    fl = flops_per_step(kind, c)
+    value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / args.steps
+    launches_per_step = 5 if kind == "fp8" else 6
+
+    # routing facts of this batch (for bytes and the roofline)
+    ids, _ = L.route(logits, k, softcap=c.get("softcap", 0.0))
+    lay = L.layout(ids, E, block_m, L.new_workspace(L.CTRL_BYTES, device=dev))
+    counts = lay["counts"].cpu().numpy()
+    touched = int((counts > 0).sum())
+    pk = peaks()
+
+    roof = dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, flush,
+                           touched, pk)
+    if kind == "fp8":
+        alg_bytes = touched * (N * K + (N // 128) * (K // 128) * 4) + M * E * 4 + M * K * 2 + M * N * 2
+        t_roof = max(fl / (2 * pk["bf16"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
+    else:
+        alg_bytes = touched * (2 * N * K + K * N) * 2 + M * E * 4 + M * K * 2 + M * K * 2
+        t_roof = max(fl / (pk["bf16"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
+    fwd_roof_frac = t_roof / (ms_per_step * 1e-3)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = bench_e2e(L, fa, d, kind, dev, args, flush, fl, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(kind, d, c)
+
+    res = {
+        "metric": "fused-MoE fwd TFLOPS on compact routed rows",
+        "value": round(value, 4), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "us_per_forward": round(ms_per_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3" if kind == "fp8" else "bf16", "data": "synthetic (seeded)",
+        "config": {"workload": desc, "l2": "flushed between steps (256 MiB write)",
+                   "block_m": block_m, "k_splits": k_splits, "sched": args.sched,
+                   "touched_experts": touched, "compact_rows": int(M * k),
+                   "parallelism": f"replicas x{world} (token data-parallel, no collective)"},
+        "forward_roofline": {"bound": "hbm" if kind == "fp8" and t_roof == alg_bytes / (pk["hbm"] * 1e9) else "tensor",
+                             "alg_bytes": int(alg_bytes), "roofline_us": round(t_roof * 1e6, 3),
+                             "frac": round(fwd_roof_frac, 4), "peak_source": pk["src"]},
+        "roofline": roof,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, flush, touched, pk):
+    """Time the grouped GEMM alone (same inputs and tiling as the forward) with
+    CUDA events on its stream and report it against its roofline."""
+    stream = torch.cuda.current_stream(dev)
+    ws = L.new_workspace(L.CTRL_BYTES, device=dev)
+    if kind == "fp8":
+        M, K, N, E, k = c["M"], c["K"], c["N"], c["E"], c["k"]
+        _, wts = L.route(d["logits"].to(dev), k, softcap=c["softcap"])
+        acc = torch.zeros(M, N, dtype=torch.float32, device=dev)
+        a_q, a_s = L.quant_gather(d["x"].to(dev), k, lay["route_slot"], zero_acc=acc)
+        w, w_s = d["w_q"].to(dev), d["w_scales"].to(dev)
+
+        def launch():
+            L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_SCATTER, a=a_q, a_scales=a_s, w=w,
+                           w_scales=w_s, offsets=lay["offsets"], tile_offsets=lay["tile_offsets"],
+                           out=acc, ws=ws, block_m=block_m, sorted_route_ids=lay["sorted_route_ids"],
+                           route_weights=wts, M=M, top_k=k, sched=sched, k_splits=k_splits)
+        R = M * k
+        alg = touched * (N * K + (N // 128) * (K // 128) * 4) + R * K + (K // 128) * R * 4 + M * N * 4
+        fl = 2.0 * R * N * K
+        name = "grouped_gemm_kernel<fp8, scatter>"
+        src = "grouped_gemm.cu"
+    else:
+        return None
+    for _ in range(3):
+        flush.zero_()
+        launch()
+    n = 20
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        st[i].record(stream)
+        launch()
+        en[i].record(stream)
+    torch.cuda.synchronize()
+    assert L.get_error(ws) == L.MOE_OK
+    avg_s = statistics.mean(s.elapsed_time(e) for s, e in zip(st, en)) * 1e-3
+    t_hbm = alg / (pk["hbm"] * 1e9)
+    t_tc = fl / (2 * pk["bf16"] * 1e12)
+    traffic = stored_traffic(src, name)
+    if t_hbm >= t_tc:
+        achieved = alg / avg_s / 1e9
+        return {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": pk["hbm"], "unit": "GB/s", "frac": round(achieved / pk["hbm"], 4),
+                "traffic": traffic, "alg_bytes_per_launch": int(alg),
+                "avg_launch_us": round(avg_s * 1e6, 3),
+                "peak_note": f"{pk['src']} copy bandwidth (burst)"}
+    achieved = fl / avg_s / 1e12
+    peak = 2 * pk["bf16"]
+    return {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+            "flops_per_launch": fl, "avg_launch_us": round(avg_s * 1e6, 3),
+            "peak_note": f"fp8 = 2 x {pk['src']} bf16 burst"}
+
+
+def stored_traffic(src_name: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else null)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    j = json.load(open(p))
+    src = os.path.join(ROOT, "mixture_experts_forward_gb300", "csrc", src_name)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    e = j.get(kernel)
+    if not e or e.get("source_sha") != sha:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def bench_e2e(L, fa, d, kind, dev, args, flush, fl, world):
+    """Same metric through moe_forward_host: pinned host inputs copied in and
+    the bf16 result copied out inside every timed step."""
+    stream = torch.cuda.current_stream(dev)
+    c = d["cfg"]
+    if kind == "fp8":
+        M, K, N = c["M"], c["K"], c["N"]
+        out_cols = N
+    else:
+        M, K, N = c["T"], c["H"], c["I"]
+        out_cols = K
+    h_logits = d["logits"].contiguous().pin_memory()
+    h_x = d["x"].contiguous().pin_memory()
+    h_out = torch.empty(M, out_cols, dtype=torch.bfloat16).pin_memory()
+    ws = L.new_workspace(L.workspace_size(fa), device=dev)
+    for _ in range(3):
+        L.forward_host(fa, h_logits, h_x, h_out, ws)
+    torch.cuda.synchronize()
+    steps = max(10, args.steps // 2)
+    st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        st[i].record(stream)
+        L.forward_host(fa, h_logits, h_x, h_out, ws)
+        en[i].record(stream)
+    torch.cuda.synchronize()
+    total = all_max(sum(s.elapsed_time(e) for s, e in zip(st, en)), world)
+    h2d = h_logits.numel() * 4 + h_x.numel() * 2
+    d2h = h_out.numel() * 2
+    return {"value": round(world * fl * steps / (total * 1e-3) / 1e12, 4), "unit": "TFLOPS",
+            "us_per_forward": round(total / steps * 1e3, 3),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_step(kind, d, c, tokens, threads):
+    import oracle
+    if kind == "fp8":
+        oracle.forward_fp8(d["logits"].numpy(), inputs.bf16_bits(d["x"]), d["w_q"].numpy(),
+                           d["w_scales"].numpy(), k=c["k"], softcap=c["softcap"], tokens=tokens,
+                           threads=threads)
+        return 2.0 * len(tokens) * c["k"] * c["N"] * c["K"]
+    ids, w = oracle.route(d["logits"].numpy(), c["k"])
+    oracle.ffn_bf16(inputs.bf16_bits(d["x"]), ids, w, inputs.bf16_bits(d["w_up"]),
+                    inputs.bf16_bits(d["w_dn"]), tokens=tokens, threads=threads)
+    R = len(tokens) * c["k"]
+    return 2.0 * R * 2 * c["I"] * c["H"] + 2.0 * R * c["H"] * c["I"]
+
+
+def cpu_baseline(kind, d, c, budget_s=12.0):
+    """The oracle as it stands, on this host's cores, over a bounded sample of
+    the workload's tokens (repeated until about budget_s of CPU work)."""
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    M = c["M"] if kind == "fp8" else c["T"]
+    n_tok = M if kind == "fp8" else 16
+    tokens = np.arange(min(M, n_tok), dtype=np.int32)
+    flops, t0, reps = 0.0, time.perf_counter(), 0
+    while True:
+        flops += oracle_step(kind, d, c, tokens, threads)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s or reps >= 50:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOPS", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{reps} oracle forwards of the first {len(tokens)} tokens "
+                      f"(all routing/layout/quantisation steps, binary64 GEMM) in {dt:.1f} s"}
+
+
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    kind, d, desc = workload(args.config, args, args.seed)
+    c = d["cfg"]
+    threads = os.cpu_count() or 1
+    M = c["M"] if kind == "fp8" else c["T"]
+    tokens = np.arange(min(M, 16 if kind == "fp8" else 4), dtype=np.int32)
+    for _ in range(args.warmup):
+        oracle_step(kind, d, c, tokens, threads)
+    fl, t0 = 0.0, time.perf_counter()
+    for _ in range(args.steps):
+        fl += oracle_step(kind, d, c, tokens, threads)
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    sample = (f"each step: oracle forward of {len(tokens)} of {M} tokens (routing, layout and "
+              f"quantisation of all tokens; binary64 GEMM for the sampled tokens' routes)")
+    res = {"impl": "reference", "metric": "fused-MoE fwd TFLOPS on compact routed rows",
+           "value": round(value, 6), "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
+           "config": {"workload": desc},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            bench_reference(args, rank, world)
+        else:
+            bench_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

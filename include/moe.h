@@ -1,0 +1,225 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) fused Mixture-of-Experts forward.
+ *
+ * The forward routes each token to top_k experts, lays the routed rows out
+ * expert by expert, quantises them blockwise to FP8 E4M3 (or keeps them in
+ * BF16), multiplies them by the experts' weights in one grouped GEMM and adds
+ * the routing-weighted results back into token order.  The steps and their
+ * data follow "Fused MoE FP8: 8.09 -> 13.18 TFLOPS (1.63x)" (section
+ * "Pipeline overview" and section "Baseline: 7 kernels", items 1-7); the BF16
+ * gated FFN follows the benchmark design (section 3) of "H200 MoE Grouped
+ * GEMM: accounting fix, online replay, SM90 tuning"; the persistent tile queue
+ * follows section 2.2 of the blog retelling of "Weave".
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers, owned by the caller, row-major,
+ *    and 16-byte aligned unless stated otherwise ("host" pointers are named so).
+ *    The library never allocates device memory in these calls.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous: they enqueue work and return.
+ *  - Argument errors are detected on the host before anything is enqueued and
+ *    returned synchronously (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_WORKSPACE).  Launch failures return MOE_ERR_CUDA.
+ *  - Errors found on the device (an expert id out of range, a pipeline wait
+ *    that timed out) are recorded in a status word inside the caller's
+ *    workspace (first error wins) and read back with moe_get_error().
+ *  - Supported sizes: 1 <= top_k <= min(E, 32); E <= 1024; K % 128 == 0 and
+ *    N % 128 == 0 on the FP8 path; K % 64 == 0 and N % 128 == 0 on the BF16
+ *    path; M * top_k < 2^31.
+ */
+#ifndef MOE_GB300_H_
+#define MOE_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad enum */
+  MOE_ERR_UNSUPPORTED = 2,   /* size outside the supported set above */
+  MOE_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call failed */
+  MOE_ERR_TIMEOUT = 5,       /* device: a pipeline wait gave up (no GPU hang) */
+  MOE_ERR_DEVICE_FAULT = 6   /* device: invalid data (e.g. expert id >= E) */
+} moe_status_t;
+
+typedef enum { MOE_DTYPE_FP8_E4M3 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype_t;
+
+typedef enum {
+  MOE_EPI_SCATTER = 0,  /* out f32 [M,N] += route_weight * row   (weighted scatter-add) */
+  MOE_EPI_STORE = 1,    /* out f32 [R,N]  = row                   (expert-compact rows) */
+  MOE_EPI_SWIGLU = 2    /* out bf16 [R,N/2] = silu(gate) * up; weight rows [0,N/2) gate, [N/2,N) up */
+} moe_epilogue_t;
+
+typedef enum {
+  MOE_SCHED_QUEUE = 0,  /* persistent CTAs pull tiles from one atomic counter */
+  MOE_SCHED_STATIC = 1  /* persistent CTAs statically partitioned over experts */
+} moe_sched_t;
+
+/* Bytes of the control block (status word and tile-queue counters) that
+ * every workspace starts with.  A fresh workspace must have this block
+ * zeroed once (cudaMemset) before its first use. */
+#define MOE_CTRL_BYTES 256
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status_t s);
+
+/* Number of streaming multiprocessors of the current device (0 on error). */
+int moe_num_sms(void);
+
+/* Route — "Fused MoE FP8" section "Baseline: 7 kernels", item 1.
+ * For each token t: z_e = softcap * tanh(logits[t,e] / softcap) (softcap == 0:
+ * z_e = logits[t,e]); the top_k experts by (z descending, expert id
+ * ascending) are written to ids[t, 0..top_k) in that order; weights are
+ * renorm = 1: exp(z_j - z_0) / sum over the selected j (sum in selection order),
+ * renorm = 0: exp(z_j - z_0) / sum over all E experts (sum in expert-id order).
+ * exp and tanh are evaluated by a fixed sequence of IEEE binary32 operations
+ * (Cody-Waite exp with a degree-7 Taylor polynomial; tanh by its degree-17
+ * Taylor series below |t| = 0.5, else 1 - 2/(exp(2|t|) + 1)), so results are
+ * reproducible bit for bit.
+ * logits: f32 [M,E]; ids: s32 [M,top_k]; weights: f32 [M,top_k]. */
+moe_status_t moe_route(const float* logits, int M, int E, int top_k, float softcap,
+                       int renorm, int32_t* ids, float* weights, void* stream);
+
+/* Count + build layout — "Fused MoE FP8" section "Fusion 3" (counts and the
+ * exclusive prefix) and section 4.3 of the Weave retelling (per-expert tiles).
+ * R = M*top_k routes, route r = t*top_k + j.  Writes
+ *   counts[E]            routes per expert,
+ *   offsets[E+1]         exclusive prefix of counts (offsets[E] = R),
+ *   sorted_route_ids[R]  routes grouped by expert, ascending route id inside
+ *                        each expert (a deterministic, stable layout),
+ *   route_slot[R]        inverse permutation (slot of each route),
+ *   tile_offsets[E+1]    exclusive prefix of ceil(counts[e] / block_m).
+ * ids: s32 [M,top_k].  ws: a workspace whose control block receives the
+ * status (MOE_ERR_DEVICE_FAULT if an id is outside [0,E)) and whose tile
+ * queue counter is reset.  block_m in [16,256], a multiple of 16. */
+moe_status_t moe_layout(const int32_t* ids, int M, int E, int top_k, int block_m,
+                        int32_t* counts, int32_t* offsets, int32_t* sorted_route_ids,
+                        int32_t* route_slot, int32_t* tile_offsets, void* ws, void* stream);
+
+/* Quantise + sort/gather — "Fused MoE FP8" section "Baseline: 7 kernels"
+ * item 4 and section "Fusion 2" (QSG).  Per token t and 1x128 block b:
+ * amax = max |x|, s = amax / 448, q = E4M3_rne_satfinite(x * (1/s)) (amax = 0:
+ * s = 0 and q = 0).  The token's codes go to every slot route_slot[t*top_k+j];
+ * a_scales is stored block-major: a_scales[b*R + slot] = s.
+ * x: bf16 [M,K]; a_q: u8 [R,K]; a_scales: f32 [K/128, R].
+ * zero_acc (optional, may be NULL): f32 [M, zero_cols] set to 0 in the same
+ * pass (the fused output memset of section "Fused Memset"). */
+moe_status_t moe_quant_gather(const void* x, int M, int K, int top_k,
+                              const int32_t* route_slot, uint8_t* a_q, float* a_scales,
+                              float* zero_acc, int zero_cols, void* stream);
+
+/* Arguments of one grouped GEMM launch (see moe_grouped_gemm). */
+typedef struct {
+  moe_dtype_t dtype;          /* FP8_E4M3 (blockwise scales) or BF16 */
+  moe_epilogue_t epilogue;    /* SCATTER, STORE or SWIGLU */
+  moe_sched_t sched;          /* QUEUE or STATIC */
+  int block_m;                /* routed rows per tile: 16..256, multiple of 16
+                                 (FP8: at most 128) */
+  int E, N, K;                /* weights are [E, N, K] */
+  int R;                      /* rows of `a` (M * top_k) */
+  int M, top_k;               /* SCATTER only: output rows and routes per token */
+  const void* a;              /* [R, K] e4m3 or bf16, expert-compact rows */
+  const float* a_scales;      /* FP8: [K/128, R] */
+  const void* w;              /* [E, N, K] e4m3 or bf16 */
+  const float* w_scales;      /* FP8: [E, N/128, K/128] (one scale per 128x128 block) */
+  const int32_t* offsets;     /* [E+1] first slot of each expert */
+  const int32_t* tile_offsets;/* [E+1] prefix of ceil(count/block_m), same block_m */
+  const int32_t* sorted_route_ids; /* SCATTER: [R] route of each slot */
+  const float* route_weights; /* SCATTER: [M*top_k] */
+  void* out;                  /* see moe_epilogue_t */
+  int k_splits;               /* FP8 SCATTER: K split into this many tiles (0 = auto) */
+  int num_ctas;               /* persistent CTAs (0 = one per SM) */
+} moe_gemm_args;
+
+/* Grouped GEMM — "Fused MoE FP8" section "Baseline: 7 kernels" item 6, with
+ * the weighted scatter of item 7 fused into its epilogue (section "Fusion 1").
+ * For every slot s of expert e and output column n:
+ *   FP8:  Y[s,n] = sum_b a_scales[b,s] * w_scales[e,n/128,b] *
+ *                  sum_{k in block b} a[s,k] * w[e,n,k]       (fp32 accumulation)
+ *   BF16: Y[s,n] = sum_k a[s,k] * w[e,n,k]
+ * and the epilogue stores Y (STORE), applies silu(gate)*up (SWIGLU) or adds
+ * route_weights[r] * Y[s,:] to out[r / top_k, :] for r = sorted_route_ids[s]
+ * (SCATTER; out must be zeroed or hold a partial sum).
+ * Runs on tcgen05 tensor cores (TMEM accumulators, TMA-fed shared memory).
+ * ws: workspace of at least MOE_CTRL_BYTES (tile-queue counter, status). */
+moe_status_t moe_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* Standalone weighted scatter (unfused form of "Baseline: 7 kernels" item 7):
+ * out[t,n] = bf16( sum_j weights[t*top_k+j] * rows[route_slot[t*top_k+j], n] )
+ * with the sum in j order in fp32.  rows: f32 [M*top_k, N]; out: bf16 [M,N]. */
+moe_status_t moe_scatter(const float* rows, const int32_t* route_slot, const float* weights,
+                         int M, int N, int top_k, void* out, void* stream);
+
+/* Arguments of the fused forward. */
+typedef struct {
+  moe_dtype_t dtype;      /* FP8_E4M3: one grouped GEMM [E,N,K] with block scales;
+                             BF16: gated FFN, up [E,2N,K] + SwiGLU, down [E,K,N] */
+  int M;                  /* tokens */
+  int K;                  /* token feature size (the GEMM's contraction size;
+                             for BF16 also the output size) */
+  int N;                  /* FP8: output size; BF16: FFN intermediate size I */
+  int E, top_k;
+  float softcap;          /* 0 = off */
+  int renorm;             /* 1 = softmax over the selected top_k (default) */
+  const float* logits;    /* [M,E] f32 */
+  const void* x;          /* [M,K] bf16 */
+  const void* w;          /* FP8: e4m3 [E,N,K]; BF16: bf16 w_up [E,2N,K] (gate rows, then up rows) */
+  const float* w_scales;  /* FP8: [E,N/128,K/128] */
+  const void* w2;         /* BF16: bf16 w_down [E,K,N] */
+  int block_m;            /* rows per tile (0 = chosen from the shape) */
+  moe_sched_t sched;      /* tile scheduler of the grouped GEMMs */
+  int k_splits;           /* FP8: 0 = auto */
+  int use_graph;          /* 1: capture the launch sequence once per argument set and
+                             replay it as a CUDA graph; 0: plain launches */
+} moe_forward_args;
+
+/* Workspace bytes needed by moe_forward / moe_forward_host for these
+ * arguments (0 if the arguments are invalid). */
+size_t moe_workspace_size(const moe_forward_args* args);
+
+/* The tile rows (block_m) and FP8 K split that moe_forward uses for these
+ * arguments, so a caller can reproduce its grouped GEMM with
+ * moe_grouped_gemm (k_splits is 1 on the BF16 path). */
+moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k_splits);
+
+/* Fused forward: route -> layout -> quantise+gather (FP8) or gather (BF16)
+ * -> grouped GEMM(s) with the weighted scatter fused -> bf16 output.
+ * out: bf16 [M, N] (FP8) or [M, K] (BF16).  ws: device workspace of
+ * moe_workspace_size() bytes, 256-byte aligned, control block zeroed once.
+ * With use_graph = 1 the launch sequence is captured on first use for this
+ * argument set (pointers included) and replayed; when `stream` is already
+ * capturing, the kernels are launched directly into the caller's capture. */
+moe_status_t moe_forward(const moe_forward_args* args, void* out, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* The same forward for host-resident inputs: `host_logits` (f32 [M,E]) and
+ * `host_x` (bf16 [M,K]) are copied into the workspace, the forward runs, and
+ * the bf16 result is copied to `host_out`, all enqueued on `stream` (pinned
+ * host memory makes the copies asynchronous).  args->logits and args->x are
+ * ignored; the weights stay device pointers. */
+moe_status_t moe_forward_host(const moe_forward_args* args, const float* host_logits,
+                              const void* host_x, void* host_out, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* Waits for `stream`, reads the workspace's device status word into *status
+ * and clears it. */
+moe_status_t moe_get_error(void* ws, moe_status_t* status, void* stream);
+
+/* Test hook for failure detection: when `drop_producer` is nonzero, the next
+ * moe_grouped_gemm launches issue no loads, so every consumer wait runs into
+ * its time limit of `timeout_ns` nanoseconds and the kernel exits with
+ * MOE_ERR_TIMEOUT in the status word instead of hanging.  timeout_ns = 0
+ * restores the default limit (2 s); drop_producer = 0 restores normal runs. */
+moe_status_t moe_debug_set_pipeline_fault(int drop_producer, uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H_ */

@@ -1,0 +1,521 @@
+// Persistent grouped GEMM on tcgen05 tensor cores (sm_103a).
+//
+// What it computes: "Fused MoE FP8: 8.09 -> 13.18 TFLOPS (1.63x)", section
+// "Baseline: 7 kernels" item 6 (grouped FP8 GEMM with 128x128 weight blocks
+// and 1x128 activation blocks; the blockwise scales are applied per 128-deep
+// K block), with item 7 (routing-weighted scatter-add to token order) fused
+// into the epilogue as in section "Fusion 1" / "Register-Direct Scatter
+// Epilogue".  Scheduling follows section 2.2 of the blog retelling of "Weave":
+// a fixed set of persistent CTAs pulls tiles from one global atomic counter;
+// the tile order is N-tile-minor so tiles that share a block of routed rows
+// run back to back (section "Grid Swap").
+//
+// How (this design, not the pages'): the MMA is "swap-AB" — the 128 weight
+// rows of a tile are the MMA's M side and the routed rows (block_m of them,
+// 16..256) are its N side, so a 4-row expert costs a 128x16 MMA instead of a
+// padded 128-row one and the kernel streams each touched weight block once.
+//   warp 0      TMA producer: tile queue, weight + activation tiles -> smem ring
+//   warp 1      one thread issues tcgen05.mma into TMEM, commits to mbarriers;
+//               the warp owns the TMEM allocation
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (thread = weight row),
+//               FP8: per K block, acc += partial * (a_scale * w_scale) in fp32
+//               registers ("promotion"; each K block has its own TMEM buffer),
+//               then weighted red.global.add into the fp32 output, a plain
+//               store, or silu(gate)*up to bf16.
+// Every wait is bounded (mbar_wait): on a time-out the CTA records
+// MOE_ERR_TIMEOUT in the workspace status word, raises a shared abort flag so
+// the other roles stop too, waits (bounded) for its own in-flight copies and
+// MMAs, frees its TMEM and returns.
+#include <cuda_bf16.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTileN = 128;           // weight rows per tile (MMA M)
+constexpr int kRowBytes = 128;        // bytes per K block row (one swizzle atom row)
+constexpr int kATileBytes = kTileN * kRowBytes;
+constexpr int kMaxStages = 16;
+constexpr int kRing = 4;              // tile descriptors in flight
+constexpr int kThreads = 192;
+constexpr int kMaxE = 1024;
+
+struct TileDesc {
+  int e, m0, rows, n_tile, kb0, nkb;
+};
+
+template <int BM, bool kFP8, int kEpi>
+struct Cfg {
+  static constexpr bool kSwiglu = kEpi == MOE_EPI_SWIGLU;
+  static constexpr int kAccCols = kSwiglu ? 2 * BM : BM;
+  static constexpr int kNumAcc = kFP8 ? (512 / BM < 8 ? 512 / BM : 8)
+                                      : (512 / kAccCols >= 2 ? 2 : 1);
+  static constexpr int kTmemNeed = kNumAcc * kAccCols;
+  static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
+                                 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
+  static constexpr int kATiles = kSwiglu ? 2 : 1;
+  static constexpr int kStageBytes = kATiles * kATileBytes + BM * kRowBytes;
+  static_assert(BM % 16 == 0 && BM >= 16 && BM <= 256, "block_m");
+  static_assert(!kFP8 || BM <= 128, "FP8 block_m <= 128");
+  static_assert(kTmemNeed <= 512, "TMEM");
+};
+
+__device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const int* s_tile_off,
+                                            int BM, TileDesc& d) {
+  const int per_m = p.n_tiles * p.k_splits;
+  const int mt = t / per_m;
+  const int r = t - mt * per_m;
+  // expert: last e with tile_off[e] <= mt
+  int lo = 0, hi = p.E;  // invariant: tile_off[lo] <= mt < tile_off[hi]
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (s_tile_off[mid] <= mt) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int seg_begin = __ldg(p.offsets + e), seg_end = __ldg(p.offsets + e + 1);
+  d.e = e;
+  d.m0 = seg_begin + (mt - s_tile_off[e]) * BM;
+  d.rows = min(BM, seg_end - d.m0);
+  d.n_tile = r / p.k_splits;
+  const int ks = r - d.n_tile * p.k_splits;
+  d.kb0 = ks * p.kb_per_split;
+  d.nkb = min(p.kb_per_split, p.KB - d.kb0);
+}
+
+template <int BM, bool kFP8, int kEpi>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                        const __grid_constant__ CUtensorMap tmap_a, const GemmParams p) {
+  using C = Cfg<BM, kFP8, kEpi>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_tfull[C::kNumAcc], bar_tempty[C::kNumAcc];
+  __shared__ __align__(8) uint64_t bar_dfull[kRing], bar_dempty[kRing], bar_drain;
+  __shared__ TileDesc s_desc[kRing];
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ int s_tile_off[kMaxE + 1];
+  __shared__ int s_tok[BM];
+  __shared__ float s_wt[BM];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
+  float* s_scale = reinterpret_cast<float*>(smem_gen + p.num_stages * C::kStageBytes);
+  const int NST = p.num_stages;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(smem_u32(&bar_full[i]), 1);
+      mbar_init(smem_u32(&bar_empty[i]), 1);
+    }
+    for (int i = 0; i < C::kNumAcc; ++i) {
+      mbar_init(smem_u32(&bar_tfull[i]), 1);
+      mbar_init(smem_u32(&bar_tempty[i]), 4);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(smem_u32(&bar_dfull[i]), 1);
+      mbar_init(smem_u32(&bar_dempty[i]), 5);
+    }
+    mbar_init(smem_u32(&bar_drain), 1);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_w);
+    tma_prefetch_desc(&tmap_a);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
+    tmem_relinquish();
+  }
+  // Everything above is independent of the preceding kernel's results.
+  pdl_wait();
+  for (int i = threadIdx.x; i <= p.E; i += kThreads) s_tile_off[i] = __ldg(p.tile_offsets + i);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+  const int total_tiles = s_tile_off[p.E] * p.n_tiles * p.k_splits;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_a = policy_evict_last();
+      int stage = 0, ds = 0;
+      uint32_t phase = 0, dphase = 0;
+      bool ok = true;
+      // static schedule state: experts handled by this CTA
+      const int G = gridDim.x, c = blockIdx.x;
+      int st_e = p.E >= 1 ? (G >= p.E ? c % p.E : c) : 0;
+      const int st_idx = G >= p.E ? c / p.E : 0;
+      const int st_stride = G >= p.E ? (G - (c % p.E) + p.E - 1) / p.E : 1;
+      int st_lt = st_idx;
+      for (;;) {
+        int t;
+        if (p.sched == MOE_SCHED_QUEUE) {
+          t = static_cast<int>(atomicAdd(p.queue_ctr, 1u));
+          if (t >= total_tiles) t = -1;
+        } else {
+          t = -1;
+          while (st_e < p.E) {
+            const int per_e = (s_tile_off[st_e + 1] - s_tile_off[st_e]) * p.n_tiles * p.k_splits;
+            if (st_lt < per_e) {
+              t = s_tile_off[st_e] * p.n_tiles * p.k_splits + st_lt;
+              st_lt += st_stride;
+              break;
+            }
+            if (G >= p.E) { st_e = p.E; break; }
+            st_e += G;
+            st_lt = 0;
+          }
+        }
+        TileDesc d;
+        if (t >= 0) {
+          decode_tile(t, p, s_tile_off, BM, d);
+          if (d.rows <= 0 || d.nkb <= 0) continue;
+        } else {
+          d.nkb = -1;
+        }
+        if (!mbar_wait(smem_u32(&bar_dempty[ds]), dphase ^ 1u, &s_abort, tmo)) { ok = false; break; }
+        s_desc[ds] = d;
+        mbar_arrive(smem_u32(&bar_dfull[ds]));
+        if (++ds == kRing) { ds = 0; dphase ^= 1u; }
+        if (t < 0) break;
+        const int w_row = d.e * p.N + d.n_tile * kTileN;
+        for (int i = 0; i < d.nkb; ++i) {
+          if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, tmo)) { ok = false; break; }
+          if (!p.drop_producer) {
+            const uint32_t full = smem_u32(&bar_full[stage]);
+            const uint32_t sa = smem_base + stage * C::kStageBytes;
+            const int kc = (d.kb0 + i) * (kFP8 ? kRowBytes : kRowBytes / 2);  // element coordinate
+            mbar_arrive_expect_tx(full, C::kStageBytes);
+            tma_load_2d(sa, &tmap_w, full, kc, w_row, pol_w);
+            if constexpr (C::kSwiglu)
+              tma_load_2d(sa + kATileBytes, &tmap_w, full, kc, w_row + p.N / 2, pol_w);
+            tma_load_2d(sa + C::kATiles * kATileBytes, &tmap_a, full, kc, d.m0, pol_a);
+          }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      if (!ok) {
+        set_error(p.ctrl, MOE_ERR_TIMEOUT, 1);
+        s_abort = 1;
+      }
+      // Wait (bounded) until every load this thread issued has landed: a
+      // stage's last fill has completed once its "full" phase has flipped.
+      if (!p.drop_producer) {
+        for (int i = 0; i < NST; ++i) {
+          // stages [0, stage) were filled in the current pass, the rest in the previous one
+          const uint32_t par = (i < stage) ? phase : phase ^ 1u;
+          mbar_wait(smem_u32(&bar_full[i]), par, &s_abort, tmo);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(kFP8 ? 0u : 1u, 128u, static_cast<uint32_t>(BM));
+      int stage = 0, ds = 0, acc_n = 0;
+      uint32_t phase = 0, dphase = 0;
+      bool ok = true;
+      for (;;) {
+        if (!mbar_wait(smem_u32(&bar_dfull[ds]), dphase, &s_abort, tmo)) { ok = false; break; }
+        const TileDesc d = s_desc[ds];
+        mbar_arrive(smem_u32(&bar_dempty[ds]));
+        if (++ds == kRing) { ds = 0; dphase ^= 1u; }
+        if (d.nkb < 0) break;
+        int buf = 0;
+        for (int i = 0; i < d.nkb; ++i) {
+          if (kFP8 || i == 0) {
+            buf = acc_n % C::kNumAcc;
+            const uint32_t use = static_cast<uint32_t>(acc_n / C::kNumAcc);
+            if (!mbar_wait(smem_u32(&bar_tempty[buf]), (use & 1u) ^ 1u, &s_abort, tmo)) { ok = false; break; }
+            tc_fence_after();
+          }
+          if (!mbar_wait(smem_u32(&bar_full[stage]), phase, &s_abort, tmo)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_base + stage * C::kStageBytes;
+          const uint32_t b_addr = a_addr + C::kATiles * kATileBytes;
+          const uint32_t d_tmem = tmem_base + buf * C::kAccCols;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t acc = kFP8 ? (kk > 0) : (i > 0 || kk > 0);
+            const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32);
+            umma<kFP8>(d_tmem, smem_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
+            if constexpr (C::kSwiglu)
+              umma<kFP8>(d_tmem + BM, smem_desc_sw128(a_addr + kATileBytes + kk * 32), bdesc, idesc,
+                         acc);
+          }
+          umma_commit(smem_u32(&bar_empty[stage]));
+          if (kFP8 || i == d.nkb - 1) {
+            umma_commit(smem_u32(&bar_tfull[buf]));
+            ++acc_n;
+          }
+          if (++stage == NST) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      if (!ok) {
+        set_error(p.ctrl, MOE_ERR_TIMEOUT, 2);
+        s_abort = 1;
+      }
+      // drain: every MMA issued above has completed before TMEM is freed
+      umma_commit(smem_u32(&bar_drain));
+      mbar_wait(smem_u32(&bar_drain), 0u, &s_abort, tmo);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;               // 0..127
+    const int quad = warp & 3;                     // TMEM lane quadrant of this warp
+    const int row = quad * 32 + lane;              // weight row within the tile
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    int ds = 0, acc_n = 0;
+    uint32_t dphase = 0;
+    bool ok = true;
+    const int NB = p.N / kTileN;
+    for (;;) {
+      // every lane waits; the warp proceeds only if all lanes saw the phase
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_dfull[ds]), dphase, &s_abort, tmo))) {
+        ok = false;
+        break;
+      }
+      const TileDesc d = s_desc[ds];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_dempty[ds]));
+      if (++ds == kRing) { ds = 0; dphase ^= 1u; }
+      if (d.nkb < 0) break;
+
+      // per-tile metadata in shared memory
+      named_bar_sync(1, 128);
+      if constexpr (kEpi == MOE_EPI_SCATTER) {
+        for (int s = et; s < BM; s += 128) {
+          int tok = -1;
+          float wt = 0.0f;
+          if (s < d.rows) {
+            const int r = __ldg(p.sorted_route_ids + d.m0 + s);
+            tok = r / p.top_k;
+            wt = __ldg(p.route_weights + r);
+          }
+          s_tok[s] = tok;
+          s_wt[s] = wt;
+        }
+      }
+      if constexpr (kFP8) {
+        const float* wsc = p.w_scales + (static_cast<size_t>(d.e) * NB + d.n_tile) * p.KB + d.kb0;
+        for (int idx = et; idx < d.nkb * BM; idx += 128) {
+          const int kb = idx / BM, s = idx - kb * BM;
+          float v = 0.0f;
+          if (s < d.rows)
+            v = __ldg(p.a_scales + static_cast<size_t>(d.kb0 + kb) * p.R + d.m0 + s) * __ldg(wsc + kb);
+          s_scale[idx] = v;
+        }
+      }
+      named_bar_sync(1, 128);
+
+      if constexpr (kFP8) {
+        float acc[BM];
+#pragma unroll
+        for (int s = 0; s < BM; ++s) acc[s] = 0.0f;
+        for (int i = 0; i < d.nkb; ++i) {
+          const int buf = acc_n % C::kNumAcc;
+          const uint32_t use = static_cast<uint32_t>(acc_n / C::kNumAcc);
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&bar_tfull[buf]), use & 1u, &s_abort, tmo))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float* sc = s_scale + i * BM;
+#pragma unroll
+          for (int c0 = 0; c0 < BM; c0 += 16) {
+            float v[16];
+            tmem_ld16(lane_addr + buf * C::kAccCols + c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(v[j], sc[c0 + j], acc[c0 + j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[buf]));
+          ++acc_n;
+        }
+        if (!ok) break;
+        const int col = d.n_tile * kTileN + row;
+        if constexpr (kEpi == MOE_EPI_SCATTER) {
+          float* out = static_cast<float*>(p.out);
+#pragma unroll
+          for (int s = 0; s < BM; ++s) {
+            if (s < d.rows) red_add_f32(out + static_cast<size_t>(s_tok[s]) * p.N + col, s_wt[s] * acc[s]);
+          }
+        } else {
+          float* out = static_cast<float*>(p.out);
+#pragma unroll
+          for (int s = 0; s < BM; ++s) {
+            if (s < d.rows) out[static_cast<size_t>(d.m0 + s) * p.N + col] = acc[s];
+          }
+        }
+      } else {
+        const int buf = acc_n % C::kNumAcc;
+        const uint32_t use = static_cast<uint32_t>(acc_n / C::kNumAcc);
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&bar_tfull[buf]), use & 1u, &s_abort, tmo))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int col = d.n_tile * kTileN + row;
+        for (int c0 = 0; c0 < BM && c0 < d.rows; c0 += 16) {
+          float v[16];
+          tmem_ld16(lane_addr + buf * C::kAccCols + c0, v);
+          if constexpr (C::kSwiglu) {
+            float u[16];
+            tmem_ld16(lane_addr + buf * C::kAccCols + BM + c0, u);
+            tmem_ld_wait();
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+            const int I = p.N / 2;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (c0 + j < d.rows) {
+                const float g = v[j];
+                const float h = __fdiv_rn(g, 1.0f + expf(-g)) * u[j];
+                out[static_cast<size_t>(d.m0 + c0 + j) * I + col] = __float2bfloat16_rn(h);
+              }
+            }
+          } else {
+            tmem_ld_wait();
+            float* out = static_cast<float*>(p.out);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (c0 + j < d.rows) {
+                if constexpr (kEpi == MOE_EPI_SCATTER)
+                  red_add_f32(out + static_cast<size_t>(s_tok[c0 + j]) * p.N + col,
+                              s_wt[c0 + j] * v[j]);
+                else
+                  out[static_cast<size_t>(d.m0 + c0 + j) * p.N + col] = v[j];
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[buf]));
+        ++acc_n;
+      }
+    }
+    if (!ok) {
+      set_error(p.ctrl, MOE_ERR_TIMEOUT, 3);
+      s_abort = 1;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  pdl_launch_dependents();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.done_ctr, 1u);
+    if (prev == gridDim.x - 1) {  // last CTA: leave the counters zeroed for the next launch
+      atomicExch(p.queue_ctr, 0u);
+      atomicExch(p.done_ctr, 0u);
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Host side: instantiations, launch.
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, GemmParams);
+
+struct GemmVariant {
+  const void* fn;
+  int stage_bytes;
+};
+
+template <int BM, bool kFP8, int kEpi>
+GemmVariant variant() {
+  using C = Cfg<BM, kFP8, kEpi>;
+  return GemmVariant{reinterpret_cast<const void*>(&grouped_gemm_kernel<BM, kFP8, kEpi>),
+                     C::kStageBytes};
+}
+
+template <bool kFP8, int kEpi>
+bool pick_bm(int bm, GemmVariant& v) {
+  switch (bm) {
+    case 16: v = variant<16, kFP8, kEpi>(); return true;
+    case 32: v = variant<32, kFP8, kEpi>(); return true;
+    case 64: v = variant<64, kFP8, kEpi>(); return true;
+    case 128: v = variant<128, kFP8, kEpi>(); return true;
+    default: break;
+  }
+  if constexpr (!kFP8) {
+    if (bm == 256) { v = variant<256, kFP8, kEpi>(); return true; }
+  }
+  return false;
+}
+
+bool select_gemm_variant(bool fp8, int epi, int bm, GemmVariant& v) {
+  if (fp8) {
+    if (epi == MOE_EPI_SCATTER) return pick_bm<true, MOE_EPI_SCATTER>(bm, v);
+    if (epi == MOE_EPI_STORE) return pick_bm<true, MOE_EPI_STORE>(bm, v);
+    return false;
+  }
+  if (epi == MOE_EPI_SCATTER) return pick_bm<false, MOE_EPI_SCATTER>(bm, v);
+  if (epi == MOE_EPI_STORE) return pick_bm<false, MOE_EPI_STORE>(bm, v);
+  if (epi == MOE_EPI_SWIGLU) return pick_bm<false, MOE_EPI_SWIGLU>(bm, v);
+  return false;
+}
+
+constexpr int kSmemLimit = 232448;  // 227 KB per CTA
+
+int gemm_num_stages(int stage_bytes, int scale_bytes) {
+  int avail = kSmemLimit - 1024 - scale_bytes - 8192;  // alignment slack + static shared memory
+  int n = avail / stage_bytes;
+  return n > kMaxStages ? kMaxStages : n;
+}
+
+cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_a,
+                                const GemmParams& p, bool fp8, int epi, int bm, int num_ctas,
+                                cudaStream_t stream, bool pdl) {
+  GemmVariant v;
+  if (!select_gemm_variant(fp8, epi, bm, v)) return cudaErrorInvalidValue;
+  const int scale_bytes = fp8 ? p.kb_per_split * bm * 4 : 0;
+  const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * v.stage_bytes + scale_bytes;
+  cudaError_t err = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {const_cast<CUtensorMap*>(&tmap_w), const_cast<CUtensorMap*>(&tmap_a),
+                  const_cast<GemmParams*>(&p)};
+  return cudaLaunchKernelExC(&cfg, v.fn, args);
+}
+
+int gemm_stage_bytes(bool fp8, int epi, int bm) {
+  GemmVariant v;
+  if (!select_gemm_variant(fp8, epi, bm, v)) return 0;
+  return v.stage_bytes;
+}
+
+}  // namespace moe

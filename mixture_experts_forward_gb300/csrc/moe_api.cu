@@ -1,0 +1,570 @@
+// C ABI of the fused MoE forward: argument checks, TMA descriptors, workspace
+// layout, the launch sequence of the forward and its CUDA-graph cache.
+//
+// The forward is the serving path of "Fused MoE FP8: 8.09 -> 13.18 TFLOPS
+// (1.63x)" (section "Phase 2": no host synchronisation between launches, the
+// launch sequence captured once into a CUDA graph and replayed), extended with
+// the router in front and a bf16 finalize at the end.  Consecutive kernels are
+// chained with programmatic dependent launch (the PDL idea of section 2.3 of
+// the Weave retelling): each kernel's prologue overlaps its predecessor's tail
+// and its griddepcontrol.wait orders the data.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
+int g_drop_producer = 0;
+unsigned long long g_timeout_ns = kDefaultTimeoutNs;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int device_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D K-major tensor map: rows of `inner` elements, `outer` rows, 128-byte
+// swizzle, box = 128 bytes x box_rows; out-of-range rows read as zero.
+bool make_tmap(CUtensorMap* m, const void* base, bool fp8, uint64_t inner, uint64_t outer,
+               uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const uint32_t esize = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {128u / esize, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int auto_block_m(bool fp8, long long R, int E) {
+  const long long avg = (R + E - 1) / E;
+  if (avg <= 16) return 16;
+  if (avg <= 32) return 32;
+  if (avg <= 64) return 64;
+  if (fp8 || avg <= 128) return 128;
+  return 256;
+}
+
+// Host checks shared by moe_grouped_gemm and the forward.
+moe_status_t check_gemm(const moe_gemm_args* a) {
+  if (a == nullptr) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = a->dtype == MOE_DTYPE_FP8_E4M3;
+  if (a->dtype != MOE_DTYPE_FP8_E4M3 && a->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (a->epilogue < MOE_EPI_SCATTER || a->epilogue > MOE_EPI_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (a->sched != MOE_SCHED_QUEUE && a->sched != MOE_SCHED_STATIC) return MOE_ERR_INVALID_ARG;
+  if (a->E <= 0 || a->N <= 0 || a->K <= 0 || a->R <= 0) return MOE_ERR_INVALID_ARG;
+  if (a->a == nullptr || a->w == nullptr || a->offsets == nullptr || a->tile_offsets == nullptr ||
+      a->out == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a->a) || !aligned16(a->w) || !aligned16(a->out)) return MOE_ERR_INVALID_ARG;
+  if (a->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (a->block_m < 16 || a->block_m > 256 || a->block_m % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((a->block_m & (a->block_m - 1)) != 0) return MOE_ERR_UNSUPPORTED;
+  if (a->N % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (fp8) {
+    if (a->K % 128 != 0 || a->block_m > 128) return MOE_ERR_UNSUPPORTED;
+    if (a->epilogue == MOE_EPI_SWIGLU) return MOE_ERR_UNSUPPORTED;
+    if (a->a_scales == nullptr || a->w_scales == nullptr) return MOE_ERR_INVALID_ARG;
+  } else {
+    if (a->K % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    if (a->epilogue == MOE_EPI_SWIGLU && a->N % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  }
+  if (a->epilogue == MOE_EPI_SCATTER) {
+    if (a->sorted_route_ids == nullptr || a->route_weights == nullptr) return MOE_ERR_INVALID_ARG;
+    if (a->M <= 0 || a->top_k <= 0 || static_cast<long long>(a->M) * a->top_k != a->R)
+      return MOE_ERR_INVALID_ARG;
+  }
+  if (a->k_splits < 0) return MOE_ERR_INVALID_ARG;
+  if (a->k_splits > 1 && !(fp8 && a->epilogue == MOE_EPI_SCATTER)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int pick_k_splits(const moe_gemm_args* a, int sms, int KB) {
+  if (a->k_splits > 0) return a->k_splits > KB ? KB : a->k_splits;
+  if (!(a->dtype == MOE_DTYPE_FP8_E4M3 && a->epilogue == MOE_EPI_SCATTER)) return 1;
+  // Upper bound of the tile count (every row in its own expert's ragged tile).
+  const long long tiles =
+      ((static_cast<long long>(a->R) + a->block_m - 1) / a->block_m + a->E) * (a->N / 128);
+  int ks = 1;
+  while (tiles * ks < 4LL * sms && ks * 2 <= KB / 4) ks *= 2;
+  return ks;
+}
+
+moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStream_t stream,
+                      bool pdl) {
+  const bool fp8 = a->dtype == MOE_DTYPE_FP8_E4M3;
+  const int sms = device_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  CUtensorMap tw, ta;
+  if (!make_tmap(&tw, a->w, fp8, static_cast<uint64_t>(a->K),
+                 static_cast<uint64_t>(a->E) * a->N, 128u))
+    return MOE_ERR_CUDA;
+  if (!make_tmap(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->R),
+                 static_cast<uint32_t>(a->block_m)))
+    return MOE_ERR_CUDA;
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.a_scales = a->a_scales;
+  p.w_scales = a->w_scales;
+  p.offsets = a->offsets;
+  p.tile_offsets = a->tile_offsets;
+  p.sorted_route_ids = a->sorted_route_ids;
+  p.route_weights = a->route_weights;
+  p.out = a->out;
+  p.ctrl = ctrl;
+  p.queue_ctr = second ? &ctrl->queue2 : &ctrl->queue;
+  p.done_ctr = second ? &ctrl->done2 : &ctrl->done;
+  p.E = a->E;
+  p.N = a->N;
+  p.K = a->K;
+  p.R = a->R;
+  p.top_k = a->top_k;
+  p.KB = fp8 ? a->K / 128 : a->K / 64;
+  p.k_splits = pick_k_splits(a, sms, p.KB);
+  p.kb_per_split = (p.KB + p.k_splits - 1) / p.k_splits;
+  p.n_tiles = (a->epilogue == MOE_EPI_SWIGLU ? a->N / 2 : a->N) / 128;
+  p.sched = a->sched;
+  p.drop_producer = g_drop_producer;
+  p.timeout_ns = g_timeout_ns;
+  const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m);
+  if (stage_bytes <= 0) return MOE_ERR_UNSUPPORTED;
+  const int scale_bytes = fp8 ? p.kb_per_split * a->block_m * 4 : 0;
+  int stages = (232448 - 1024 - 12288 - scale_bytes) / stage_bytes;
+  if (stages > 16) stages = 16;
+  if (stages < 2) return MOE_ERR_UNSUPPORTED;
+  p.num_stages = stages;
+  const int ctas = a->num_ctas > 0 ? a->num_ctas : sms;
+  return cuda_status(launch_grouped_gemm(tw, ta, p, fp8, a->epilogue, a->block_m, ctas, stream,
+                                         pdl));
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout of the forward.
+struct WsLayout {
+  size_t ctrl, ids, weights, counts, offsets, tile_off, sorted, slot, a, a_scales, acc, h;
+  size_t st_logits, st_x, st_out;
+  size_t total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool forward_shape_ok(const moe_forward_args* f) {
+  return f != nullptr && f->M > 0 && f->K > 0 && f->N > 0 && f->E > 0 && f->top_k > 0;
+}
+
+WsLayout ws_layout(const moe_forward_args* f) {
+  WsLayout L;
+  std::memset(&L, 0, sizeof(L));
+  const bool fp8 = f->dtype == MOE_DTYPE_FP8_E4M3;
+  const size_t M = f->M, K = f->K, N = f->N, E = f->E, k = f->top_k, R = M * k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.ctrl = take(MOE_CTRL_BYTES);
+  L.ids = take(R * 4);
+  L.weights = take(R * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.tile_off = take((E + 1) * 4);
+  L.sorted = take(R * 4);
+  L.slot = take(R * 4);
+  L.a = take(fp8 ? R * K : R * K * 2);
+  L.a_scales = fp8 ? take((K / 128) * R * 4) : 0;
+  const size_t out_cols = fp8 ? N : K;
+  L.acc = take(M * out_cols * 4);
+  L.h = fp8 ? 0 : take(R * N * 2);
+  L.st_logits = take(M * E * 4);
+  L.st_x = take(M * K * 2);
+  L.st_out = take(M * out_cols * 2);
+  L.total = off;
+  return L;
+}
+
+moe_status_t check_forward(const moe_forward_args* f) {
+  if (!forward_shape_ok(f)) return MOE_ERR_INVALID_ARG;
+  if (f->dtype != MOE_DTYPE_FP8_E4M3 && f->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (f->sched != MOE_SCHED_QUEUE && f->sched != MOE_SCHED_STATIC) return MOE_ERR_INVALID_ARG;
+  if (f->w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (f->E > 1024 || f->top_k > 32 || f->top_k > f->E) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(f->M) * f->top_k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (f->K % 128 != 0 || f->N % 128 != 0 || f->K > 16384) return MOE_ERR_UNSUPPORTED;
+  if (!(f->softcap >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (f->block_m != 0 && (f->block_m < 16 || f->block_m > 256 || (f->block_m & (f->block_m - 1))))
+    return MOE_ERR_UNSUPPORTED;
+  if (f->dtype == MOE_DTYPE_FP8_E4M3) {
+    if (f->w_scales == nullptr) return MOE_ERR_INVALID_ARG;
+    if (f->block_m > 128) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (f->w2 == nullptr) return MOE_ERR_INVALID_ARG;
+  }
+  if (!aligned16(f->w) || (f->w2 && !aligned16(f->w2))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// The launch sequence of one forward (no host synchronisation).
+moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, const void* x,
+                             void* out, uint8_t* ws, cudaStream_t stream) {
+  const bool fp8 = f->dtype == MOE_DTYPE_FP8_E4M3;
+  const WsLayout L = ws_layout(f);
+  const int M = f->M, K = f->K, N = f->N, E = f->E, k = f->top_k, R = M * k;
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws + L.ctrl);
+  int32_t* ids = reinterpret_cast<int32_t*>(ws + L.ids);
+  float* wts = reinterpret_cast<float*>(ws + L.weights);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* tile_off = reinterpret_cast<int32_t*>(ws + L.tile_off);
+  int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  int32_t* slot = reinterpret_cast<int32_t*>(ws + L.slot);
+  float* acc = reinterpret_cast<float*>(ws + L.acc);
+  const int bm = f->block_m > 0 ? f->block_m : auto_block_m(fp8, R, E);
+  const bool pdl = true;
+  cudaError_t e;
+
+  e = launch_route(logits, M, E, k, f->softcap, f->renorm, ids, wts, stream, false);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_layout(ids, R, E, bm, counts, offsets, sorted, slot, tile_off, ctrl, stream, pdl);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const int sms = device_sms();
+  if (fp8) {
+    uint8_t* a_q = ws + L.a;
+    float* a_s = reinterpret_cast<float*>(ws + L.a_scales);
+    e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, stream, pdl);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    moe_gemm_args g;
+    std::memset(&g, 0, sizeof(g));
+    g.dtype = MOE_DTYPE_FP8_E4M3;
+    g.epilogue = MOE_EPI_SCATTER;
+    g.sched = f->sched;
+    g.block_m = bm;
+    g.E = E;
+    g.N = N;
+    g.K = K;
+    g.R = R;
+    g.M = M;
+    g.top_k = k;
+    g.a = a_q;
+    g.a_scales = a_s;
+    g.w = f->w;
+    g.w_scales = f->w_scales;
+    g.offsets = offsets;
+    g.tile_offsets = tile_off;
+    g.sorted_route_ids = sorted;
+    g.route_weights = wts;
+    g.out = acc;
+    g.k_splits = f->k_splits;
+    moe_status_t s = run_gemm(&g, ctrl, false, stream, pdl);
+    if (s != MOE_OK) return s;
+    e = launch_finalize(acc, out, static_cast<size_t>(M) * N, sms, stream, pdl);
+    return cuda_status(e);
+  }
+  // BF16 gated FFN: gather -> up (SwiGLU) -> down (scatter) -> finalize
+  void* a = ws + L.a;
+  void* h = ws + L.h;
+  e = launch_gather_rows_bf16(x, M, K, k, slot, a, acc, K, stream, pdl);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  moe_gemm_args g;
+  std::memset(&g, 0, sizeof(g));
+  g.dtype = MOE_DTYPE_BF16;
+  g.epilogue = MOE_EPI_SWIGLU;
+  g.sched = f->sched;
+  g.block_m = bm;
+  g.E = E;
+  g.N = 2 * N;
+  g.K = K;
+  g.R = R;
+  g.M = M;
+  g.top_k = k;
+  g.a = a;
+  g.w = f->w;
+  g.offsets = offsets;
+  g.tile_offsets = tile_off;
+  g.out = h;
+  g.k_splits = 1;
+  moe_status_t s = run_gemm(&g, ctrl, false, stream, pdl);
+  if (s != MOE_OK) return s;
+  g.epilogue = MOE_EPI_SCATTER;
+  g.N = K;
+  g.K = N;
+  g.a = h;
+  g.w = f->w2;
+  g.sorted_route_ids = sorted;
+  g.route_weights = wts;
+  g.out = acc;
+  s = run_gemm(&g, ctrl, true, stream, pdl);
+  if (s != MOE_OK) return s;
+  e = launch_finalize(acc, out, static_cast<size_t>(M) * K, sms, stream, pdl);
+  return cuda_status(e);
+}
+
+// ---------------------------------------------------------------------------
+// Graph cache: one instantiated graph per (arguments, pointers, stream).
+struct GraphEntry {
+  moe_forward_args args;
+  const float* logits;
+  const void* x;
+  void* out;
+  void* ws;
+  cudaStream_t stream;
+  int device;
+  cudaGraphExec_t exec;
+};
+constexpr int kGraphCache = 32;
+GraphEntry g_graphs[kGraphCache];
+int g_graph_count = 0, g_graph_next = 0;
+std::mutex g_graph_mu;
+
+bool same_entry(const GraphEntry& g, const moe_forward_args* f, const float* logits, const void* x,
+                void* out, void* ws, cudaStream_t stream, int dev) {
+  return std::memcmp(&g.args, f, sizeof(*f)) == 0 && g.logits == logits && g.x == x &&
+         g.out == out && g.ws == ws && g.stream == stream && g.device == dev;
+}
+
+moe_status_t forward_impl(const moe_forward_args* f, const float* logits, const void* x, void* out,
+                          void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_status_t s = check_forward(f);
+  if (s != MOE_OK) return s;
+  if (logits == nullptr || x == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(f).total) return MOE_ERR_WORKSPACE;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!f->use_graph || cap != cudaStreamCaptureStatusNone)
+    return enqueue_forward(f, logits, x, out, w8, stream);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_graph_mu);
+  for (int i = 0; i < g_graph_count; ++i) {
+    if (same_entry(g_graphs[i], f, logits, x, out, ws, stream, dev))
+      return cuda_status(cudaGraphLaunch(g_graphs[i].exec, stream));
+  }
+  cudaGraph_t graph = nullptr;
+  if (cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_status_t es = enqueue_forward(f, logits, x, out, w8, stream);
+  cudaError_t ce = cudaStreamEndCapture(stream, &graph);
+  if (es != MOE_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return es;
+  }
+  if (ce != cudaSuccess) return MOE_ERR_CUDA;
+  cudaGraphExec_t exec = nullptr;
+  ce = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ce != cudaSuccess) return MOE_ERR_CUDA;
+  GraphEntry& slot = g_graphs[g_graph_next];
+  if (g_graph_count == kGraphCache) cudaGraphExecDestroy(slot.exec);
+  slot.args = *f;
+  slot.logits = logits;
+  slot.x = x;
+  slot.out = out;
+  slot.ws = ws;
+  slot.stream = stream;
+  slot.device = dev;
+  slot.exec = exec;
+  g_graph_next = (g_graph_next + 1) % kGraphCache;
+  if (g_graph_count < kGraphCache) ++g_graph_count;
+  return cuda_status(cudaGraphLaunch(exec, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case MOE_ERR_DEVICE_FAULT: return "invalid data found on the device";
+  }
+  return "unknown status";
+}
+
+int moe_num_sms(void) { return device_sms(); }
+
+moe_status_t moe_route(const float* logits, int M, int E, int top_k, float softcap, int renorm,
+                       int32_t* ids, float* weights, void* stream) {
+  if (logits == nullptr || ids == nullptr || weights == nullptr) return MOE_ERR_INVALID_ARG;
+  if (M <= 0 || E <= 0 || top_k <= 0 || !(softcap >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || top_k > 32 || top_k > E) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_route(logits, M, E, top_k, softcap, renorm, ids, weights,
+                                  static_cast<cudaStream_t>(stream), false));
+}
+
+moe_status_t moe_layout(const int32_t* ids, int M, int E, int top_k, int block_m, int32_t* counts,
+                        int32_t* offsets, int32_t* sorted_route_ids, int32_t* route_slot,
+                        int32_t* tile_offsets, void* ws, void* stream) {
+  if (ids == nullptr || counts == nullptr || offsets == nullptr || sorted_route_ids == nullptr ||
+      route_slot == nullptr || tile_offsets == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (M <= 0 || E <= 0 || top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (block_m < 16 || block_m > 256 || block_m % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(M) * top_k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_layout(ids, M * top_k, E, block_m, counts, offsets, sorted_route_ids,
+                                   route_slot, tile_offsets, static_cast<Ctrl*>(ws),
+                                   static_cast<cudaStream_t>(stream), false));
+}
+
+moe_status_t moe_quant_gather(const void* x, int M, int K, int top_k, const int32_t* route_slot,
+                              uint8_t* a_q, float* a_scales, float* zero_acc, int zero_cols,
+                              void* stream) {
+  if (x == nullptr || route_slot == nullptr || a_q == nullptr || a_scales == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (M <= 0 || K <= 0 || top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 128 != 0 || K > 16384 || top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(a_q)) return MOE_ERR_INVALID_ARG;
+  if (zero_acc != nullptr && (zero_cols <= 0 || zero_cols % 4 != 0 || !aligned16(zero_acc)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quant_gather(x, M, K, top_k, route_slot, a_q, a_scales, zero_acc,
+                                         zero_cols, static_cast<cudaStream_t>(stream), false));
+}
+
+moe_status_t moe_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t s = check_gemm(args);
+  if (s != MOE_OK) return s;
+  if (ws == nullptr || ws_bytes < MOE_CTRL_BYTES || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return MOE_ERR_WORKSPACE;
+  return run_gemm(args, static_cast<Ctrl*>(ws), false, static_cast<cudaStream_t>(stream), false);
+}
+
+moe_status_t moe_scatter(const float* rows, const int32_t* route_slot, const float* weights, int M,
+                         int N, int top_k, void* out, void* stream) {
+  if (rows == nullptr || route_slot == nullptr || weights == nullptr || out == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || top_k <= 0) return MOE_ERR_INVALID_ARG;
+  if (top_k > 32) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_scatter(rows, route_slot, weights, M, N, top_k, out,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_workspace_size(const moe_forward_args* args) {
+  if (check_forward(args) != MOE_OK) return 0;
+  return ws_layout(args).total;
+}
+
+moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k_splits) {
+  moe_status_t s = check_forward(args);
+  if (s != MOE_OK) return s;
+  if (block_m == nullptr || k_splits == nullptr) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = args->dtype == MOE_DTYPE_FP8_E4M3;
+  const int R = args->M * args->top_k;
+  *block_m = args->block_m > 0 ? args->block_m : auto_block_m(fp8, R, args->E);
+  *k_splits = 1;
+  if (fp8) {
+    moe_gemm_args g;
+    std::memset(&g, 0, sizeof(g));
+    g.dtype = MOE_DTYPE_FP8_E4M3;
+    g.epilogue = MOE_EPI_SCATTER;
+    g.block_m = *block_m;
+    g.E = args->E;
+    g.N = args->N;
+    g.K = args->K;
+    g.R = R;
+    g.k_splits = args->k_splits;
+    const int sms = device_sms();
+    *k_splits = pick_k_splits(&g, sms > 0 ? sms : 148, args->K / 128);
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(const moe_forward_args* args, void* out, void* ws, size_t ws_bytes,
+                         void* stream) {
+  if (args == nullptr) return MOE_ERR_INVALID_ARG;
+  return forward_impl(args, args->logits, args->x, out, ws, ws_bytes,
+                      static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_forward_host(const moe_forward_args* args, const float* host_logits,
+                              const void* host_x, void* host_out, void* ws, size_t ws_bytes,
+                              void* stream) {
+  moe_status_t s = check_forward(args);
+  if (s != MOE_OK) return s;
+  if (host_logits == nullptr || host_x == nullptr || host_out == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(args);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  const size_t M = args->M;
+  const size_t out_cols = args->dtype == MOE_DTYPE_FP8_E4M3 ? args->N : args->K;
+  if (cudaMemcpyAsync(w8 + L.st_logits, host_logits, M * args->E * 4, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(w8 + L.st_x, host_x, M * args->K * 2, cudaMemcpyHostToDevice, st) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  s = forward_impl(args, reinterpret_cast<const float*>(w8 + L.st_logits), w8 + L.st_x,
+                   w8 + L.st_out, ws, ws_bytes, st);
+  if (s != MOE_OK) return s;
+  return cuda_status(
+      cudaMemcpyAsync(host_out, w8 + L.st_out, M * out_cols * 2, cudaMemcpyDeviceToHost, st));
+}
+
+moe_status_t moe_get_error(void* ws, moe_status_t* status, void* stream) {
+  if (ws == nullptr || status == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  Ctrl* c = static_cast<Ctrl*>(ws);
+  if (cudaMemcpy(&v, &c->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemset(&c->status, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = static_cast<moe_status_t>(v);
+  return MOE_OK;
+}
+
+moe_status_t moe_debug_set_pipeline_fault(int drop_producer, uint64_t timeout_ns) {
+  g_drop_producer = drop_producer ? 1 : 0;
+  g_timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,124 @@
+"""The C-ABI library loads without a GPU, exports every entry point that
+include/moe.h declares, and rejects bad arguments on the host before any
+CUDA call (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_forward_gb300 import _lib as L
+from mixture_experts_forward_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return L.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_pipeline():
+    names = declared_functions()
+    for n in ("moe_route", "moe_layout", "moe_quant_gather", "moe_grouped_gemm", "moe_scatter",
+              "moe_forward"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(L.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert L.status_string(code)
+
+
+FAKE = 1 << 20  # a non-null, aligned fake device address; never dereferenced
+
+
+def test_route_argument_errors(lib):
+    P = ctypes.c_void_p
+    assert lib.moe_route(None, 4, 8, 2, 0.0, 1, P(FAKE), P(FAKE), None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(P(FAKE), 4, 8, 9, 0.0, 1, P(FAKE), P(FAKE), None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(P(FAKE), 4, 2000, 2, 0.0, 1, P(FAKE), P(FAKE), None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(P(FAKE), 4, 64, 33, 0.0, 1, P(FAKE), P(FAKE), None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(P(FAKE), 0, 8, 2, 0.0, 1, P(FAKE), P(FAKE), None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(P(FAKE), 4, 8, 2, -1.0, 1, P(FAKE), P(FAKE), None) == L.MOE_ERR_INVALID_ARG
+
+
+def test_layout_and_quant_argument_errors(lib):
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    assert lib.moe_layout(f, 4, 8, 2, 24, f, f, f, f, f, f, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_layout(f, 4, 8, 2, 16, f, f, f, f, f, None, None) == L.MOE_ERR_WORKSPACE
+    assert lib.moe_layout(f, 4, 8, 2, 16, f, f, f, f, f, P(FAKE + 16), None) == L.MOE_ERR_WORKSPACE
+    assert lib.moe_quant_gather(f, 4, 200, 2, f, f, f, None, 0, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_quant_gather(P(FAKE + 4), 4, 256, 2, f, f, f, None, 0, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_gather(f, 4, 256, 2, f, f, f, f, 6, None) == L.MOE_ERR_INVALID_ARG
+
+
+def _gemm(**kw):
+    base = dict(dtype=L.DTYPE_FP8, epilogue=L.EPI_SCATTER, sched=L.SCHED_QUEUE, block_m=16, E=8,
+                N=256, K=256, R=32, M=16, top_k=2, a=FAKE, a_scales=FAKE, w=FAKE, w_scales=FAKE,
+                offsets=FAKE, tile_offsets=FAKE, sorted_route_ids=FAKE, route_weights=FAKE,
+                out=FAKE, k_splits=0, num_ctas=0)
+    base.update(kw)
+    return L.GemmArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(block_m=24), L.MOE_ERR_UNSUPPORTED), (dict(block_m=256), L.MOE_ERR_UNSUPPORTED),
+    (dict(K=200), L.MOE_ERR_UNSUPPORTED), (dict(N=200), L.MOE_ERR_UNSUPPORTED),
+    (dict(E=2000), L.MOE_ERR_UNSUPPORTED), (dict(epilogue=L.EPI_SWIGLU), L.MOE_ERR_UNSUPPORTED),
+    (dict(a=None), L.MOE_ERR_INVALID_ARG), (dict(a_scales=None), L.MOE_ERR_INVALID_ARG),
+    (dict(R=33), L.MOE_ERR_INVALID_ARG), (dict(sorted_route_ids=None), L.MOE_ERR_INVALID_ARG),
+    (dict(epilogue=L.EPI_STORE, k_splits=2), L.MOE_ERR_UNSUPPORTED),
+    (dict(dtype=7), L.MOE_ERR_INVALID_ARG), (dict(out=FAKE + 8), L.MOE_ERR_INVALID_ARG),
+    (dict(dtype=L.DTYPE_BF16, epilogue=L.EPI_SWIGLU, N=384), L.MOE_ERR_UNSUPPORTED),
+])
+def test_gemm_argument_errors(lib, kw, code):
+    g = _gemm(**kw)
+    assert lib.moe_grouped_gemm(ctypes.byref(g), ctypes.c_void_p(FAKE), 4096, None) == code
+
+
+def test_gemm_workspace_errors(lib):
+    g = _gemm()
+    assert lib.moe_grouped_gemm(ctypes.byref(g), None, 4096, None) == L.MOE_ERR_WORKSPACE
+    assert lib.moe_grouped_gemm(ctypes.byref(g), ctypes.c_void_p(FAKE), 100, None) == L.MOE_ERR_WORKSPACE
+
+
+def test_workspace_size_and_forward_errors(lib):
+    a = L.forward_args(dtype=L.DTYPE_FP8, M=128, K=2048, N=512, E=256, top_k=8, softcap=30.0)
+    a.w = FAKE
+    a.w_scales = FAKE
+    n = L.workspace_size(a)
+    R = 128 * 8
+    assert n >= R * 2048 + 16 * R * 4 + 128 * 512 * 4      # codes, scales, accumulator
+    a2 = L.forward_args(dtype=L.DTYPE_FP8, M=256, K=2048, N=512, E=256, top_k=8)
+    a2.w = FAKE
+    a2.w_scales = FAKE
+    assert L.workspace_size(a2) > n
+    bad = L.forward_args(dtype=L.DTYPE_FP8, M=128, K=2000, N=512, E=256, top_k=8)
+    bad.w = FAKE
+    bad.w_scales = FAKE
+    assert lib.moe_workspace_size(ctypes.byref(bad)) == 0
+    a.logits = FAKE
+    a.x = FAKE
+    assert lib.moe_forward(ctypes.byref(a), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 16,
+                           None) == L.MOE_ERR_WORKSPACE
+    bf = L.forward_args(dtype=L.DTYPE_BF16, M=64, K=256, N=256, E=4, top_k=2)
+    bf.w = FAKE
+    assert lib.moe_workspace_size(ctypes.byref(bf)) == 0        # w2 missing
+    bf.w2 = FAKE
+    assert lib.moe_workspace_size(ctypes.byref(bf)) > 0
