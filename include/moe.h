@@ -71,6 +71,10 @@ const char* moe_status_string(moe_status_t s);
 /* Number of streaming multiprocessors of the current device (0 on error). */
 int moe_num_sms(void);
 
+/* Name and text of the CUDA error behind the calling thread's most recent
+ * MOE_ERR_CUDA ("" if none); a static per-thread buffer. */
+const char* moe_last_cuda_error(void);
+
 /* Route — "Fused MoE FP8" section "Baseline: 7 kernels", item 1.
  * For each token t: z_e = softcap * tanh(logits[t,e] / softcap) (softcap == 0:
  * z_e = logits[t,e]); the top_k experts by (z descending, expert id
@@ -192,9 +196,10 @@ moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k
  * -> grouped GEMM(s) with the weighted scatter fused -> bf16 output.
  * out: bf16 [M, N] (FP8) or [M, K] (BF16).  ws: device workspace of
  * moe_workspace_size() bytes, 256-byte aligned, control block zeroed once.
- * With use_graph = 1 the launch sequence is captured on first use for this
- * argument set (pointers included) and replayed; when `stream` is already
- * capturing, the kernels are launched directly into the caller's capture. */
+ * With use_graph = 1 the launch sequence is captured (on a private stream) on
+ * first use for this argument set, pointers included, and the graph is
+ * replayed on `stream`; when `stream` is already capturing, the kernels are
+ * launched directly into the caller's capture. */
 moe_status_t moe_forward(const moe_forward_args* args, void* out, void* ws, size_t ws_bytes,
                          void* stream);
 

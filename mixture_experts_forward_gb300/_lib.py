@@ -22,12 +22,16 @@ CTRL_BYTES = 256
 
 EXPORTS = ["moe_status_string", "moe_num_sms", "moe_route", "moe_layout", "moe_quant_gather",
            "moe_grouped_gemm", "moe_scatter", "moe_workspace_size", "moe_forward",
-           "moe_forward_host", "moe_get_error", "moe_debug_set_pipeline_fault", "moe_forward_plan"]
+           "moe_forward_host", "moe_get_error", "moe_debug_set_pipeline_fault", "moe_forward_plan",
+           "moe_last_cuda_error"]
 
 
 class MoeError(RuntimeError):
     def __init__(self, code: int, what: str):
-        super().__init__(f"{what}: {status_string(code)} ({code})")
+        detail = ""
+        if code == MOE_ERR_CUDA:
+            detail = " — " + lib().moe_last_cuda_error().decode()
+        super().__init__(f"{what}: {status_string(code)} ({code}){detail}")
         self.code = code
 
 
@@ -67,6 +71,7 @@ def lib():
         L.moe_status_string.argtypes = [I]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_num_sms.restype = I
+        L.moe_last_cuda_error.restype = ctypes.c_char_p
         L.moe_route.argtypes = [P, I, I, I, F, I, P, P, P]
         L.moe_layout.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P]
         L.moe_quant_gather.argtypes = [P, I, I, I, P, P, P, P, I, P]
@@ -81,8 +86,8 @@ def lib():
         L.moe_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
         L.moe_debug_set_pipeline_fault.argtypes = [I, ctypes.c_uint64]
         for name in EXPORTS:
-            if name != "moe_status_string" and name != "moe_num_sms" and \
-                    name != "moe_workspace_size":
+            if name not in ("moe_status_string", "moe_num_sms", "moe_workspace_size",
+                            "moe_last_cuda_error"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib

@@ -10,6 +10,7 @@
 // and its griddepcontrol.wait orders the data.
 #include <cudaTypedefs.h>
 
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -70,7 +71,14 @@ bool make_tmap(CUtensorMap* m, const void* base, bool fp8, uint64_t inner, uint6
   return r == CUDA_SUCCESS;
 }
 
-moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+thread_local char g_last_error[256] = "";
+
+moe_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
 
 int auto_block_m(bool fp8, long long R, int E) {
   const long long avg = (R + E - 1) / E;
@@ -260,15 +268,15 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   cudaError_t e;
 
   e = launch_route(logits, M, E, k, f->softcap, f->renorm, ids, wts, stream, false);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   e = launch_layout(ids, R, E, bm, counts, offsets, sorted, slot, tile_off, ctrl, stream, pdl);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   const int sms = device_sms();
   if (fp8) {
     uint8_t* a_q = ws + L.a;
     float* a_s = reinterpret_cast<float*>(ws + L.a_scales);
     e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, stream, pdl);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));
     g.dtype = MOE_DTYPE_FP8_E4M3;
@@ -300,7 +308,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   void* a = ws + L.a;
   void* h = ws + L.h;
   e = launch_gather_rows_bf16(x, M, K, k, slot, a, acc, K, stream, pdl);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   moe_gemm_args g;
   std::memset(&g, 0, sizeof(g));
   g.dtype = MOE_DTYPE_BF16;
@@ -343,19 +351,19 @@ struct GraphEntry {
   const void* x;
   void* out;
   void* ws;
-  cudaStream_t stream;
   int device;
   cudaGraphExec_t exec;
 };
 constexpr int kGraphCache = 32;
 GraphEntry g_graphs[kGraphCache];
 int g_graph_count = 0, g_graph_next = 0;
+cudaStream_t g_capture_stream[64] = {};
 std::mutex g_graph_mu;
 
 bool same_entry(const GraphEntry& g, const moe_forward_args* f, const float* logits, const void* x,
-                void* out, void* ws, cudaStream_t stream, int dev) {
+                void* out, void* ws, int dev) {
   return std::memcmp(&g.args, f, sizeof(*f)) == 0 && g.logits == logits && g.x == x &&
-         g.out == out && g.ws == ws && g.stream == stream && g.device == dev;
+         g.out == out && g.ws == ws && g.device == dev;
 }
 
 moe_status_t forward_impl(const moe_forward_args* f, const float* logits, const void* x, void* out,
@@ -368,31 +376,44 @@ moe_status_t forward_impl(const moe_forward_args* f, const float* logits, const 
   if (ws_bytes < ws_layout(f).total) return MOE_ERR_WORKSPACE;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status_t cs = cuda_status(cudaStreamIsCapturing(stream, &cap));
+  if (cs != MOE_OK) return cs;
   if (!f->use_graph || cap != cudaStreamCaptureStatusNone)
     return enqueue_forward(f, logits, x, out, w8, stream);
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  cs = cuda_status(cudaGetDevice(&dev));
+  if (cs != MOE_OK) return cs;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_graph_mu);
   for (int i = 0; i < g_graph_count; ++i) {
-    if (same_entry(g_graphs[i], f, logits, x, out, ws, stream, dev))
+    if (same_entry(g_graphs[i], f, logits, x, out, ws, dev))
       return cuda_status(cudaGraphLaunch(g_graphs[i].exec, stream));
   }
+  // The launch sequence is recorded on a private stream (the caller's may be
+  // the legacy default stream, which cannot be captured); the graph itself
+  // is then launched on the caller's stream.
+  if (g_capture_stream[dev] == nullptr) {
+    cs = cuda_status(cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking));
+    if (cs != MOE_OK) return cs;
+  }
+  cudaStream_t cap_stream = g_capture_stream[dev];
   cudaGraph_t graph = nullptr;
-  if (cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  moe_status_t es = enqueue_forward(f, logits, x, out, w8, stream);
-  cudaError_t ce = cudaStreamEndCapture(stream, &graph);
+  cs = cuda_status(cudaStreamBeginCapture(cap_stream, cudaStreamCaptureModeThreadLocal));
+  if (cs != MOE_OK) return cs;
+  moe_status_t es = enqueue_forward(f, logits, x, out, w8, cap_stream);
+  cudaError_t ce = cudaStreamEndCapture(cap_stream, &graph);
   if (es != MOE_OK) {
     if (graph) cudaGraphDestroy(graph);
     return es;
   }
-  if (ce != cudaSuccess) return MOE_ERR_CUDA;
+  cs = cuda_status(ce);
+  if (cs != MOE_OK) return cs;
   cudaGraphExec_t exec = nullptr;
   ce = cudaGraphInstantiate(&exec, graph, 0);
   cudaGraphDestroy(graph);
-  if (ce != cudaSuccess) return MOE_ERR_CUDA;
+  cs = cuda_status(ce);
+  if (cs != MOE_OK) return cs;
   GraphEntry& slot = g_graphs[g_graph_next];
   if (g_graph_count == kGraphCache) cudaGraphExecDestroy(slot.exec);
   slot.args = *f;
@@ -400,7 +421,6 @@ moe_status_t forward_impl(const moe_forward_args* f, const float* logits, const 
   slot.x = x;
   slot.out = out;
   slot.ws = ws;
-  slot.stream = stream;
   slot.device = dev;
   slot.exec = exec;
   g_graph_next = (g_graph_next + 1) % kGraphCache;
@@ -426,6 +446,8 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 int moe_num_sms(void) { return device_sms(); }
+
+const char* moe_last_cuda_error(void) { return g_last_error; }
 
 moe_status_t moe_route(const float* logits, int M, int E, int top_k, float softcap, int renorm,
                        int32_t* ids, float* weights, void* stream) {
