@@ -42,8 +42,8 @@ FLUSH_BYTES = 256 * 1024 * 1024
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20000)   # ~2-3 s timed: room for clock samples
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="qwen_small_batch_fp8",
                     choices=list(inputs.FP8_CONFIGS) + list(inputs.BF16_CONFIGS))
@@ -132,7 +132,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
 
@@ -367,7 +367,7 @@ def bench_e2e(L, fa, d, kind, dev, args, flush, fl, world):
     for _ in range(3):
         L.forward_host(fa, h_logits, h_x, h_out, ws)
     torch.cuda.synchronize()
-    steps = max(10, args.steps // 2)
+    steps = max(10, min(args.steps // 2, 5000))
     st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):

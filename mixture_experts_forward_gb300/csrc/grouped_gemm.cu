@@ -50,7 +50,9 @@ template <int BM, bool kFP8, int kEpi>
 struct Cfg {
   static constexpr bool kSwiglu = kEpi == MOE_EPI_SWIGLU;
   static constexpr int kAccCols = kSwiglu ? 2 * BM : BM;
-  static constexpr int kNumAcc = kFP8 ? (512 / BM < 8 ? 512 / BM : 8)
+  // FP8: one buffer per K block, up to all 512 columns, so the MMA can run a
+  // whole tile or more ahead of the epilogue; BF16: double-buffered tiles.
+  static constexpr int kNumAcc = kFP8 ? (512 / BM < 32 ? 512 / BM : 32)
                                       : (512 / kAccCols >= 2 ? 2 : 1);
   static constexpr int kTmemNeed = kNumAcc * kAccCols;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
@@ -155,11 +157,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st_idx = G >= p.E ? c / p.E : 0;
       const int st_stride = G >= p.E ? (G - (c % p.E) + p.E - 1) / p.E : 1;
       int st_lt = st_idx;
+      // queue: the next tile index is claimed one tile ahead, so the atomic's
+      // round trip overlaps this tile's loads
+      int queued = p.sched == MOE_SCHED_QUEUE ? static_cast<int>(atomicAdd(p.queue_ctr, 1u)) : -1;
       for (;;) {
         int t;
         if (p.sched == MOE_SCHED_QUEUE) {
-          t = static_cast<int>(atomicAdd(p.queue_ctr, 1u));
-          if (t >= total_tiles) t = -1;
+          t = queued < total_tiles ? queued : -1;
+          if (t >= 0) queued = static_cast<int>(atomicAdd(p.queue_ctr, 1u));
         } else {
           t = -1;
           while (st_e < p.E) {

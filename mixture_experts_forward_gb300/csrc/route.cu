@@ -5,6 +5,9 @@
 // top-k by warp-shuffle reduction, one warp per token with E/32 values per
 // lane.  Ties go to the lower expert id.  Selection uses the capped logits z
 // (before exp), and the weights are the softmax over the selected experts.
+// Each lane keeps its best remaining expert; a selection round is one
+// warp-wide max over order-preserving keys (redux.sync), one min over the
+// ids that hold it, and a rescan by the winning lane only.
 //
 // exp and tanh are not libdevice calls: they are evaluated by a fixed
 // sequence of IEEE binary32 operations (round-to-nearest multiply, add,
@@ -20,8 +23,6 @@
 
 namespace moe {
 namespace {
-
-constexpr int kMaxPerLane = 32;  // E <= 1024
 
 __device__ __forceinline__ float f32_bits(uint32_t u) { return __uint_as_float(u); }
 
@@ -71,11 +72,16 @@ __device__ __forceinline__ float tanh_ieee(float t) {
   return signbit(t) ? -y : y;
 }
 
-// (value desc, id asc) ordering
-__device__ __forceinline__ bool better(float za, int ia, float zb, int ib) {
-  return za > zb || (za == zb && ia < ib);
+// Order-preserving map of a binary32 value to an unsigned key: larger value,
+// larger key.  -0.0 is first made +0.0 so that the two zeros tie (and the
+// lower expert id wins), as they do under floating-point comparison.
+__device__ __forceinline__ uint32_t order_key(float z) {
+  uint32_t u = __float_as_uint(z == 0.0f ? 0.0f : z);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// NPL = experts per lane (E <= 32 * NPL); lane l owns experts l, l+32, ...
+template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int M,
                                                     int E, int k, float softcap, int renorm,
                                                     int32_t* __restrict__ ids,
@@ -87,51 +93,61 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
   pdl_launch_dependents();
   if (t >= M) return;
   const float* row = logits + static_cast<size_t>(t) * E;
-  const int per_lane = (E + 31) >> 5;
 
-  float z[kMaxPerLane];
+  float z[NPL];
+  uint32_t key[NPL];
 #pragma unroll
-  for (int i = 0; i < kMaxPerLane; ++i) {
-    int e = lane + 32 * i;
-    float v = -__int_as_float(0x7f800000);
-    if (i < per_lane && e < E) {
-      v = __ldg(row + e);
-      if (softcap > 0.0f) v = __fmul_rn(softcap, tanh_ieee(__fdiv_rn(v, softcap)));
-    }
-    z[i] = v;
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    z[i] = e < E ? __ldg(row + e) : 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    if (softcap > 0.0f) z[i] = __fmul_rn(softcap, tanh_ieee(__fdiv_rn(z[i], softcap)));
+    key[i] = e < E ? order_key(z[i]) : 0u;  // key 0: below every real value
   }
 
-  uint32_t taken = 0;
-  float my_z = 0.0f;  // lane j keeps the j-th selected value
+  // this lane's best remaining expert (largest key; the first one wins ties,
+  // which is the lowest id because ids grow with i)
+  auto head_of = [&](uint32_t& hk, int& hi) {
+    hk = 0u;
+    hi = 0;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i)
+      if (key[i] > hk) {
+        hk = key[i];
+        hi = i;
+      }
+  };
+  uint32_t hk;
+  int hi;
+  head_of(hk, hi);
+
+  float my_z = 0.0f;  // lane j keeps the j-th selected value and id
   int my_id = 0;
-  float z0 = 0.0f;
   for (int j = 0; j < k; ++j) {
-    float bz = -__int_as_float(0x7f800000);
-    int bi = 0x7fffffff;
+    const uint32_t best = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t cand = (hk == best && best != 0u) ? static_cast<uint32_t>(lane + 32 * hi) : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    const int owner = static_cast<int>(win & 31u);
+    float zv = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      int e = lane + 32 * i;
-      if (i < per_lane && e < E && !((taken >> i) & 1u) && better(z[i], e, bz, bi)) {
-        bz = z[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      float oz = __shfl_xor_sync(0xffffffffu, bz, off);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (better(oz, oi, bz, bi)) {
-        bz = oz;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    for (int i = 0; i < NPL; ++i)
+      if (i == hi) zv = z[i];
+    zv = __shfl_sync(0xffffffffu, zv, owner);
     if (lane == j) {
-      my_z = bz;
-      my_id = bi;
+      my_z = zv;
+      my_id = static_cast<int>(win);
     }
-    if (j == 0) z0 = bz;
+    if (lane == owner) {
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (i == hi) key[i] = 0u;
+      head_of(hk, hi);
+    }
   }
+  const float z0 = __shfl_sync(0xffffffffu, my_z, 0);
 
   float my_e = 0.0f;
   if (lane < k) my_e = exp_ieee(__fsub_rn(my_z, z0));
@@ -143,9 +159,9 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     for (int e = 0; e < E; ++e) {
       float mine = 0.0f;
 #pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i)
+      for (int i = 0; i < NPL; ++i)
         if (i == (e >> 5)) mine = z[i];
-      float ze = __shfl_sync(0xffffffffu, mine, e & 31);
+      const float ze = __shfl_sync(0xffffffffu, mine, e & 31);
       s = __fadd_rn(s, exp_ieee(__fsub_rn(ze, z0)));
     }
   }
@@ -169,7 +185,13 @@ cudaError_t launch_route(const float* logits, int M, int E, int k, float softcap
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, route_kernel, logits, M, E, k, softcap, renorm, ids, weights);
+  const int npl = (E + 31) / 32;
+  if (npl <= 1) return cudaLaunchKernelEx(&cfg, route_kernel<1>, logits, M, E, k, softcap, renorm, ids, weights);
+  if (npl <= 2) return cudaLaunchKernelEx(&cfg, route_kernel<2>, logits, M, E, k, softcap, renorm, ids, weights);
+  if (npl <= 4) return cudaLaunchKernelEx(&cfg, route_kernel<4>, logits, M, E, k, softcap, renorm, ids, weights);
+  if (npl <= 8) return cudaLaunchKernelEx(&cfg, route_kernel<8>, logits, M, E, k, softcap, renorm, ids, weights);
+  if (npl <= 16) return cudaLaunchKernelEx(&cfg, route_kernel<16>, logits, M, E, k, softcap, renorm, ids, weights);
+  return cudaLaunchKernelEx(&cfg, route_kernel<32>, logits, M, E, k, softcap, renorm, ids, weights);
 }
 
 }  // namespace moe
