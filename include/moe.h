@@ -216,6 +216,37 @@ moe_status_t moe_forward_host(const moe_forward_args* args, const float* host_lo
  * and clears it. */
 moe_status_t moe_get_error(void* ws, moe_status_t* status, void* stream);
 
+/* Bytes of device memory that moe_grouped_gemm_noalloc keeps for its own use. */
+#define MOE_NOALLOC_SCRATCH_BYTES 256
+
+/* moe_grouped_gemm without a workspace.  No counterpart on the source pages:
+ * this entry point exists for callers that cannot allocate device memory —
+ * for example code running under an allocator or runtime that it does not
+ * own, or a latency-critical thread that must not call cudaMalloc — and so
+ * have no workspace to pass.
+ *
+ * The arguments, the computation and the output are those of
+ * moe_grouped_gemm.  The kernel's scratch (its tile-queue counters and status
+ * word, MOE_NOALLOC_SCRATCH_BYTES = 256 bytes) lives in a static device array
+ * inside this library instead of a caller workspace; that scratch does not
+ * grow with the problem, so every size moe_grouped_gemm accepts is accepted
+ * (argument errors are returned exactly as moe_grouped_gemm returns them).
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ * - Each call clears the scratch (cudaMemsetAsync on `stream`) before its
+ *   kernel, since the array keeps the previous call's contents.
+ * - All calls in the process share the one array per device: calls whose
+ *   work overlaps on the GPU (different streams, no ordering between them)
+ *   race on the counters and give wrong results.  Order them on one stream.
+ * - Device-side errors (a pipeline wait that timed out) are recorded in the
+ *   scratch status word, which this entry point does not return; callers who
+ *   need them use moe_grouped_gemm with a workspace and moe_get_error. */
+moe_status_t moe_grouped_gemm_noalloc(const moe_gemm_args* args, void* stream);
+
 /* Test hook for failure detection: when `drop_producer` is nonzero, the next
  * moe_grouped_gemm launches issue no loads, so every consumer wait runs into
  * its time limit of `timeout_ns` nanoseconds and the kernel exits with

@@ -23,7 +23,7 @@ CTRL_BYTES = 256
 EXPORTS = ["moe_status_string", "moe_num_sms", "moe_route", "moe_layout", "moe_quant_gather",
            "moe_grouped_gemm", "moe_scatter", "moe_workspace_size", "moe_forward",
            "moe_forward_host", "moe_get_error", "moe_debug_set_pipeline_fault", "moe_forward_plan",
-           "moe_last_cuda_error"]
+           "moe_last_cuda_error", "moe_grouped_gemm_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -76,6 +76,7 @@ def lib():
         L.moe_layout.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P]
         L.moe_quant_gather.argtypes = [P, I, I, I, P, P, P, P, I, P]
         L.moe_grouped_gemm.argtypes = [ctypes.POINTER(GemmArgs), P, ctypes.c_size_t, P]
+        L.moe_grouped_gemm_noalloc.argtypes = [ctypes.POINTER(GemmArgs), P]
         L.moe_scatter.argtypes = [P, P, P, I, I, I, P, P]
         L.moe_workspace_size.argtypes = [ctypes.POINTER(ForwardArgs)]
         L.moe_workspace_size.restype = ctypes.c_size_t
@@ -169,6 +170,25 @@ def grouped_gemm(*, dtype, epilogue, a, w, offsets, tile_offsets, out, ws, block
                  out=out.data_ptr(), k_splits=k_splits, num_ctas=num_ctas)
     _check(lib().moe_grouped_gemm(ctypes.byref(g), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_grouped_gemm")
+    return out
+
+
+def grouped_gemm_noalloc(*, dtype, epilogue, a, w, offsets, tile_offsets, out, block_m,
+                         a_scales=None, w_scales=None, sorted_route_ids=None, route_weights=None,
+                         M=0, top_k=0, sched=SCHED_QUEUE, k_splits=0, num_ctas=0, stream=None):
+    """moe_grouped_gemm_noalloc: the same GEMM with the library's own static
+    scratch instead of a workspace (for callers that cannot allocate)."""
+    E, N, K = w.shape
+    g = GemmArgs(dtype=dtype, epilogue=epilogue, sched=sched, block_m=block_m, E=E, N=N, K=K,
+                 R=a.shape[0], M=M, top_k=top_k, a=a.data_ptr(),
+                 a_scales=None if a_scales is None else a_scales.data_ptr(), w=w.data_ptr(),
+                 w_scales=None if w_scales is None else w_scales.data_ptr(),
+                 offsets=offsets.data_ptr(), tile_offsets=tile_offsets.data_ptr(),
+                 sorted_route_ids=None if sorted_route_ids is None else sorted_route_ids.data_ptr(),
+                 route_weights=None if route_weights is None else route_weights.data_ptr(),
+                 out=out.data_ptr(), k_splits=k_splits, num_ctas=num_ctas)
+    _check(lib().moe_grouped_gemm_noalloc(ctypes.byref(g), _stream(stream)),
+           "moe_grouped_gemm_noalloc")
     return out
 
 

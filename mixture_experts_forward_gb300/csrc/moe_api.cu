@@ -428,6 +428,18 @@ moe_status_t forward_impl(const moe_forward_args* f, const float* logits, const 
   return cuda_status(cudaGraphLaunch(exec, stream));
 }
 
+// ---------------------------------------------------------------------------
+// Scratch of moe_grouped_gemm_noalloc: the grouped GEMM's control block (tile
+// queue counters and status word) in a file-scope device array instead of a
+// caller workspace.  Every GPU that loads this library holds these 256 bytes
+// until the process exits.  Host code must not pass the symbol itself to a
+// kernel (on the host it only stands for the device variable); the device
+// address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+static_assert(MOE_NOALLOC_SCRATCH_BYTES >= sizeof(Ctrl), "the scratch holds one control block");
+void* g_noalloc_addr[64] = {};
+std::mutex g_noalloc_mu;
+
 }  // namespace
 
 extern "C" {
@@ -581,6 +593,30 @@ moe_status_t moe_get_error(void* ws, moe_status_t* status, void* stream) {
   if (cudaMemset(&c->status, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   *status = static_cast<moe_status_t>(v);
   return MOE_OK;
+}
+
+moe_status_t moe_grouped_gemm_noalloc(const moe_gemm_args* args, void* stream) {
+  moe_status_t s = check_gemm(args);
+  if (s != MOE_OK) return s;
+  int dev = 0;
+  s = cuda_status(cudaGetDevice(&dev));
+  if (s != MOE_OK) return s;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+      // first call on this device: look up the device address of the array
+      s = cuda_status(cudaGetSymbolAddress(&g_noalloc_addr[dev], g_noalloc_scratch));
+      if (s != MOE_OK) return s;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The counters must start at zero; the previous call's contents are still there.
+  s = cuda_status(cudaMemsetAsync(scratch, 0, MOE_NOALLOC_SCRATCH_BYTES, st));
+  if (s != MOE_OK) return s;
+  return run_gemm(args, static_cast<Ctrl*>(scratch), false, st, false);
 }
 
 moe_status_t moe_debug_set_pipeline_fault(int drop_producer, uint64_t timeout_ns) {
