@@ -86,6 +86,33 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const in
   d.nkb = min(p.kb_per_split, p.KB - d.kb0);
 }
 
+// Fused finalize (weighted-scatter epilogue): after this tile's reds, each of
+// its rows s adds one arrival to the counter of (token, n_tile); the arrival
+// that completes top_k * k_splits contributions makes this CTA round the
+// token's 128-column segment of the fp32 output to bf16.  Called by all 128
+// epilogue threads; the reds of every contributing CTA are ordered before
+// its arrival by a device-scope fence.
+__device__ __forceinline__ void finalize_segments(const GemmParams& p, const TileDesc& d, int et,
+                                                  int col, const int* s_tok, int* s_fin) {
+  __threadfence();
+  named_bar_sync(1, 128);
+  const unsigned target = static_cast<unsigned>(p.top_k * p.k_splits);
+  for (int s = et; s < d.rows; s += 128) {
+    const unsigned prev = atomicAdd(p.tile_cnt + static_cast<size_t>(s_tok[s]) * p.n_tiles + d.n_tile, 1u);
+    s_fin[s] = prev == target - 1u;
+  }
+  named_bar_sync(1, 128);
+  __threadfence();
+  const float* acc = static_cast<const float*>(p.out);
+  __nv_bfloat16* outb = static_cast<__nv_bfloat16*>(p.out_bf16);
+  for (int s = 0; s < d.rows; ++s) {
+    if (s_fin[s]) {
+      const size_t idx = static_cast<size_t>(s_tok[s]) * p.N + col;
+      outb[idx] = __float2bfloat16_rn(__ldcg(acc + idx));
+    }
+  }
+}
+
 template <int BM, bool kFP8, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
@@ -101,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_tile_off[kMaxE + 1];
   __shared__ int s_tok[BM];
   __shared__ float s_wt[BM];
+  __shared__ int s_fin[BM];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -358,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < BM; ++s) {
             if (s < d.rows) red_add_f32(out + static_cast<size_t>(s_tok[s]) * p.N + col, s_wt[s] * acc[s]);
           }
+          if (p.out_bf16 != nullptr) finalize_segments(p, d, et, col, s_tok, s_fin);
         } else {
           float* out = static_cast<float*>(p.out);
 #pragma unroll
@@ -411,6 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[buf]));
         ++acc_n;
+        if constexpr (kEpi == MOE_EPI_SCATTER) {
+          if (p.out_bf16 != nullptr) finalize_segments(p, d, et, col, s_tok, s_fin);
+        }
       }
     }
     if (!ok) {

@@ -135,7 +135,7 @@ int pick_k_splits(const moe_gemm_args* a, int sms, int KB) {
 }
 
 moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStream_t stream,
-                      bool pdl) {
+                      bool pdl, void* out_bf16 = nullptr, unsigned* tile_cnt = nullptr) {
   const bool fp8 = a->dtype == MOE_DTYPE_FP8_E4M3;
   const int sms = device_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
@@ -170,6 +170,8 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   p.sched = a->sched;
   p.drop_producer = g_drop_producer;
   p.timeout_ns = g_timeout_ns;
+  p.out_bf16 = a->epilogue == MOE_EPI_SCATTER ? out_bf16 : nullptr;
+  p.tile_cnt = tile_cnt;
   const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m);
   if (stage_bytes <= 0) return MOE_ERR_UNSUPPORTED;
   const int scale_bytes = fp8 ? p.kb_per_split * a->block_m * 4 : 0;
@@ -185,7 +187,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
 // ---------------------------------------------------------------------------
 // Workspace layout of the forward.
 struct WsLayout {
-  size_t ctrl, ids, weights, counts, offsets, tile_off, sorted, slot, a, a_scales, acc, h;
+  size_t ctrl, ids, weights, counts, offsets, tile_off, sorted, slot, a, a_scales, acc, cnt, h;
   size_t st_logits, st_x, st_out;
   size_t total;
 };
@@ -219,6 +221,7 @@ WsLayout ws_layout(const moe_forward_args* f) {
   L.a_scales = fp8 ? take((K / 128) * R * 4) : 0;
   const size_t out_cols = fp8 ? N : K;
   L.acc = take(M * out_cols * 4);
+  L.cnt = take(M * (out_cols / 128) * 4);
   L.h = fp8 ? 0 : take(R * N * 2);
   L.st_logits = take(M * E * 4);
   L.st_x = take(M * K * 2);
@@ -267,15 +270,14 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   const bool pdl = true;
   cudaError_t e;
 
-  e = launch_route(logits, M, E, k, f->softcap, f->renorm, ids, wts, stream, false);
+  e = launch_route_layout(logits, M, E, k, f->softcap, f->renorm, ids, wts, bm, counts, offsets,
+                          sorted, slot, tile_off, ctrl, stream, false);
   if (e != cudaSuccess) return cuda_status(e);
-  e = launch_layout(ids, R, E, bm, counts, offsets, sorted, slot, tile_off, ctrl, stream, pdl);
-  if (e != cudaSuccess) return cuda_status(e);
-  const int sms = device_sms();
+  unsigned* cnt = reinterpret_cast<unsigned*>(ws + L.cnt);
   if (fp8) {
     uint8_t* a_q = ws + L.a;
     float* a_s = reinterpret_cast<float*>(ws + L.a_scales);
-    e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, stream, pdl);
+    e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, cnt, N / 128, stream, pdl);
     if (e != cudaSuccess) return cuda_status(e);
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));
@@ -299,15 +301,12 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     g.route_weights = wts;
     g.out = acc;
     g.k_splits = f->k_splits;
-    moe_status_t s = run_gemm(&g, ctrl, false, stream, pdl);
-    if (s != MOE_OK) return s;
-    e = launch_finalize(acc, out, static_cast<size_t>(M) * N, sms, stream, pdl);
-    return cuda_status(e);
+    return run_gemm(&g, ctrl, false, stream, pdl, out, cnt);
   }
   // BF16 gated FFN: gather -> up (SwiGLU) -> down (scatter) -> finalize
   void* a = ws + L.a;
   void* h = ws + L.h;
-  e = launch_gather_rows_bf16(x, M, K, k, slot, a, acc, K, stream, pdl);
+  e = launch_gather_rows_bf16(x, M, K, k, slot, a, acc, K, cnt, K / 128, stream, pdl);
   if (e != cudaSuccess) return cuda_status(e);
   moe_gemm_args g;
   std::memset(&g, 0, sizeof(g));
@@ -337,10 +336,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   g.sorted_route_ids = sorted;
   g.route_weights = wts;
   g.out = acc;
-  s = run_gemm(&g, ctrl, true, stream, pdl);
-  if (s != MOE_OK) return s;
-  e = launch_finalize(acc, out, static_cast<size_t>(M) * K, sms, stream, pdl);
-  return cuda_status(e);
+  return run_gemm(&g, ctrl, true, stream, pdl, out, cnt);
 }
 
 // ---------------------------------------------------------------------------
@@ -497,7 +493,8 @@ moe_status_t moe_quant_gather(const void* x, int M, int K, int top_k, const int3
   if (zero_acc != nullptr && (zero_cols <= 0 || zero_cols % 4 != 0 || !aligned16(zero_acc)))
     return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_quant_gather(x, M, K, top_k, route_slot, a_q, a_scales, zero_acc,
-                                         zero_cols, static_cast<cudaStream_t>(stream), false));
+                                         zero_cols, nullptr, 0, static_cast<cudaStream_t>(stream),
+                                         false));
 }
 
 moe_status_t moe_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_bytes, void* stream) {

@@ -21,7 +21,8 @@ struct Ctrl {
   int err_info;          // diagnostic: where the first error happened
   unsigned queue2;       // second GEMM of a forward (BF16 FFN down projection)
   unsigned done2;
-  int pad[58];
+  unsigned route_done;   // CTAs of the fused route+layout kernel that have finished routing
+  int pad[57];
 };
 static_assert(sizeof(Ctrl) == MOE_CTRL_BYTES, "control block size");
 

@@ -19,6 +19,7 @@
 //   tanh(t): |t| < 0.5: a + (a*s)*q(s), s = a*a, q the odd Taylor series of
 //            tanh to degree 17 by Horner in s; 0.5 <= |t| < 10:
 //            1 - 2/(exp(2|t|) + 1); |t| >= 10: 1; sign of t restored.
+#include "layout_block.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -80,20 +81,13 @@ __device__ __forceinline__ uint32_t order_key(float z) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// NPL = experts per lane (E <= 32 * NPL); lane l owns experts l, l+32, ...
+// Routes one token with one warp.  NPL = experts per lane (E <= 32 * NPL);
+// lane l owns experts l, l+32, ...
 template <int NPL>
-__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int M,
-                                                    int E, int k, float softcap, int renorm,
-                                                    int32_t* __restrict__ ids,
-                                                    float* __restrict__ weights) {
-  pdl_wait();
-  const int warps = blockDim.x >> 5;
-  const int t = blockIdx.x * warps + (threadIdx.x >> 5);
+__device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k,
+                                            float softcap, int renorm, int32_t* __restrict__ ids,
+                                            float* __restrict__ weights) {
   const int lane = threadIdx.x & 31;
-  pdl_launch_dependents();
-  if (t >= M) return;
-  const float* row = logits + static_cast<size_t>(t) * E;
-
   float z[NPL];
   uint32_t key[NPL];
 #pragma unroll
@@ -110,25 +104,21 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 
   // this lane's best remaining expert (largest key; the first one wins ties,
   // which is the lowest id because ids grow with i)
-  auto head_of = [&](uint32_t& hk, int& hi) {
-    hk = 0u;
-    hi = 0;
+  uint32_t hk = 0u;
+  int hi = 0;
 #pragma unroll
-    for (int i = 0; i < NPL; ++i)
-      if (key[i] > hk) {
-        hk = key[i];
-        hi = i;
-      }
-  };
-  uint32_t hk;
-  int hi;
-  head_of(hk, hi);
+  for (int i = 0; i < NPL; ++i)
+    if (key[i] > hk) {
+      hk = key[i];
+      hi = i;
+    }
 
   float my_z = 0.0f;  // lane j keeps the j-th selected value and id
   int my_id = 0;
   for (int j = 0; j < k; ++j) {
     const uint32_t best = __reduce_max_sync(0xffffffffu, hk);
-    const uint32_t cand = (hk == best && best != 0u) ? static_cast<uint32_t>(lane + 32 * hi) : 0xffffffffu;
+    const uint32_t cand =
+        (hk == best && best != 0u) ? static_cast<uint32_t>(lane + 32 * hi) : 0xffffffffu;
     const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
     const int owner = static_cast<int>(win & 31u);
     float zv = 0.0f;
@@ -144,7 +134,14 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 #pragma unroll
       for (int i = 0; i < NPL; ++i)
         if (i == hi) key[i] = 0u;
-      head_of(hk, hi);
+      hk = 0u;
+      hi = 0;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i)
+        if (key[i] > hk) {
+          hk = key[i];
+          hi = i;
+        }
     }
   }
   const float z0 = __shfl_sync(0xffffffffu, my_z, 0);
@@ -166,9 +163,53 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
     }
   }
   if (lane < k) {
-    ids[static_cast<size_t>(t) * k + lane] = my_id;
-    weights[static_cast<size_t>(t) * k + lane] = __fdiv_rn(my_e, s);
+    ids[lane] = my_id;
+    weights[lane] = __fdiv_rn(my_e, s);
   }
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits, int M,
+                                                    int E, int k, float softcap, int renorm,
+                                                    int32_t* __restrict__ ids,
+                                                    float* __restrict__ weights) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= M) return;
+  route_token<NPL>(logits + static_cast<size_t>(t) * E, E, k, softcap, renorm,
+                   ids + static_cast<size_t>(t) * k, weights + static_cast<size_t>(t) * k);
+}
+
+// Route + layout in one launch: every CTA routes 32 tokens (a warp each);
+// the CTA that finishes last (an arrival counter in the control block) then
+// builds the layout of all routes (layout_block.cuh) and re-arms the counter.
+template <int NPL>
+__global__ void __launch_bounds__(kLayoutThreads, 1)
+    route_layout_kernel(const float* __restrict__ logits, int M, int E, int k, float softcap,
+                        int renorm, int32_t* ids, float* __restrict__ weights, int block_m,
+                        int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                        int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ route_slot,
+                        int32_t* __restrict__ tile_offsets, Ctrl* ctrl) {
+  extern __shared__ int s_hist[];
+  __shared__ int s_last;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = blockIdx.x * (kLayoutThreads / 32) + (threadIdx.x >> 5);
+  if (t < M)
+    route_token<NPL>(logits + static_cast<size_t>(t) * E, E, k, softcap, renorm,
+                     ids + static_cast<size_t>(t) * k, weights + static_cast<size_t>(t) * k);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's ids are visible before it is counted
+    s_last = atomicAdd(&ctrl->route_done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  layout_block(ids, M * k, E, block_m, counts, offsets, sorted_route_ids, route_slot,
+               tile_offsets, ctrl, s_hist);
+  if (threadIdx.x == 0) ctrl->route_done = 0u;
 }
 
 }  // namespace
@@ -192,6 +233,51 @@ cudaError_t launch_route(const float* logits, int M, int E, int k, float softcap
   if (npl <= 8) return cudaLaunchKernelEx(&cfg, route_kernel<8>, logits, M, E, k, softcap, renorm, ids, weights);
   if (npl <= 16) return cudaLaunchKernelEx(&cfg, route_kernel<16>, logits, M, E, k, softcap, renorm, ids, weights);
   return cudaLaunchKernelEx(&cfg, route_kernel<32>, logits, M, E, k, softcap, renorm, ids, weights);
+}
+
+template <int NPL>
+cudaError_t launch_route_layout_t(const float* logits, int M, int E, int k, float softcap,
+                                  int renorm, int32_t* ids, float* weights, int block_m,
+                                  int32_t* counts, int32_t* offsets, int32_t* sorted_route_ids,
+                                  int32_t* route_slot, int32_t* tile_offsets, Ctrl* ctrl,
+                                  cudaStream_t stream, bool pdl) {
+  const size_t smem = static_cast<size_t>(layout_warps(M * k)) * E * sizeof(int);
+  cudaError_t err = cudaFuncSetAttribute(route_layout_kernel<NPL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((M + 31) / 32);
+  cfg.blockDim = dim3(kLayoutThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, route_layout_kernel<NPL>, logits, M, E, k, softcap, renorm, ids,
+                            weights, block_m, counts, offsets, sorted_route_ids, route_slot,
+                            tile_offsets, ctrl);
+}
+
+cudaError_t launch_route_layout(const float* logits, int M, int E, int k, float softcap,
+                                int renorm, int32_t* ids, float* weights, int block_m,
+                                int32_t* counts, int32_t* offsets, int32_t* sorted_route_ids,
+                                int32_t* route_slot, int32_t* tile_offsets, Ctrl* ctrl,
+                                cudaStream_t stream, bool pdl) {
+  const int npl = (E + 31) / 32;
+#define MOE_RL(N)                                                                             \
+  return launch_route_layout_t<N>(logits, M, E, k, softcap, renorm, ids, weights, block_m,    \
+                                  counts, offsets, sorted_route_ids, route_slot, tile_offsets, \
+                                  ctrl, stream, pdl)
+  if (npl <= 1) MOE_RL(1);
+  if (npl <= 2) MOE_RL(2);
+  if (npl <= 4) MOE_RL(4);
+  if (npl <= 8) MOE_RL(8);
+  if (npl <= 16) MOE_RL(16);
+  MOE_RL(32);
+#undef MOE_RL
 }
 
 }  // namespace moe
