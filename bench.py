@@ -226,7 +226,7 @@ def bench_ours(args, rank, world, local):
     fl = flops_per_step(kind, c)
     value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
     ms_per_step = total_ms / args.steps
-    launches_per_step = 3 if kind == "fp8" else 4   # route+layout, quant/gather, GEMM(s)
+    launches_per_step = 4 if kind == "fp8" else 5   # route+layout, quant/gather, GEMM(s), finalize
 
     # routing facts of this batch (for bytes and the roofline)
     ids, _ = L.route(logits, k, softcap=c.get("softcap", 0.0))

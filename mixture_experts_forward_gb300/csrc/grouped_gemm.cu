@@ -21,7 +21,10 @@
 //               FP8: per K block, acc += partial * (a_scale * w_scale) in fp32
 //               registers ("promotion"; each K block has its own TMEM buffer),
 //               then weighted red.global.add into the fp32 output, a plain
-//               store, or silu(gate)*up to bf16.
+//               store, or silu(gate)*up to bf16
+//   warp 6      tile metadata: routed-row tokens, route weights and the FP8
+//               scale products of each tile, staged into a shared ring ahead
+//               of the epilogue
 // Every wait is bounded (mbar_wait): on a time-out the CTA records
 // MOE_ERR_TIMEOUT in the workspace status word, raises a shared abort flag so
 // the other roles stop too, waits (bounded) for its own in-flight copies and
@@ -38,8 +41,9 @@ constexpr int kTileN = 128;           // weight rows per tile (MMA M)
 constexpr int kRowBytes = 128;        // bytes per K block row (one swizzle atom row)
 constexpr int kATileBytes = kTileN * kRowBytes;
 constexpr int kMaxStages = 16;
-constexpr int kRing = 4;              // tile descriptors in flight
-constexpr int kThreads = 192;
+constexpr int kRing = 4;              // tile descriptors (and metadata slots) in flight
+constexpr int kThreads = 224;         // 7 warps
+constexpr int kMetaWarp = 6;
 constexpr int kMaxE = 1024;
 
 struct TileDesc {
@@ -59,13 +63,23 @@ struct Cfg {
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kATiles = kSwiglu ? 2 : 1;
   static constexpr int kStageBytes = kATiles * kATileBytes + BM * kRowBytes;
+  // FP8 epilogue: K blocks whose partials are loaded before one wait (<= 64 columns)
+  static constexpr int kKbGroup = BM <= 64 ? 64 / BM : 1;
+  static constexpr int kLdCols = BM <= 64 ? BM : 64;   // columns per load wave
   static_assert(BM % 16 == 0 && BM >= 16 && BM <= 256, "block_m");
   static_assert(!kFP8 || BM <= 128, "FP8 block_m <= 128");
   static_assert(kTmemNeed <= 512, "TMEM");
 };
 
+// Bytes of one metadata slot: [kb_per_split][BM] FP8 scale products, then
+// BM token ids and BM route weights.
+__host__ __device__ inline int meta_slot_bytes(bool fp8, int bm, int kb_per_split) {
+  const int n = (fp8 ? kb_per_split * bm : 0) + 2 * bm;
+  return (n * 4 + 15) & ~15;
+}
+
 __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const int* s_tile_off,
-                                            int BM, TileDesc& d) {
+                                            const int* s_off, int BM, TileDesc& d) {
   const int per_m = p.n_tiles * p.k_splits;
   const int mt = t / per_m;
   const int r = t - mt * per_m;
@@ -76,7 +90,7 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const in
     if (s_tile_off[mid] <= mt) lo = mid; else hi = mid;
   }
   const int e = lo;
-  const int seg_begin = __ldg(p.offsets + e), seg_end = __ldg(p.offsets + e + 1);
+  const int seg_begin = s_off[e], seg_end = s_off[e + 1];
   d.e = e;
   d.m0 = seg_begin + (mt - s_tile_off[e]) * BM;
   d.rows = min(BM, seg_end - d.m0);
@@ -84,33 +98,6 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const in
   const int ks = r - d.n_tile * p.k_splits;
   d.kb0 = ks * p.kb_per_split;
   d.nkb = min(p.kb_per_split, p.KB - d.kb0);
-}
-
-// Fused finalize (weighted-scatter epilogue): after this tile's reds, each of
-// its rows s adds one arrival to the counter of (token, n_tile); the arrival
-// that completes top_k * k_splits contributions makes this CTA round the
-// token's 128-column segment of the fp32 output to bf16.  Called by all 128
-// epilogue threads; the reds of every contributing CTA are ordered before
-// its arrival by a device-scope fence.
-__device__ __forceinline__ void finalize_segments(const GemmParams& p, const TileDesc& d, int et,
-                                                  int col, const int* s_tok, int* s_fin) {
-  __threadfence();
-  named_bar_sync(1, 128);
-  const unsigned target = static_cast<unsigned>(p.top_k * p.k_splits);
-  for (int s = et; s < d.rows; s += 128) {
-    const unsigned prev = atomicAdd(p.tile_cnt + static_cast<size_t>(s_tok[s]) * p.n_tiles + d.n_tile, 1u);
-    s_fin[s] = prev == target - 1u;
-  }
-  named_bar_sync(1, 128);
-  __threadfence();
-  const float* acc = static_cast<const float*>(p.out);
-  __nv_bfloat16* outb = static_cast<__nv_bfloat16*>(p.out_bf16);
-  for (int s = 0; s < d.rows; ++s) {
-    if (s_fin[s]) {
-      const size_t idx = static_cast<size_t>(s_tok[s]) * p.N + col;
-      outb[idx] = __float2bfloat16_rn(__ldcg(acc + idx));
-    }
-  }
 }
 
 template <int BM, bool kFP8, int kEpi>
@@ -121,20 +108,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_tfull[C::kNumAcc], bar_tempty[C::kNumAcc];
-  __shared__ __align__(8) uint64_t bar_dfull[kRing], bar_dempty[kRing], bar_drain;
+  __shared__ __align__(8) uint64_t bar_dfull[kRing], bar_dempty[kRing], bar_mfull[kRing];
+  __shared__ __align__(8) uint64_t bar_drain;
   __shared__ TileDesc s_desc[kRing];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_tile_off[kMaxE + 1];
-  __shared__ int s_tok[BM];
-  __shared__ float s_wt[BM];
-  __shared__ int s_fin[BM];
+  __shared__ int s_off[kMaxE + 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
-  float* s_scale = reinterpret_cast<float*>(smem_gen + p.num_stages * C::kStageBytes);
   const int NST = p.num_stages;
+  const int meta_bytes = meta_slot_bytes(kFP8, BM, p.kb_per_split);
+  uint8_t* s_meta = smem_gen + NST * C::kStageBytes;  // kRing slots of meta_bytes
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -147,7 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(smem_u32(&bar_dfull[i]), 1);
-      mbar_init(smem_u32(&bar_dempty[i]), 5);
+      mbar_init(smem_u32(&bar_dempty[i]), 5);  // MMA thread + 4 epilogue warps
+      mbar_init(smem_u32(&bar_mfull[i]), 1);
     }
     mbar_init(smem_u32(&bar_drain), 1);
     s_abort = 0;
@@ -163,10 +151,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Everything above is independent of the preceding kernel's results.
   pdl_wait();
-  for (int i = threadIdx.x; i <= p.E; i += kThreads) s_tile_off[i] = __ldg(p.tile_offsets + i);
+  for (int i = threadIdx.x; i <= p.E; i += kThreads) {
+    s_tile_off[i] = __ldg(p.tile_offsets + i);
+    s_off[i] = __ldg(p.offsets + i);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The dependent kernel (the forward's finalize) may become resident now;
+  // its griddepcontrol.wait still waits for this grid to complete.
+  pdl_launch_dependents();
   const uint32_t tmem_base = s_tmem;
   const int total_tiles = s_tile_off[p.E] * p.n_tiles * p.k_splits;
   const uint64_t tmo = p.timeout_ns;
@@ -181,18 +175,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       // static schedule state: experts handled by this CTA
       const int G = gridDim.x, c = blockIdx.x;
-      int st_e = p.E >= 1 ? (G >= p.E ? c % p.E : c) : 0;
+      int st_e = G >= p.E ? c % p.E : c;
       const int st_idx = G >= p.E ? c / p.E : 0;
       const int st_stride = G >= p.E ? (G - (c % p.E) + p.E - 1) / p.E : 1;
       int st_lt = st_idx;
-      // queue: the next tile index is claimed one tile ahead, so the atomic's
+      // queue: CTA c starts with tile c; later tiles come from the counter
+      // (offset by the grid size), claimed one tile ahead so the atomic's
       // round trip overlaps this tile's loads
-      int queued = p.sched == MOE_SCHED_QUEUE ? static_cast<int>(atomicAdd(p.queue_ctr, 1u)) : -1;
+      int queued = p.sched == MOE_SCHED_QUEUE ? c : -1;
       for (;;) {
         int t;
         if (p.sched == MOE_SCHED_QUEUE) {
           t = queued < total_tiles ? queued : -1;
-          if (t >= 0) queued = static_cast<int>(atomicAdd(p.queue_ctr, 1u));
+          if (t >= 0) queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
         } else {
           t = -1;
           while (st_e < p.E) {
@@ -209,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         TileDesc d;
         if (t >= 0) {
-          decode_tile(t, p, s_tile_off, BM, d);
+          decode_tile(t, p, s_tile_off, s_off, BM, d);
           if (d.rows <= 0 || d.nkb <= 0) continue;
         } else {
           d.nkb = -1;
@@ -302,91 +297,125 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(smem_u32(&bar_drain));
       mbar_wait(smem_u32(&bar_drain), 0u, &s_abort, tmo);
     }
+  } else if (warp == kMetaWarp) {
+    // ------------------------------------------------------------ tile metadata
+    int ds = 0;
+    uint32_t dphase = 0;
+    const int NB = p.N / kTileN;
+    for (;;) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_dfull[ds]), dphase, &s_abort, tmo))) {
+        set_error(p.ctrl, MOE_ERR_TIMEOUT, 4);
+        s_abort = 1;
+        break;
+      }
+      const TileDesc d = s_desc[ds];
+      if (d.nkb >= 0) {
+        float* sc = reinterpret_cast<float*>(s_meta + ds * meta_bytes);
+        int* tok = reinterpret_cast<int*>(sc + (kFP8 ? p.kb_per_split * BM : 0));
+        float* wt = reinterpret_cast<float*>(tok + BM);
+        if constexpr (kEpi == MOE_EPI_SCATTER) {
+          for (int s = lane; s < BM; s += 32) {
+            int tk = 0;
+            float w = 0.0f;
+            if (s < d.rows) {
+              const int r = __ldg(p.sorted_route_ids + d.m0 + s);
+              tk = r / p.top_k;
+              w = __ldg(p.route_weights + r);
+            }
+            tok[s] = tk;
+            wt[s] = w;
+          }
+        }
+        if constexpr (kFP8) {
+          const float* wsc = p.w_scales + (static_cast<size_t>(d.e) * NB + d.n_tile) * p.KB + d.kb0;
+          for (int idx = lane; idx < d.nkb * BM; idx += 32) {
+            const int kb = idx / BM, s = idx - kb * BM;
+            float v = 0.0f;
+            if (s < d.rows)
+              v = __ldg(p.a_scales + static_cast<size_t>(d.kb0 + kb) * p.R + d.m0 + s) * __ldg(wsc + kb);
+            sc[idx] = v;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_mfull[ds]));
+      if (++ds == kRing) { ds = 0; dphase ^= 1u; }
+      if (d.nkb < 0) break;
+    }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 64;               // 0..127
     const int quad = warp & 3;                     // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;              // weight row within the tile
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
     int ds = 0, acc_n = 0;
     uint32_t dphase = 0;
     bool ok = true;
-    const int NB = p.N / kTileN;
     for (;;) {
       // every lane waits; the warp proceeds only if all lanes saw the phase
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_dfull[ds]), dphase, &s_abort, tmo))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mfull[ds]), dphase, &s_abort, tmo))) {
         ok = false;
         break;
       }
       const TileDesc d = s_desc[ds];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bar_dempty[ds]));
-      if (++ds == kRing) { ds = 0; dphase ^= 1u; }
       if (d.nkb < 0) break;
-
-      // per-tile metadata in shared memory
-      named_bar_sync(1, 128);
-      if constexpr (kEpi == MOE_EPI_SCATTER) {
-        for (int s = et; s < BM; s += 128) {
-          int tok = -1;
-          float wt = 0.0f;
-          if (s < d.rows) {
-            const int r = __ldg(p.sorted_route_ids + d.m0 + s);
-            tok = r / p.top_k;
-            wt = __ldg(p.route_weights + r);
-          }
-          s_tok[s] = tok;
-          s_wt[s] = wt;
-        }
-      }
-      if constexpr (kFP8) {
-        const float* wsc = p.w_scales + (static_cast<size_t>(d.e) * NB + d.n_tile) * p.KB + d.kb0;
-        for (int idx = et; idx < d.nkb * BM; idx += 128) {
-          const int kb = idx / BM, s = idx - kb * BM;
-          float v = 0.0f;
-          if (s < d.rows)
-            v = __ldg(p.a_scales + static_cast<size_t>(d.kb0 + kb) * p.R + d.m0 + s) * __ldg(wsc + kb);
-          s_scale[idx] = v;
-        }
-      }
-      named_bar_sync(1, 128);
+      const float* sc = reinterpret_cast<const float*>(s_meta + ds * meta_bytes);
+      const int* tok = reinterpret_cast<const int*>(sc + (kFP8 ? p.kb_per_split * BM : 0));
+      const float* wt = reinterpret_cast<const float*>(tok + BM);
+      const int col = d.n_tile * kTileN + row;
 
       if constexpr (kFP8) {
         float acc[BM];
 #pragma unroll
         for (int s = 0; s < BM; ++s) acc[s] = 0.0f;
-        for (int i = 0; i < d.nkb; ++i) {
-          const int buf = acc_n % C::kNumAcc;
-          const uint32_t use = static_cast<uint32_t>(acc_n / C::kNumAcc);
-          if (!__all_sync(0xffffffffu,
-                          mbar_wait(smem_u32(&bar_tfull[buf]), use & 1u, &s_abort, tmo))) {
+        for (int i = 0; i < d.nkb && ok; i += C::kKbGroup) {
+          const int ng = min(C::kKbGroup, d.nkb - i);
+          // wait for the partials of K blocks i .. i+ng-1
+          bool got = true;
+          for (int g = 0; g < ng; ++g) {
+            const int a = acc_n + g;
+            got = got && mbar_wait(smem_u32(&bar_tfull[a % C::kNumAcc]),
+                                   static_cast<uint32_t>(a / C::kNumAcc) & 1u, &s_abort, tmo);
+          }
+          if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const float* sc = s_scale + i * BM;
 #pragma unroll
-          for (int c0 = 0; c0 < BM; c0 += 16) {
-            float v[16];
-            tmem_ld16(lane_addr + buf * C::kAccCols + c0, v);
+          for (int c0 = 0; c0 < BM; c0 += C::kLdCols) {
+            float v[C::kKbGroup][C::kLdCols];
+#pragma unroll
+            for (int g = 0; g < C::kKbGroup; ++g) {
+              if (g < ng) {
+                const uint32_t base = lane_addr + ((acc_n + g) % C::kNumAcc) * C::kAccCols + c0;
+#pragma unroll
+                for (int j = 0; j < C::kLdCols; j += 16)
+                  tmem_ld16(base + j, *reinterpret_cast<float(*)[16]>(&v[g][j]));
+              }
+            }
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[c0 + j] = fmaf(v[j], sc[c0 + j], acc[c0 + j]);
+            for (int g = 0; g < C::kKbGroup; ++g) {
+              if (g < ng) {
+                const float* scg = sc + (i + g) * BM + c0;
+#pragma unroll
+                for (int j = 0; j < C::kLdCols; ++j) acc[c0 + j] = fmaf(v[g][j], scg[j], acc[c0 + j]);
+              }
+            }
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[buf]));
-          ++acc_n;
+          if (lane == 0)
+            for (int g = 0; g < ng; ++g) mbar_arrive(smem_u32(&bar_tempty[(acc_n + g) % C::kNumAcc]));
+          acc_n += ng;
         }
         if (!ok) break;
-        const int col = d.n_tile * kTileN + row;
         if constexpr (kEpi == MOE_EPI_SCATTER) {
           float* out = static_cast<float*>(p.out);
 #pragma unroll
           for (int s = 0; s < BM; ++s) {
-            if (s < d.rows) red_add_f32(out + static_cast<size_t>(s_tok[s]) * p.N + col, s_wt[s] * acc[s]);
+            if (s < d.rows) red_add_f32(out + static_cast<size_t>(tok[s]) * p.N + col, wt[s] * acc[s]);
           }
-          if (p.out_bf16 != nullptr) finalize_segments(p, d, et, col, s_tok, s_fin);
         } else {
           float* out = static_cast<float*>(p.out);
 #pragma unroll
@@ -403,7 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const int col = d.n_tile * kTileN + row;
         for (int c0 = 0; c0 < BM && c0 < d.rows; c0 += 16) {
           float v[16];
           tmem_ld16(lane_addr + buf * C::kAccCols + c0, v);
@@ -428,8 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 16; ++j) {
               if (c0 + j < d.rows) {
                 if constexpr (kEpi == MOE_EPI_SCATTER)
-                  red_add_f32(out + static_cast<size_t>(s_tok[c0 + j]) * p.N + col,
-                              s_wt[c0 + j] * v[j]);
+                  red_add_f32(out + static_cast<size_t>(tok[c0 + j]) * p.N + col, wt[c0 + j] * v[j]);
                 else
                   out[static_cast<size_t>(d.m0 + c0 + j) * p.N + col] = v[j];
               }
@@ -440,10 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[buf]));
         ++acc_n;
-        if constexpr (kEpi == MOE_EPI_SCATTER) {
-          if (p.out_bf16 != nullptr) finalize_segments(p, d, et, col, s_tok, s_fin);
-        }
       }
+      // this tile's descriptor and metadata slot may now be reused
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bar_dempty[ds]));
+      if (++ds == kRing) { ds = 0; dphase ^= 1u; }
     }
     if (!ok) {
       set_error(p.ctrl, MOE_ERR_TIMEOUT, 3);
@@ -454,7 +482,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  pdl_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
@@ -474,8 +501,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // Host side: instantiations, launch.
-
-using KernelFn = void (*)(CUtensorMap, CUtensorMap, GemmParams);
 
 struct GemmVariant {
   const void* fn;
@@ -516,12 +541,14 @@ bool select_gemm_variant(bool fp8, int epi, int bm, GemmVariant& v) {
   return false;
 }
 
-constexpr int kSmemLimit = 232448;  // 227 KB per CTA
+int gemm_stage_bytes(bool fp8, int epi, int bm) {
+  GemmVariant v;
+  if (!select_gemm_variant(fp8, epi, bm, v)) return 0;
+  return v.stage_bytes;
+}
 
-int gemm_num_stages(int stage_bytes, int scale_bytes) {
-  int avail = kSmemLimit - 1024 - scale_bytes - 8192;  // alignment slack + static shared memory
-  int n = avail / stage_bytes;
-  return n > kMaxStages ? kMaxStages : n;
+int gemm_meta_bytes(bool fp8, int bm, int kb_per_split) {
+  return kRing * meta_slot_bytes(fp8, bm, kb_per_split);
 }
 
 cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_a,
@@ -529,10 +556,13 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
                                 cudaStream_t stream, bool pdl) {
   GemmVariant v;
   if (!select_gemm_variant(fp8, epi, bm, v)) return cudaErrorInvalidValue;
-  const int scale_bytes = fp8 ? p.kb_per_split * bm * 4 : 0;
-  const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * v.stage_bytes + scale_bytes;
+  const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * v.stage_bytes +
+                      gemm_meta_bytes(fp8, bm, p.kb_per_split);
   cudaError_t err = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
+  if (err == cudaSuccess)
+    err = cudaFuncSetAttribute(v.fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
@@ -547,12 +577,6 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
   void* args[] = {const_cast<CUtensorMap*>(&tmap_w), const_cast<CUtensorMap*>(&tmap_a),
                   const_cast<GemmParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, v.fn, args);
-}
-
-int gemm_stage_bytes(bool fp8, int epi, int bm) {
-  GemmVariant v;
-  if (!select_gemm_variant(fp8, epi, bm, v)) return 0;
-  return v.stage_bytes;
 }
 
 }  // namespace moe

@@ -9,7 +9,7 @@
 // Slot order inside an expert is deterministic: ascending route id
 // (t*top_k + j); the pages hand out slots with atomicAdd, in arbitrary order.
 //
-// Work split: warps 0..nw-1 own consecutive route ranges.  Pass 1 counts each
+// Work split: warps 0..nw-1 (nw <= 32) own consecutive route ranges.  Pass 1 counts each
 // range into the warp's private row of an [nw][E] shared histogram, grouping
 // equal ids of a 32-route step with __match_any_sync (no atomics).  Per expert
 // (one thread each), the rows become exclusive per-warp bases; counts and
@@ -24,9 +24,10 @@ namespace moe {
 
 constexpr int kLayoutThreads = 1024;
 
-// Warps that take part in the histogram passes: about 256 routes each.
+// Warps that take part in the histogram passes: about 32 routes each, so a
+// small layout is one step per warp.
 __host__ __device__ inline int layout_warps(int R) {
-  int nw = (R + 255) / 256;
+  int nw = (R + 31) / 32;
   return nw < 1 ? 1 : (nw > 32 ? 32 : nw);
 }
 
@@ -94,17 +95,32 @@ static __device__ void layout_block(const int32_t* ids, int R, int E, int block_
   const int r_end = warp < nw ? min(R, r_begin + chunk) : R;
   int* my_row = s_hist + (warp < nw ? warp : 0) * E;
 
-  // pass 1: per-warp histogram
-  for (int r0 = r_begin; r0 < r_end; r0 += 32) {
-    const int r = r0 + lane;
-    int e = r < r_end ? __ldcg(ids + r) : -1;
-    if (r < r_end && (e < 0 || e >= E)) {
-      s_bad = 1;
-      e = -2;  // excluded from the layout
+  // pass 1: per-warp histogram.  A warp walks its range in steps of 32
+  // routes; the ids of kBatch steps are loaded together so their latencies
+  // overlap.  When the whole range is one batch (R <= 32 * 32 * kBatch) the
+  // ids and match masks stay in registers for pass 2.
+  constexpr int kBatch = 8;
+  const bool one_batch = r_end - r_begin <= 32 * kBatch;
+  int eb[kBatch];
+  uint32_t mb[kBatch];
+  for (int b0 = r_begin; b0 < r_end; b0 += 32 * kBatch) {
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int r = b0 + 32 * j + lane;
+      eb[j] = r < r_end ? __ldcg(ids + r) : -1;
     }
-    const uint32_t same = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(same) - 1) my_row[e] += __popc(same);
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int r = b0 + 32 * j + lane;
+      if (b0 + 32 * j >= r_end) break;  // warp-uniform
+      if (r < r_end && (eb[j] < 0 || eb[j] >= E)) {
+        s_bad = 1;
+        eb[j] = -2;  // excluded from the layout
+      }
+      mb[j] = __match_any_sync(0xffffffffu, eb[j]);
+      if (eb[j] >= 0 && lane == __ffs(mb[j]) - 1) my_row[eb[j]] += __popc(mb[j]);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
@@ -135,22 +151,34 @@ static __device__ void layout_block(const int32_t* ids, int R, int E, int block_
 
   // pass 2: stable placement
   const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int r0 = r_begin; r0 < r_end; r0 += 32) {
-    const int r = r0 + lane;
-    int ex = r < r_end ? __ldcg(ids + r) : -1;
-    if (r < r_end && (ex < 0 || ex >= E)) ex = -2;
-    const uint32_t same = __match_any_sync(0xffffffffu, ex);
-    const int base = ex >= 0 ? my_row[ex] : 0;
-    __syncwarp();
-    if (ex >= 0) {
-      const int slot = base + __popc(same & lt_mask);
-      sorted_route_ids[slot] = r;
-      route_slot[r] = slot;
-      if (lane == __ffs(same) - 1) my_row[ex] = base + __popc(same);
-    } else if (ex == -2) {
-      route_slot[r] = -1;  // invalid id: the route has no slot
+  for (int b0 = r_begin; b0 < r_end; b0 += 32 * kBatch) {
+    if (!one_batch) {
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int r = b0 + 32 * j + lane;
+        int ex = r < r_end ? __ldcg(ids + r) : -1;
+        if (r < r_end && (ex < 0 || ex >= E)) ex = -2;
+        eb[j] = ex;
+      }
     }
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int r = b0 + 32 * j + lane;
+      if (b0 + 32 * j >= r_end) break;  // warp-uniform
+      const int ex = eb[j];
+      const uint32_t same = one_batch ? mb[j] : __match_any_sync(0xffffffffu, ex);
+      const int base = ex >= 0 ? my_row[ex] : 0;
+      __syncwarp();
+      if (ex >= 0) {
+        const int slot = base + __popc(same & lt_mask);
+        sorted_route_ids[slot] = r;
+        route_slot[r] = slot;
+        if (lane == __ffs(same) - 1) my_row[ex] = base + __popc(same);
+      } else if (ex == -2) {
+        route_slot[r] = -1;  // invalid id: the route has no slot
+      }
+      __syncwarp();
+    }
   }
   __syncthreads();
   if (tid == 0 && s_bad) set_error(ctrl, MOE_ERR_DEVICE_FAULT, 1);

@@ -21,6 +21,8 @@ using namespace moe;
 namespace {
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
+// L2 prefetch of FP8 expert weights issued at the start of a forward (bytes).
+constexpr long long kPrefetchBytes = 64ll << 20;
 int g_drop_producer = 0;
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 
@@ -135,7 +137,7 @@ int pick_k_splits(const moe_gemm_args* a, int sms, int KB) {
 }
 
 moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStream_t stream,
-                      bool pdl, void* out_bf16 = nullptr, unsigned* tile_cnt = nullptr) {
+                      bool pdl) {
   const bool fp8 = a->dtype == MOE_DTYPE_FP8_E4M3;
   const int sms = device_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
@@ -170,12 +172,10 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   p.sched = a->sched;
   p.drop_producer = g_drop_producer;
   p.timeout_ns = g_timeout_ns;
-  p.out_bf16 = a->epilogue == MOE_EPI_SCATTER ? out_bf16 : nullptr;
-  p.tile_cnt = tile_cnt;
   const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m);
   if (stage_bytes <= 0) return MOE_ERR_UNSUPPORTED;
-  const int scale_bytes = fp8 ? p.kb_per_split * a->block_m * 4 : 0;
-  int stages = (232448 - 1024 - 12288 - scale_bytes) / stage_bytes;
+  const int meta_bytes = gemm_meta_bytes(fp8, a->block_m, p.kb_per_split);
+  int stages = (232448 - 1024 - 12288 - meta_bytes) / stage_bytes;
   if (stages > 16) stages = 16;
   if (stages < 2) return MOE_ERR_UNSUPPORTED;
   p.num_stages = stages;
@@ -187,7 +187,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
 // ---------------------------------------------------------------------------
 // Workspace layout of the forward.
 struct WsLayout {
-  size_t ctrl, ids, weights, counts, offsets, tile_off, sorted, slot, a, a_scales, acc, cnt, h;
+  size_t ctrl, ids, weights, counts, offsets, tile_off, sorted, slot, a, a_scales, acc, h;
   size_t st_logits, st_x, st_out;
   size_t total;
 };
@@ -221,7 +221,6 @@ WsLayout ws_layout(const moe_forward_args* f) {
   L.a_scales = fp8 ? take((K / 128) * R * 4) : 0;
   const size_t out_cols = fp8 ? N : K;
   L.acc = take(M * out_cols * 4);
-  L.cnt = take(M * (out_cols / 128) * 4);
   L.h = fp8 ? 0 : take(R * N * 2);
   L.st_logits = take(M * E * 4);
   L.st_x = take(M * K * 2);
@@ -251,6 +250,41 @@ moe_status_t check_forward(const moe_forward_args* f) {
   return MOE_OK;
 }
 
+// A second stream for work that runs beside the forward's chain (captured
+// into the same graph as a parallel branch): fork() makes it wait for
+// `origin`, record_join() marks the end of its work, join() makes `origin`
+// wait for that end.  One stream and two events per device, created once.
+struct SideBranch {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+  moe_status_t fork(cudaStream_t origin) {
+    static cudaStream_t streams[64] = {};
+    static cudaEvent_t forks[64] = {}, joins[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    moe_status_t s = cuda_status(cudaGetDevice(&dev));
+    if (s != MOE_OK) return s;
+    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (streams[dev] == nullptr) {
+        s = cuda_status(cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking));
+        if (s == MOE_OK) s = cuda_status(cudaEventCreateWithFlags(&forks[dev], cudaEventDisableTiming));
+        if (s == MOE_OK) s = cuda_status(cudaEventCreateWithFlags(&joins[dev], cudaEventDisableTiming));
+        if (s != MOE_OK) return s;
+      }
+    }
+    stream = streams[dev];
+    fork_ev = forks[dev];
+    join_ev = joins[dev];
+    s = cuda_status(cudaEventRecord(fork_ev, origin));
+    if (s != MOE_OK) return s;
+    return cuda_status(cudaStreamWaitEvent(stream, fork_ev, 0));
+  }
+  moe_status_t record_join() { return cuda_status(cudaEventRecord(join_ev, stream)); }
+  moe_status_t join(cudaStream_t origin) { return cuda_status(cudaStreamWaitEvent(origin, join_ev, 0)); }
+};
+
 // The launch sequence of one forward (no host synchronisation).
 moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, const void* x,
                              void* out, uint8_t* ws, cudaStream_t stream) {
@@ -270,14 +304,27 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   const bool pdl = true;
   cudaError_t e;
 
+  // FP8: prefetch the first weights the GEMM will stream (expert order) into L2
+  // on a side branch (fork here, join after the finalize) while routing,
+  // layout and quantisation run.
+  const long long w_bytes = static_cast<long long>(E) * N * K;
+  const long long pf_bytes = fp8 ? (w_bytes < kPrefetchBytes ? w_bytes : kPrefetchBytes) : 0;
+  SideBranch side;
+  if (pf_bytes > 0) {
+    moe_status_t fs = side.fork(stream);
+    if (fs != MOE_OK) return fs;
+    e = launch_prefetch_l2(f->w, pf_bytes, side.stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    fs = side.record_join();
+    if (fs != MOE_OK) return fs;
+  }
   e = launch_route_layout(logits, M, E, k, f->softcap, f->renorm, ids, wts, bm, counts, offsets,
                           sorted, slot, tile_off, ctrl, stream, false);
   if (e != cudaSuccess) return cuda_status(e);
-  unsigned* cnt = reinterpret_cast<unsigned*>(ws + L.cnt);
   if (fp8) {
     uint8_t* a_q = ws + L.a;
     float* a_s = reinterpret_cast<float*>(ws + L.a_scales);
-    e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, cnt, N / 128, stream, pdl);
+    e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, stream, pdl);
     if (e != cudaSuccess) return cuda_status(e);
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));
@@ -301,12 +348,17 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     g.route_weights = wts;
     g.out = acc;
     g.k_splits = f->k_splits;
-    return run_gemm(&g, ctrl, false, stream, pdl, out, cnt);
+    moe_status_t s = run_gemm(&g, ctrl, false, stream, pdl);
+    if (s != MOE_OK) return s;
+    s = cuda_status(launch_finalize(acc, out, static_cast<size_t>(M) * N, device_sms(), stream,
+                                    pdl));
+    if (s != MOE_OK) return s;
+    return pf_bytes > 0 ? side.join(stream) : MOE_OK;
   }
   // BF16 gated FFN: gather -> up (SwiGLU) -> down (scatter) -> finalize
   void* a = ws + L.a;
   void* h = ws + L.h;
-  e = launch_gather_rows_bf16(x, M, K, k, slot, a, acc, K, cnt, K / 128, stream, pdl);
+  e = launch_gather_rows_bf16(x, M, K, k, slot, a, acc, K, stream, pdl);
   if (e != cudaSuccess) return cuda_status(e);
   moe_gemm_args g;
   std::memset(&g, 0, sizeof(g));
@@ -336,7 +388,10 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   g.sorted_route_ids = sorted;
   g.route_weights = wts;
   g.out = acc;
-  return run_gemm(&g, ctrl, true, stream, pdl, out, cnt);
+  s = run_gemm(&g, ctrl, true, stream, pdl);
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_finalize(acc, out, static_cast<size_t>(M) * K, device_sms(), stream,
+                                     pdl));
 }
 
 // ---------------------------------------------------------------------------
@@ -493,8 +548,7 @@ moe_status_t moe_quant_gather(const void* x, int M, int K, int top_k, const int3
   if (zero_acc != nullptr && (zero_cols <= 0 || zero_cols % 4 != 0 || !aligned16(zero_acc)))
     return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_quant_gather(x, M, K, top_k, route_slot, a_q, a_scales, zero_acc,
-                                         zero_cols, nullptr, 0, static_cast<cudaStream_t>(stream),
-                                         false));
+                                         zero_cols, static_cast<cudaStream_t>(stream), false));
 }
 
 moe_status_t moe_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_bytes, void* stream) {

@@ -5,6 +5,17 @@
 
 namespace moe {
 
+// Small kernels that run next to (or just before) the grouped GEMM ask for
+// the largest shared-memory carveout: an SM still holding one of their CTAs
+// can then take a GEMM CTA (210 KB of shared memory) without first draining
+// to change its L1/shared split.
+template <typename F>
+inline cudaError_t prefer_max_shared(F* kernel) {
+  return cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
+                              cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
 // Parameters of one grouped-GEMM launch (beyond the two TMA descriptors).
 struct GemmParams {
   const float* a_scales;        // FP8: [KB, R]
@@ -25,12 +36,6 @@ struct GemmParams {
   int num_stages;
   int drop_producer;
   unsigned long long timeout_ns;
-  // SCATTER only, optional: when out_bf16 is set, the CTA that adds the last
-  // contribution to a (token, 128-column tile) of the fp32 output rounds that
-  // segment to bf16 into out_bf16; tile_cnt[M * n_tiles] counts contributions
-  // and must be zero at launch (top_k * k_splits arrive per entry).
-  void* out_bf16;
-  unsigned* tile_cnt;
 };
 
 cudaError_t launch_route(const float* logits, int M, int E, int k, float softcap, int renorm,
@@ -43,18 +48,21 @@ cudaError_t launch_route_layout(const float* logits, int M, int E, int k, float 
                                 int32_t* counts, int32_t* offsets, int32_t* sorted_route_ids,
                                 int32_t* route_slot, int32_t* tile_offsets, Ctrl* ctrl,
                                 cudaStream_t stream, bool pdl);
+cudaError_t launch_prefetch_l2(const void* base, long long bytes, cudaStream_t stream);
+cudaError_t launch_finalize(const float* acc, void* out, size_t n, int num_sms,
+                            cudaStream_t stream, bool pdl);
 cudaError_t launch_quant_gather(const void* x, int M, int K, int k, const int32_t* route_slot,
                                 uint8_t* a_q, float* a_scales, float* zero_acc, int zero_cols,
-                                unsigned* zero_cnt, int cnt_per_token, cudaStream_t stream,
-                                bool pdl);
+                                cudaStream_t stream, bool pdl);
 cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const float* weights,
                            int M, int N, int k, void* out, cudaStream_t stream);
 cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, const int32_t* route_slot,
-                                    void* a, float* zero_acc, int zero_cols, unsigned* zero_cnt,
-                                    int cnt_per_token, cudaStream_t stream, bool pdl);
+                                    void* a, float* zero_acc, int zero_cols, cudaStream_t stream,
+                                    bool pdl);
 cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_a,
                                 const GemmParams& p, bool fp8, int epi, int bm, int num_ctas,
                                 cudaStream_t stream, bool pdl);
 int gemm_stage_bytes(bool fp8, int epi, int bm);
+int gemm_meta_bytes(bool fp8, int bm, int kb_per_split);
 
 }  // namespace moe

@@ -29,7 +29,7 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
 __global__ void __launch_bounds__(1024) quant_gather_kernel(
     const __nv_bfloat16* __restrict__ x, int M, int K, int k, const int32_t* __restrict__ route_slot,
     uint8_t* __restrict__ a_q, float* __restrict__ a_scales, float* __restrict__ zero_acc,
-    int zero_cols, unsigned* __restrict__ zero_cnt, int cnt_per_token) {
+    int zero_cols) {
   const int G = K >> 4;                            // threads per token
   const int tpc = max(1, static_cast<int>(blockDim.x) / G);  // tokens per CTA
   const int t = blockIdx.x * tpc + threadIdx.x / G;
@@ -38,15 +38,14 @@ __global__ void __launch_bounds__(1024) quant_gather_kernel(
   // Idle threads (past the last token) still take part in the shuffles.
   const bool valid = threadIdx.x < tpc * G && t < M;
 
-  pdl_wait();
+  // let the grouped GEMM's CTAs start their setup now; they wait for this grid
   pdl_launch_dependents();
+  pdl_wait();
 
   if (valid && zero_acc != nullptr) {
     float4* row = reinterpret_cast<float4*>(zero_acc + static_cast<size_t>(t) * zero_cols);
     for (int i = c; i < (zero_cols >> 2); i += G) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (valid && zero_cnt != nullptr)
-    for (int i = c; i < cnt_per_token; i += G) zero_cnt[static_cast<size_t>(t) * cnt_per_token + i] = 0u;
 
   uint4 raw0 = make_uint4(0u, 0u, 0u, 0u), raw1 = raw0;
   if (valid) {
@@ -100,8 +99,7 @@ __global__ void __launch_bounds__(1024) quant_gather_kernel(
 
 cudaError_t launch_quant_gather(const void* x, int M, int K, int k, const int32_t* route_slot,
                                 uint8_t* a_q, float* a_scales, float* zero_acc, int zero_cols,
-                                unsigned* zero_cnt, int cnt_per_token, cudaStream_t stream,
-                                bool pdl) {
+                                cudaStream_t stream, bool pdl) {
   const int G = K / 16;
   int threads, tpc;
   if (G <= 256) {
@@ -111,6 +109,8 @@ cudaError_t launch_quant_gather(const void* x, int M, int K, int k, const int32_
     threads = (G + 31) / 32 * 32;  // K <= 16384
     tpc = 1;
   }
+  cudaError_t err = prefer_max_shared(quant_gather_kernel);
+  if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((M + tpc - 1) / tpc);
   cfg.blockDim = dim3(threads);
@@ -121,8 +121,7 @@ cudaError_t launch_quant_gather(const void* x, int M, int K, int k, const int32_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, quant_gather_kernel, static_cast<const __nv_bfloat16*>(x), M, K,
-                            k, route_slot, a_q, a_scales, zero_acc, zero_cols, zero_cnt,
-                            cnt_per_token);
+                            k, route_slot, a_q, a_scales, zero_acc, zero_cols);
 }
 
 }  // namespace moe

@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
                    ids + static_cast<size_t>(t) * k, weights + static_cast<size_t>(t) * k);
 }
 
-// Route + layout in one launch: every CTA routes 32 tokens (a warp each);
+// Route + layout in one launch: every CTA routes tokens_per_cta tokens (a
+// warp each; 8 for small batches so the routing spreads over more SMs);
 // the CTA that finishes last (an arrival counter in the control block) then
 // builds the layout of all routes (layout_block.cuh) and re-arms the counter.
 template <int NPL>
@@ -190,23 +191,29 @@ __global__ void __launch_bounds__(kLayoutThreads, 1)
                         int renorm, int32_t* ids, float* __restrict__ weights, int block_m,
                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                         int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ route_slot,
-                        int32_t* __restrict__ tile_offsets, Ctrl* ctrl) {
+                        int32_t* __restrict__ tile_offsets, Ctrl* ctrl, int tokens_per_cta) {
   extern __shared__ int s_hist[];
   __shared__ int s_last;
   pdl_wait();
   pdl_launch_dependents();
-  const int t = blockIdx.x * (kLayoutThreads / 32) + (threadIdx.x >> 5);
-  if (t < M)
+  const int w = threadIdx.x >> 5;
+  const int t = blockIdx.x * tokens_per_cta + w;
+  if (w < tokens_per_cta && t < M)
     route_token<NPL>(logits + static_cast<size_t>(t) * E, E, k, softcap, renorm,
                      ids + static_cast<size_t>(t) * k, weights + static_cast<size_t>(t) * k);
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();  // this CTA's ids are visible before it is counted
-    s_last = atomicAdd(&ctrl->route_done, 1u) == gridDim.x - 1;
+    // acq_rel arrival: releases this CTA's ids and weights (ordered before it
+    // by the barrier) and, for the last CTA, acquires every other CTA's
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(&ctrl->route_done)
+                 : "memory");
+    s_last = prev == gridDim.x - 1;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   layout_block(ids, M * k, E, block_m, counts, offsets, sorted_route_ids, route_slot,
                tile_offsets, ctrl, s_hist);
   if (threadIdx.x == 0) ctrl->route_done = 0u;
@@ -235,6 +242,23 @@ cudaError_t launch_route(const float* logits, int M, int E, int k, float softcap
   return cudaLaunchKernelEx(&cfg, route_kernel<32>, logits, M, E, k, softcap, renorm, ids, weights);
 }
 
+// Speculative L2 prefetch of the first `bytes` of the expert weights.  The
+// grouped GEMM hands out tiles in expert order, so these are the first
+// weights it streams; the forward runs this kernel on a side branch while
+// routing, layout and quantisation run, so HBM is busy from the start.
+__global__ void __launch_bounds__(32) prefetch_l2_kernel(const uint8_t* __restrict__ base,
+                                                         long long bytes) {
+  constexpr long long kChunk = 64 * 1024;
+  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long per = (bytes / nthreads + kChunk - 1) / kChunk * kChunk;
+  const long long begin = per * (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+  const long long end = min(bytes, begin + per);
+  for (long long off = begin; off < end; off += kChunk) {
+    const unsigned n = static_cast<unsigned>(min(kChunk, end - off));
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(n) : "memory");
+  }
+}
+
 template <int NPL>
 cudaError_t launch_route_layout_t(const float* logits, int M, int E, int k, float softcap,
                                   int renorm, int32_t* ids, float* weights, int block_m,
@@ -245,9 +269,11 @@ cudaError_t launch_route_layout_t(const float* logits, int M, int E, int k, floa
   cudaError_t err = cudaFuncSetAttribute(route_layout_kernel<NPL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
+  if (err == cudaSuccess) err = prefer_max_shared(route_layout_kernel<NPL>);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((M + 31) / 32);
+  const int tpc = M <= 8 * 160 ? 8 : 32;
+  cfg.gridDim = dim3((M + tpc - 1) / tpc);
   cfg.blockDim = dim3(kLayoutThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -258,7 +284,7 @@ cudaError_t launch_route_layout_t(const float* logits, int M, int E, int k, floa
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, route_layout_kernel<NPL>, logits, M, E, k, softcap, renorm, ids,
                             weights, block_m, counts, offsets, sorted_route_ids, route_slot,
-                            tile_offsets, ctrl);
+                            tile_offsets, ctrl, tpc);
 }
 
 cudaError_t launch_route_layout(const float* logits, int M, int E, int k, float softcap,
@@ -278,6 +304,14 @@ cudaError_t launch_route_layout(const float* logits, int M, int E, int k, float 
   if (npl <= 16) MOE_RL(16);
   MOE_RL(32);
 #undef MOE_RL
+}
+
+cudaError_t launch_prefetch_l2(const void* base, long long bytes, cudaStream_t stream) {
+  if (bytes <= 0) return cudaSuccess;
+  cudaError_t err = prefer_max_shared(prefetch_l2_kernel);
+  if (err != cudaSuccess) return err;
+  prefetch_l2_kernel<<<8, 32, 0, stream>>>(static_cast<const uint8_t*>(base), bytes & ~15ll);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -1,4 +1,8 @@
 // Output-side glue of the forward:
+//  - finalize: the fp32 accumulator that the grouped GEMM's scatter epilogue
+//    adds into is rounded once to bf16 (round to nearest even).  It is
+//    launched as a programmatic dependent of the GEMM, which triggers early,
+//    so its CTAs are resident and start converting as soon as the GEMM ends;
 //  - scatter: the unfused weighted scatter of "Fused MoE FP8: 8.09 -> 13.18
 //    TFLOPS (1.63x)", section "Baseline: 7 kernels" item 7, written as a
 //    deterministic gather per token (sum over j in order, fp32);
@@ -11,6 +15,22 @@
 
 namespace moe {
 namespace {
+
+__global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ acc,
+                                                       uint2* __restrict__ out, size_t n4) {
+  pdl_wait();
+  pdl_launch_dependents();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 v = __ldcg(acc + i);
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&a);
+    o.y = *reinterpret_cast<uint32_t*>(&b);
+    out[i] = o;
+  }
+}
 
 __global__ void __launch_bounds__(256) scatter_kernel(const float* __restrict__ rows,
                                                       const int32_t* __restrict__ route_slot,
@@ -39,11 +59,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                           const int32_t* __restrict__ route_slot,
                                                           uint4* __restrict__ a,
                                                           float* __restrict__ zero_acc,
-                                                          int zero_cols,
-                                                          unsigned* __restrict__ zero_cnt,
-                                                          int cnt_per_token) {
-  pdl_wait();
+                                                          int zero_cols) {
   pdl_launch_dependents();
+  pdl_wait();
   const int t = blockIdx.x;
   if (t >= M) return;
   const int R = M * k;
@@ -52,9 +70,6 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     for (int i = threadIdx.x; i < (zero_cols >> 2); i += blockDim.x)
       row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (zero_cnt != nullptr)
-    for (int i = threadIdx.x; i < cnt_per_token; i += blockDim.x)
-      zero_cnt[static_cast<size_t>(t) * cnt_per_token + i] = 0u;
   int slots[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j)
@@ -83,6 +98,19 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t stream, bool pdl
 
 }  // namespace
 
+cudaError_t launch_finalize(const float* acc, void* out, size_t n, int num_sms,
+                            cudaStream_t stream, bool pdl) {
+  const size_t n4 = n / 4;
+  int blocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, static_cast<size_t>(num_sms)));
+  if (blocks < 1) blocks = 1;
+  cudaError_t err = prefer_max_shared(finalize_kernel);
+  if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(blocks), dim3(256), stream, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, finalize_kernel, reinterpret_cast<const float4*>(acc),
+                            static_cast<uint2*>(out), n4);
+}
+
 cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const float* weights,
                            int M, int N, int k, void* out, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
@@ -92,13 +120,14 @@ cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const f
 }
 
 cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, const int32_t* route_slot,
-                                    void* a, float* zero_acc, int zero_cols, unsigned* zero_cnt,
-                                    int cnt_per_token, cudaStream_t stream, bool pdl) {
+                                    void* a, float* zero_acc, int zero_cols, cudaStream_t stream,
+                                    bool pdl) {
+  cudaError_t err = prefer_max_shared(gather_rows_kernel);
+  if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(256), stream, pdl, attr);
   return cudaLaunchKernelEx(&cfg, gather_rows_kernel, static_cast<const uint4*>(x), M, K / 8, k,
-                            route_slot, static_cast<uint4*>(a), zero_acc, zero_cols, zero_cnt,
-                            cnt_per_token);
+                            route_slot, static_cast<uint4*>(a), zero_acc, zero_cols);
 }
 
 }  // namespace moe
