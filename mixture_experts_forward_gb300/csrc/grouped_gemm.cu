@@ -327,13 +327,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if constexpr (kFP8) {
+          // scale products for up to 16 K blocks at a time, all loads in flight together
+          constexpr int kRows = (BM + 31) / 32;  // rows of the tile per lane
           const float* wsc = p.w_scales + (static_cast<size_t>(d.e) * NB + d.n_tile) * p.KB + d.kb0;
-          for (int idx = lane; idx < d.nkb * BM; idx += 32) {
-            const int kb = idx / BM, s = idx - kb * BM;
-            float v = 0.0f;
-            if (s < d.rows)
-              v = __ldg(p.a_scales + static_cast<size_t>(d.kb0 + kb) * p.R + d.m0 + s) * __ldg(wsc + kb);
-            sc[idx] = v;
+          const float* asc = p.a_scales + static_cast<size_t>(d.kb0) * p.R + d.m0;
+          for (int kb0 = 0; kb0 < d.nkb; kb0 += 16) {
+            float va[16][kRows];
+            float vb[16];
+#pragma unroll
+            for (int kb = 0; kb < 16; ++kb) {
+              vb[kb] = kb0 + kb < d.nkb ? __ldg(wsc + kb0 + kb) : 0.0f;
+#pragma unroll
+              for (int j = 0; j < kRows; ++j) {
+                const int s = lane + 32 * j;
+                va[kb][j] = (kb0 + kb < d.nkb && s < d.rows)
+                                ? __ldg(asc + static_cast<size_t>(kb0 + kb) * p.R + s)
+                                : 0.0f;
+              }
+            }
+#pragma unroll
+            for (int kb = 0; kb < 16; ++kb) {
+#pragma unroll
+              for (int j = 0; j < kRows; ++j) {
+                const int s = lane + 32 * j;
+                if (kb0 + kb < d.nkb && s < BM) sc[(kb0 + kb) * BM + s] = va[kb][j] * vb[kb];
+              }
+            }
           }
         }
       }

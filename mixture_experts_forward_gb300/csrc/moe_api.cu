@@ -318,13 +318,23 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     fs = side.record_join();
     if (fs != MOE_OK) return fs;
   }
-  e = launch_route_layout(logits, M, E, k, f->softcap, f->renorm, ids, wts, bm, counts, offsets,
-                          sorted, slot, tile_off, ctrl, stream, false);
+  const bool small = fp8 && quant_layout_fits(M, K, k, E);
+  if (small) {
+    // small batch: route, then quantise + layout + gather in one kernel
+    e = launch_route(logits, M, E, k, f->softcap, f->renorm, ids, wts, stream, false);
+  } else {
+    e = launch_route_layout(logits, M, E, k, f->softcap, f->renorm, ids, wts, bm, counts,
+                            offsets, sorted, slot, tile_off, ctrl, stream, false);
+  }
   if (e != cudaSuccess) return cuda_status(e);
   if (fp8) {
     uint8_t* a_q = ws + L.a;
     float* a_s = reinterpret_cast<float*>(ws + L.a_scales);
-    e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, stream, pdl);
+    if (small)
+      e = launch_quant_layout(x, M, K, k, E, bm, ids, a_q, a_s, acc, N, counts, offsets, sorted,
+                              slot, tile_off, ctrl, stream, pdl);
+    else
+      e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, stream, pdl);
     if (e != cudaSuccess) return cuda_status(e);
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));

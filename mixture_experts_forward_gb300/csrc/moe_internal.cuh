@@ -49,6 +49,15 @@ cudaError_t launch_route_layout(const float* logits, int M, int E, int k, float 
                                 int32_t* route_slot, int32_t* tile_offsets, Ctrl* ctrl,
                                 cudaStream_t stream, bool pdl);
 cudaError_t launch_prefetch_l2(const void* base, long long bytes, cudaStream_t stream);
+// Largest M * top_k for which the forward folds the layout into the
+// quantise/gather kernel (every CTA scans all routes' expert ids).
+constexpr int kQuantLayoutMaxRoutes = 4096;
+bool quant_layout_fits(int M, int K, int k, int E);
+cudaError_t launch_quant_layout(const void* x, int M, int K, int k, int E, int block_m,
+                                const int32_t* ids, uint8_t* a_q, float* a_scales, float* zero_acc,
+                                int zero_cols, int32_t* counts, int32_t* offsets,
+                                int32_t* sorted_route_ids, int32_t* route_slot,
+                                int32_t* tile_offsets, Ctrl* ctrl, cudaStream_t stream, bool pdl);
 cudaError_t launch_finalize(const float* acc, void* out, size_t n, int num_sms,
                             cudaStream_t stream, bool pdl);
 cudaError_t launch_quant_gather(const void* x, int M, int K, int k, const int32_t* route_slot,

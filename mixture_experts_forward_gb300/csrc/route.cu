@@ -224,6 +224,13 @@ __global__ void __launch_bounds__(kLayoutThreads, 1)
 cudaError_t launch_route(const float* logits, int M, int E, int k, float softcap, int renorm,
                          int32_t* ids, float* weights, cudaStream_t stream, bool pdl) {
   const int warps = 8;
+  cudaError_t err = prefer_max_shared(route_kernel<1>);
+  if (err == cudaSuccess) err = prefer_max_shared(route_kernel<2>);
+  if (err == cudaSuccess) err = prefer_max_shared(route_kernel<4>);
+  if (err == cudaSuccess) err = prefer_max_shared(route_kernel<8>);
+  if (err == cudaSuccess) err = prefer_max_shared(route_kernel<16>);
+  if (err == cudaSuccess) err = prefer_max_shared(route_kernel<32>);
+  if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((M + warps - 1) / warps);
   cfg.blockDim = dim3(32 * warps);
