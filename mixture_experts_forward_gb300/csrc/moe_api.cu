@@ -188,6 +188,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
 // Workspace layout of the forward.
 struct WsLayout {
   size_t ctrl, ids, weights, counts, offsets, tile_off, sorted, slot, a, a_scales, acc, h;
+  size_t local_rank, cta_hist, cta_base;
   size_t st_logits, st_x, st_out;
   size_t total;
 };
@@ -217,6 +218,10 @@ WsLayout ws_layout(const moe_forward_args* f) {
   L.tile_off = take((E + 1) * 4);
   L.sorted = take(R * 4);
   L.slot = take(R * 4);
+  const size_t n_rank_ctas = (M + kRankTokensPerCta - 1) / kRankTokensPerCta;
+  L.local_rank = take(R * 4);
+  L.cta_hist = take(n_rank_ctas * E * 4);
+  L.cta_base = take(n_rank_ctas * E * 4);
   L.a = take(fp8 ? R * K : R * K * 2);
   L.a_scales = fp8 ? take((K / 128) * R * 4) : 0;
   const size_t out_cols = fp8 ? N : K;
@@ -323,8 +328,19 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     // small batch: route, then quantise + layout + gather in one kernel
     e = launch_route(logits, M, E, k, f->softcap, f->renorm, ids, wts, stream, false);
   } else {
-    e = launch_route_layout(logits, M, E, k, f->softcap, f->renorm, ids, wts, bm, counts,
-                            offsets, sorted, slot, tile_off, ctrl, stream, false);
+    e = launch_route_rank(logits, M, E, k, f->softcap, f->renorm, ids, wts, bm, counts, offsets,
+                          tile_off, ctrl, reinterpret_cast<int32_t*>(ws + L.local_rank),
+                          reinterpret_cast<int32_t*>(ws + L.cta_hist),
+                          reinterpret_cast<int32_t*>(ws + L.cta_base), stream, false);
+  }
+  Placement pl;  // large batches: the gather kernels place the routes
+  if (!small) {
+    pl.ids = ids;
+    pl.local_rank = reinterpret_cast<const int32_t*>(ws + L.local_rank);
+    pl.cta_base = reinterpret_cast<const int32_t*>(ws + L.cta_base);
+    pl.offsets = offsets;
+    pl.sorted_route_ids = sorted;
+    pl.E = E;
   }
   if (e != cudaSuccess) return cuda_status(e);
   if (fp8) {
@@ -334,7 +350,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
       e = launch_quant_layout(x, M, K, k, E, bm, ids, a_q, a_s, acc, N, counts, offsets, sorted,
                               slot, tile_off, ctrl, stream, pdl);
     else
-      e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, stream, pdl);
+      e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, pl, stream, pdl);
     if (e != cudaSuccess) return cuda_status(e);
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));
@@ -365,10 +381,11 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     if (s != MOE_OK) return s;
     return pf_bytes > 0 ? side.join(stream) : MOE_OK;
   }
-  // BF16 gated FFN: gather -> up (SwiGLU) -> down (scatter) -> finalize
+  // BF16 gated FFN: (route + rank above) -> gather, placing the routes -> up (SwiGLU)
+  // -> down (scatter) -> finalize
   void* a = ws + L.a;
   void* h = ws + L.h;
-  e = launch_gather_rows_bf16(x, M, K, k, slot, a, acc, K, stream, pdl);
+  e = launch_gather_rows_bf16(x, M, K, k, slot, a, acc, K, pl, stream, pdl);
   if (e != cudaSuccess) return cuda_status(e);
   moe_gemm_args g;
   std::memset(&g, 0, sizeof(g));
@@ -557,8 +574,9 @@ moe_status_t moe_quant_gather(const void* x, int M, int K, int top_k, const int3
   if (!aligned16(x) || !aligned16(a_q)) return MOE_ERR_INVALID_ARG;
   if (zero_acc != nullptr && (zero_cols <= 0 || zero_cols % 4 != 0 || !aligned16(zero_acc)))
     return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_quant_gather(x, M, K, top_k, route_slot, a_q, a_scales, zero_acc,
-                                         zero_cols, static_cast<cudaStream_t>(stream), false));
+  return cuda_status(launch_quant_gather(x, M, K, top_k, const_cast<int32_t*>(route_slot), a_q,
+                                         a_scales, zero_acc, zero_cols, Placement(),
+                                         static_cast<cudaStream_t>(stream), false));
 }
 
 moe_status_t moe_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_bytes, void* stream) {

@@ -43,11 +43,27 @@ cudaError_t launch_route(const float* logits, int M, int E, int k, float softcap
 cudaError_t launch_layout(const int32_t* ids, int R, int E, int block_m, int32_t* counts,
                           int32_t* offsets, int32_t* sorted_route_ids, int32_t* route_slot,
                           int32_t* tile_offsets, Ctrl* ctrl, cudaStream_t stream, bool pdl);
-cudaError_t launch_route_layout(const float* logits, int M, int E, int k, float softcap,
-                                int renorm, int32_t* ids, float* weights, int block_m,
-                                int32_t* counts, int32_t* offsets, int32_t* sorted_route_ids,
-                                int32_t* route_slot, int32_t* tile_offsets, Ctrl* ctrl,
-                                cudaStream_t stream, bool pdl);
+// Route + per-CTA ranking of 32-token groups; the last CTA writes the per-CTA
+// bases, counts, offsets and tile offsets (see Placement).
+cudaError_t launch_route_rank(const float* logits, int M, int E, int k, float softcap, int renorm,
+                              int32_t* ids, float* weights, int block_m, int32_t* counts,
+                              int32_t* offsets, int32_t* tile_offsets, Ctrl* ctrl,
+                              int32_t* local_rank, int32_t* cta_hist, int32_t* cta_base,
+                              cudaStream_t stream, bool pdl);
+
+// How a gather kernel finds the slot of route r = t*k + j: from route_slot
+// (cta_base == nullptr), or — after launch_route_rank — as
+// offsets[e] + cta_base[(t / 32) * E + e] + local_rank[r] with e = ids[r], in
+// which case the kernel also writes route_slot[r] and sorted_route_ids[slot].
+struct Placement {
+  const int32_t* ids = nullptr;
+  const int32_t* local_rank = nullptr;
+  const int32_t* cta_base = nullptr;
+  const int32_t* offsets = nullptr;
+  int32_t* sorted_route_ids = nullptr;
+  int E = 0;
+};
+constexpr int kRankTokensPerCta = 32;
 cudaError_t launch_prefetch_l2(const void* base, long long bytes, cudaStream_t stream);
 // Largest M * top_k for which the forward folds the layout into the
 // quantise/gather kernel (every CTA scans all routes' expert ids).
@@ -60,14 +76,14 @@ cudaError_t launch_quant_layout(const void* x, int M, int K, int k, int E, int b
                                 int32_t* tile_offsets, Ctrl* ctrl, cudaStream_t stream, bool pdl);
 cudaError_t launch_finalize(const float* acc, void* out, size_t n, int num_sms,
                             cudaStream_t stream, bool pdl);
-cudaError_t launch_quant_gather(const void* x, int M, int K, int k, const int32_t* route_slot,
+cudaError_t launch_quant_gather(const void* x, int M, int K, int k, int32_t* route_slot,
                                 uint8_t* a_q, float* a_scales, float* zero_acc, int zero_cols,
-                                cudaStream_t stream, bool pdl);
+                                const Placement& pl, cudaStream_t stream, bool pdl);
 cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const float* weights,
                            int M, int N, int k, void* out, cudaStream_t stream);
-cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, const int32_t* route_slot,
-                                    void* a, float* zero_acc, int zero_cols, cudaStream_t stream,
-                                    bool pdl);
+cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, int32_t* route_slot,
+                                    void* a, float* zero_acc, int zero_cols, const Placement& pl,
+                                    cudaStream_t stream, bool pdl);
 cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_a,
                                 const GemmParams& p, bool fp8, int epi, int bm, int num_ctas,
                                 cudaStream_t stream, bool pdl);

@@ -19,13 +19,30 @@
 namespace moe {
 namespace {
 
+// Slot of route r (see Placement); writes route_slot / sorted_route_ids when placing.
+__device__ __forceinline__ int route_slot_of(int r, int t, const int32_t* route_slot_in,
+                                             int32_t* route_slot, const Placement& pl, int R) {
+  if (pl.cta_base == nullptr) return __ldg(route_slot_in + r);
+  const int e = __ldg(pl.ids + r);
+  if (e < 0 || e >= pl.E) return -1;
+  const int slot = __ldg(pl.offsets + e) +
+                   __ldg(pl.cta_base + static_cast<size_t>(t / kRankTokensPerCta) * pl.E + e) +
+                   __ldg(pl.local_rank + r);
+  if (slot < 0 || slot >= R) return -1;
+  route_slot[r] = slot;
+  pl.sorted_route_ids[slot] = r;
+  return slot;
+}
+
 __global__ void __launch_bounds__(1024) quant_gather_kernel(
-    const __nv_bfloat16* __restrict__ x, int M, int K, int k, const int32_t* __restrict__ route_slot,
+    const __nv_bfloat16* __restrict__ x, int M, int K, int k, int32_t* route_slot,
     uint8_t* __restrict__ a_q, float* __restrict__ a_scales, float* __restrict__ zero_acc,
-    int zero_cols) {
+    int zero_cols, const Placement pl) {
+  __shared__ int s_slot[1024];
   const int G = K >> 4;                            // threads per token
   const int tpc = max(1, static_cast<int>(blockDim.x) / G);  // tokens per CTA
-  const int t = blockIdx.x * tpc + threadIdx.x / G;
+  const int lt = static_cast<int>(threadIdx.x) / G;
+  const int t = blockIdx.x * tpc + lt;
   const int c = threadIdx.x % G;
   const int R = M * k;
   // Idle threads (past the last token) still take part in the shuffles.
@@ -33,21 +50,24 @@ __global__ void __launch_bounds__(1024) quant_gather_kernel(
 
   // let the grouped GEMM's CTAs start their setup now; they wait for this grid
   pdl_launch_dependents();
-  pdl_wait();
-
+  // x does not depend on the previous kernel: clear the accumulator rows and
+  // quantise before waiting for it
   if (valid && zero_acc != nullptr) {
     float4* row = reinterpret_cast<float4*>(zero_acc + static_cast<size_t>(t) * zero_cols);
     for (int i = c; i < (zero_cols >> 2); i += G) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-
   uint4 q;
   float s;
   quantize16(x + static_cast<size_t>(valid ? t : 0) * K, c, valid, q, s);
+  pdl_wait();
+
+  if (valid && c < k) s_slot[lt * k + c] = route_slot_of(t * k + c, t, route_slot, route_slot, pl, R);
+  __syncthreads();
   if (!valid) return;
 
   const int b = c >> 3;  // 128-element block of this thread
   for (int j = 0; j < k; ++j) {
-    const int slot = __ldg(route_slot + static_cast<size_t>(t) * k + j);
+    const int slot = s_slot[lt * k + j];
     if (slot < 0 || slot >= R) continue;
     *reinterpret_cast<uint4*>(a_q + static_cast<size_t>(slot) * K + 16 * c) = q;
     if ((c & 7) == 0) a_scales[static_cast<size_t>(b) * R + slot] = s;
@@ -211,9 +231,9 @@ __global__ void __launch_bounds__(1024) quant_layout_kernel(
 
 }  // namespace
 
-cudaError_t launch_quant_gather(const void* x, int M, int K, int k, const int32_t* route_slot,
+cudaError_t launch_quant_gather(const void* x, int M, int K, int k, int32_t* route_slot,
                                 uint8_t* a_q, float* a_scales, float* zero_acc, int zero_cols,
-                                cudaStream_t stream, bool pdl) {
+                                const Placement& pl, cudaStream_t stream, bool pdl) {
   const int G = K / 16;
   int threads, tpc;
   if (G <= 256) {
@@ -235,7 +255,7 @@ cudaError_t launch_quant_gather(const void* x, int M, int K, int k, const int32_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, quant_gather_kernel, static_cast<const __nv_bfloat16*>(x), M, K,
-                            k, route_slot, a_q, a_scales, zero_acc, zero_cols);
+                            k, route_slot, a_q, a_scales, zero_acc, zero_cols, pl);
 }
 
 bool quant_layout_fits(int M, int K, int k, int E) {

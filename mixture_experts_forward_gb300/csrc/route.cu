@@ -84,9 +84,9 @@ __device__ __forceinline__ uint32_t order_key(float z) {
 // Routes one token with one warp.  NPL = experts per lane (E <= 32 * NPL);
 // lane l owns experts l, l+32, ...
 template <int NPL>
-__device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k,
-                                            float softcap, int renorm, int32_t* __restrict__ ids,
-                                            float* __restrict__ weights) {
+__device__ __forceinline__ int route_token(const float* __restrict__ row, int E, int k,
+                                           float softcap, int renorm, int32_t* __restrict__ ids,
+                                           float* __restrict__ weights) {
   const int lane = threadIdx.x & 31;
   float z[NPL];
   uint32_t key[NPL];
@@ -166,6 +166,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ row, int E
     ids[lane] = my_id;
     weights[lane] = __fdiv_rn(my_e, s);
   }
+  return my_id;  // lane j < k: the j-th selected expert
 }
 
 template <int NPL>
@@ -181,30 +182,56 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
                    ids + static_cast<size_t>(t) * k, weights + static_cast<size_t>(t) * k);
 }
 
-// Route + layout in one launch: every CTA routes tokens_per_cta tokens (a
-// warp each; 8 for small batches so the routing spreads over more SMs);
-// the CTA that finishes last (an arrival counter in the control block) then
-// builds the layout of all routes (layout_block.cuh) and re-arms the counter.
+// Large batches: route + per-CTA ranking, and in the last CTA the expert
+// offsets.  Every CTA routes 32 tokens (a warp each).  The k experts of one
+// token are distinct, so the rank of route (t, j) among this CTA's routes to
+// its expert e is the number of earlier tokens of the CTA that chose e: a
+// per-warp 0/1 row of a [32][E] shared table, prefix-summed over the warps.
+// The CTA publishes its per-expert totals (cta_hist[cta][E]) and the ranks
+// (local_rank[R]).  The CTA that arrives last (acq_rel counter) turns the
+// totals into per-CTA bases (cta_base[cta][E], exclusive over the CTAs, several
+// threads per expert), counts, offsets and tile offsets.  The quantise/gather
+// kernel then places route r of expert e at
+// offsets[e] + cta_base[cta(r)][e] + local_rank[r] — the stable layout by
+// route id.
 template <int NPL>
 __global__ void __launch_bounds__(kLayoutThreads, 1)
-    route_layout_kernel(const float* __restrict__ logits, int M, int E, int k, float softcap,
-                        int renorm, int32_t* ids, float* __restrict__ weights, int block_m,
-                        int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                        int32_t* __restrict__ sorted_route_ids, int32_t* __restrict__ route_slot,
-                        int32_t* __restrict__ tile_offsets, Ctrl* ctrl, int tokens_per_cta) {
-  extern __shared__ int s_hist[];
+    route_rank_kernel(const float* __restrict__ logits, int M, int E, int k, float softcap,
+                      int renorm, int32_t* ids, float* __restrict__ weights, int block_m,
+                      int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                      int32_t* __restrict__ tile_offsets, Ctrl* ctrl, int32_t* local_rank,
+                      int32_t* cta_hist, int32_t* __restrict__ cta_base) {
+  extern __shared__ int s_tab[];  // [32][E]
   __shared__ int s_last;
+  __shared__ int s_wa[32], s_wb[32];
   pdl_wait();
   pdl_launch_dependents();
-  const int w = threadIdx.x >> 5;
-  const int t = blockIdx.x * tokens_per_cta + w;
-  if (w < tokens_per_cta && t < M)
-    route_token<NPL>(logits + static_cast<size_t>(t) * E, E, k, softcap, renorm,
-                     ids + static_cast<size_t>(t) * k, weights + static_cast<size_t>(t) * k);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int t = blockIdx.x * 32 + w;
+  int e_sel = -1;
+  if (t < M) {
+    const int id = route_token<NPL>(logits + static_cast<size_t>(t) * E, E, k, softcap, renorm,
+                                    ids + static_cast<size_t>(t) * k,
+                                    weights + static_cast<size_t>(t) * k);
+    if (lane < k) e_sel = id;
+  }
+  for (int i = tid; i < 32 * E; i += kLayoutThreads) s_tab[i] = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // acq_rel arrival: releases this CTA's ids and weights (ordered before it
-    // by the barrier) and, for the last CTA, acquires every other CTA's
+  if (e_sel >= 0) s_tab[w * E + e_sel] = 1;
+  __syncthreads();
+  for (int e = tid; e < E; e += kLayoutThreads) {
+    int run = 0;
+    for (int ww = 0; ww < 32; ++ww) {
+      const int v = s_tab[ww * E + e];
+      s_tab[ww * E + e] = run;
+      run += v;
+    }
+    cta_hist[static_cast<size_t>(blockIdx.x) * E + e] = run;
+  }
+  __syncthreads();
+  if (e_sel >= 0) local_rank[static_cast<size_t>(t) * k + lane] = s_tab[w * E + e_sel];
+  __syncthreads();
+  if (tid == 0) {
     unsigned prev;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
                  : "=r"(prev)
@@ -214,9 +241,70 @@ __global__ void __launch_bounds__(kLayoutThreads, 1)
   }
   __syncthreads();
   if (!s_last) return;
-  layout_block(ids, M * k, E, block_m, counts, offsets, sorted_route_ids, route_slot,
-               tile_offsets, ctrl, s_hist);
-  if (threadIdx.x == 0) ctrl->route_done = 0u;
+
+  // ---- last CTA: per-CTA bases, counts, offsets, tile offsets
+  const int nC = gridDim.x;
+  int G = 1;  // threads per expert (a power of two, G * E <= 1024)
+  while (G * 2 * E <= kLayoutThreads && G * 2 <= 128) G *= 2;
+  int* s_part = s_tab;                 // [E][G]
+  int* s_cnt = s_tab + kLayoutThreads; // [E]
+  const int e = tid / G, g = tid % G;
+  const int chunk = (nC + G - 1) / G;
+  const int c0 = min(nC, g * chunk), c1 = min(nC, c0 + chunk);
+  int part = 0;
+  if (e < E) {
+    for (int cb = c0; cb < c1; cb += 8) {  // 8 loads in flight per step
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = cb + u < c1 ? __ldcg(cta_hist + static_cast<size_t>(cb + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) part += v[u];
+    }
+  }
+  if (e < E) s_part[e * G + g] = part;
+  __syncthreads();
+  if (e < E) {
+    int start = 0;
+    for (int gg = 0; gg < g; ++gg) start += s_part[e * G + gg];
+    if (g == G - 1) s_cnt[e] = start + part;
+    int run = start;
+    for (int cb = c0; cb < c1; cb += 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = cb + u < c1 ? __ldcg(cta_hist + static_cast<size_t>(cb + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (cb + u < c1) cta_base[static_cast<size_t>(cb + u) * E + e] = run;
+        run += v[u];
+      }
+    }
+  }
+  __syncthreads();
+  int cnt = 0, ntile = 0;
+  if (tid < E) {
+    cnt = s_cnt[tid];
+    ntile = (cnt + block_m - 1) / block_m;
+  }
+  int inc_c = cnt, inc_t = ntile;
+  block_scan2(inc_c, inc_t, s_wa, s_wb);
+  if (tid < E) {
+    counts[tid] = cnt;
+    offsets[tid] = inc_c - cnt;
+    tile_offsets[tid] = inc_t - ntile;
+    if (tid == E - 1) {
+      offsets[E] = inc_c;
+      tile_offsets[E] = inc_t;
+    }
+  }
+  if (tid == 0) {
+    ctrl->queue = 0;
+    ctrl->done = 0;
+    ctrl->queue2 = 0;
+    ctrl->done2 = 0;
+    ctrl->route_done = 0u;
+  }
 }
 
 }  // namespace
@@ -267,20 +355,21 @@ __global__ void __launch_bounds__(32) prefetch_l2_kernel(const uint8_t* __restri
 }
 
 template <int NPL>
-cudaError_t launch_route_layout_t(const float* logits, int M, int E, int k, float softcap,
-                                  int renorm, int32_t* ids, float* weights, int block_m,
-                                  int32_t* counts, int32_t* offsets, int32_t* sorted_route_ids,
-                                  int32_t* route_slot, int32_t* tile_offsets, Ctrl* ctrl,
-                                  cudaStream_t stream, bool pdl) {
-  const size_t smem = static_cast<size_t>(layout_warps(M * k)) * E * sizeof(int);
-  cudaError_t err = cudaFuncSetAttribute(route_layout_kernel<NPL>,
+cudaError_t launch_route_rank_t(const float* logits, int M, int E, int k, float softcap,
+                                int renorm, int32_t* ids, float* weights, int block_m,
+                                int32_t* counts, int32_t* offsets, int32_t* tile_offsets,
+                                Ctrl* ctrl, int32_t* local_rank, int32_t* cta_hist,
+                                int32_t* cta_base, cudaStream_t stream, bool pdl) {
+  // [32][E] ranking table; the last CTA reuses it for [E][G] partial sums and [E] counts
+  const size_t smem = static_cast<size_t>(32 * E > 2 * kLayoutThreads ? 32 * E : 2 * kLayoutThreads) *
+                      sizeof(int);
+  cudaError_t err = cudaFuncSetAttribute(route_rank_kernel<NPL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
-  if (err == cudaSuccess) err = prefer_max_shared(route_layout_kernel<NPL>);
+  if (err == cudaSuccess) err = prefer_max_shared(route_rank_kernel<NPL>);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  const int tpc = M <= 8 * 160 ? 8 : 32;
-  cfg.gridDim = dim3((M + tpc - 1) / tpc);
+  cfg.gridDim = dim3((M + 31) / 32);
   cfg.blockDim = dim3(kLayoutThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -289,28 +378,28 @@ cudaError_t launch_route_layout_t(const float* logits, int M, int E, int k, floa
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, route_layout_kernel<NPL>, logits, M, E, k, softcap, renorm, ids,
-                            weights, block_m, counts, offsets, sorted_route_ids, route_slot,
-                            tile_offsets, ctrl, tpc);
+  return cudaLaunchKernelEx(&cfg, route_rank_kernel<NPL>, logits, M, E, k, softcap, renorm, ids,
+                            weights, block_m, counts, offsets, tile_offsets, ctrl, local_rank,
+                            cta_hist, cta_base);
 }
 
-cudaError_t launch_route_layout(const float* logits, int M, int E, int k, float softcap,
-                                int renorm, int32_t* ids, float* weights, int block_m,
-                                int32_t* counts, int32_t* offsets, int32_t* sorted_route_ids,
-                                int32_t* route_slot, int32_t* tile_offsets, Ctrl* ctrl,
-                                cudaStream_t stream, bool pdl) {
+cudaError_t launch_route_rank(const float* logits, int M, int E, int k, float softcap, int renorm,
+                              int32_t* ids, float* weights, int block_m, int32_t* counts,
+                              int32_t* offsets, int32_t* tile_offsets, Ctrl* ctrl,
+                              int32_t* local_rank, int32_t* cta_hist, int32_t* cta_base,
+                              cudaStream_t stream, bool pdl) {
   const int npl = (E + 31) / 32;
-#define MOE_RL(N)                                                                             \
-  return launch_route_layout_t<N>(logits, M, E, k, softcap, renorm, ids, weights, block_m,    \
-                                  counts, offsets, sorted_route_ids, route_slot, tile_offsets, \
-                                  ctrl, stream, pdl)
-  if (npl <= 1) MOE_RL(1);
-  if (npl <= 2) MOE_RL(2);
-  if (npl <= 4) MOE_RL(4);
-  if (npl <= 8) MOE_RL(8);
-  if (npl <= 16) MOE_RL(16);
-  MOE_RL(32);
-#undef MOE_RL
+#define MOE_RR(N)                                                                           \
+  return launch_route_rank_t<N>(logits, M, E, k, softcap, renorm, ids, weights, block_m,    \
+                                counts, offsets, tile_offsets, ctrl, local_rank, cta_hist,  \
+                                cta_base, stream, pdl)
+  if (npl <= 1) MOE_RR(1);
+  if (npl <= 2) MOE_RR(2);
+  if (npl <= 4) MOE_RR(4);
+  if (npl <= 8) MOE_RR(8);
+  if (npl <= 16) MOE_RR(16);
+  MOE_RR(32);
+#undef MOE_RR
 }
 
 cudaError_t launch_prefetch_l2(const void* base, long long bytes, cudaStream_t stream) {

@@ -20,8 +20,25 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict_
                                                        uint2* __restrict__ out, size_t n4) {
   pdl_wait();
   pdl_launch_dependents();
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+  // four independent 16-byte loads in flight per thread per step
+  constexpr int kUnroll = 4;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+  for (; i + (kUnroll - 1) * stride < n4; i += kUnroll * stride) {
+    float4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = __ldcg(acc + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(v[u].x, v[u].y);
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[u].z, v[u].w);
+      uint2 o;
+      o.x = *reinterpret_cast<uint32_t*>(&a);
+      o.y = *reinterpret_cast<uint32_t*>(&b);
+      out[i + u * stride] = o;
+    }
+  }
+  for (; i < n4; i += stride) {
     const float4 v = __ldcg(acc + i);
     __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
     __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
@@ -55,13 +72,12 @@ __global__ void __launch_bounds__(256) scatter_kernel(const float* __restrict__ 
 }
 
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int M,
-                                                          int row_vecs, int k,
-                                                          const int32_t* __restrict__ route_slot,
+                                                          int row_vecs, int k, int32_t* route_slot,
                                                           uint4* __restrict__ a,
                                                           float* __restrict__ zero_acc,
-                                                          int zero_cols) {
+                                                          int zero_cols, const Placement pl) {
+  __shared__ int s_slot[32];
   pdl_launch_dependents();
-  pdl_wait();
   const int t = blockIdx.x;
   if (t >= M) return;
   const int R = M * k;
@@ -70,15 +86,34 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     for (int i = threadIdx.x; i < (zero_cols >> 2); i += blockDim.x)
       row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  int slots[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    slots[j] = j < k ? __ldg(route_slot + static_cast<size_t>(t) * k + j) : -1;
+  pdl_wait();
+  if (static_cast<int>(threadIdx.x) < k) {
+    const int r = t * k + threadIdx.x;
+    int slot;
+    if (pl.cta_base == nullptr) {
+      slot = __ldg(route_slot + r);
+    } else {
+      const int e = __ldg(pl.ids + r);
+      slot = -1;
+      if (e >= 0 && e < pl.E) {
+        slot = __ldg(pl.offsets + e) +
+               __ldg(pl.cta_base + static_cast<size_t>(t / kRankTokensPerCta) * pl.E + e) +
+               __ldg(pl.local_rank + r);
+        if (slot >= R) slot = -1;
+        if (slot >= 0) {
+          route_slot[r] = slot;
+          pl.sorted_route_ids[slot] = r;
+        }
+      }
+    }
+    s_slot[threadIdx.x] = slot;
+  }
+  __syncthreads();
   for (int i = threadIdx.x; i < row_vecs; i += blockDim.x) {
-    uint4 v = __ldg(x + static_cast<size_t>(t) * row_vecs + i);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j < k && slots[j] >= 0 && slots[j] < R) a[static_cast<size_t>(slots[j]) * row_vecs + i] = v;
+    const uint4 v = __ldg(x + static_cast<size_t>(t) * row_vecs + i);
+    for (int j = 0; j < k; ++j) {
+      const int slot = s_slot[j];
+      if (slot >= 0 && slot < R) a[static_cast<size_t>(slot) * row_vecs + i] = v;
     }
   }
 }
@@ -101,7 +136,8 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t stream, bool pdl
 cudaError_t launch_finalize(const float* acc, void* out, size_t n, int num_sms,
                             cudaStream_t stream, bool pdl) {
   const size_t n4 = n / 4;
-  int blocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, static_cast<size_t>(num_sms)));
+  // up to 8 CTAs of 256 threads per SM; each thread converts >= 4 vectors
+  int blocks = static_cast<int>(std::min<size_t>((n4 + 1023) / 1024, static_cast<size_t>(num_sms) * 8));
   if (blocks < 1) blocks = 1;
   cudaError_t err = prefer_max_shared(finalize_kernel);
   if (err != cudaSuccess) return err;
@@ -119,15 +155,15 @@ cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const f
                             static_cast<__nv_bfloat16*>(out));
 }
 
-cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, const int32_t* route_slot,
-                                    void* a, float* zero_acc, int zero_cols, cudaStream_t stream,
-                                    bool pdl) {
+cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, int32_t* route_slot,
+                                    void* a, float* zero_acc, int zero_cols, const Placement& pl,
+                                    cudaStream_t stream, bool pdl) {
   cudaError_t err = prefer_max_shared(gather_rows_kernel);
   if (err != cudaSuccess) return err;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(256), stream, pdl, attr);
   return cudaLaunchKernelEx(&cfg, gather_rows_kernel, static_cast<const uint4*>(x), M, K / 8, k,
-                            route_slot, static_cast<uint4*>(a), zero_acc, zero_cols);
+                            route_slot, static_cast<uint4*>(a), zero_acc, zero_cols, pl);
 }
 
 }  // namespace moe
