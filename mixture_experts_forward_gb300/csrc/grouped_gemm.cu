@@ -14,7 +14,9 @@
 // rows of a tile are the MMA's M side and the routed rows (block_m of them,
 // 16..256) are its N side, so a 4-row expert costs a 128x16 MMA instead of a
 // padded 128-row one and the kernel streams each touched weight block once.
-//   warp 0      TMA producer: tile queue, weight + activation tiles -> smem ring
+//   warps 0, 7  TMA producers, alternating stages; warp 0 also runs the tile
+//               queue.  A stage holds sk K blocks and each of its 3-D boxes
+//               (weight and activation tiles, sk K blocks deep) has its own lane
 //   warp 1      one thread issues tcgen05.mma into TMEM, commits to mbarriers;
 //               the warp owns the TMEM allocation
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (thread = weight row),
@@ -42,8 +44,9 @@ constexpr int kRowBytes = 128;        // bytes per K block row (one swizzle atom
 constexpr int kATileBytes = kTileN * kRowBytes;
 constexpr int kMaxStages = 16;
 constexpr int kRing = 4;              // tile descriptors (and metadata slots) in flight
-constexpr int kThreads = 224;         // 7 warps
+constexpr int kThreads = 256;         // 8 warps
 constexpr int kMetaWarp = 6;
+constexpr int kProducer2 = 7;          // second TMA producer warp
 constexpr int kMaxE = 1024;
 
 struct TileDesc {
@@ -62,6 +65,8 @@ struct Cfg {
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kATiles = kSwiglu ? 2 : 1;
+  // bytes of one K block of a stage; a stage holds p.sk K blocks laid out as
+  // [kATiles][sk] weight tiles, then [sk] activation tiles
   static constexpr int kStageBytes = kATiles * kATileBytes + BM * kRowBytes;
   // FP8 epilogue: K blocks whose partials are loaded before one wait (<= 64 columns)
   static constexpr int kKbGroup = BM <= 64 ? 64 / BM : 1;
@@ -120,8 +125,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
   const int NST = p.num_stages;
+  const int SK = p.sk;                                  // K blocks per stage
+  const int stage_bytes = SK * C::kStageBytes;
   const int meta_bytes = meta_slot_bytes(kFP8, BM, p.kb_per_split);
-  uint8_t* s_meta = smem_gen + NST * C::kStageBytes;  // kRing slots of meta_bytes
+  uint8_t* s_meta = smem_gen + NST * stage_bytes;       // kRing slots of meta_bytes
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -134,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(smem_u32(&bar_dfull[i]), 1);
-      mbar_init(smem_u32(&bar_dempty[i]), 5);  // MMA thread + 4 epilogue warps
+      mbar_init(smem_u32(&bar_dempty[i]), 6);  // MMA thread, 4 epilogue warps, second producer
       mbar_init(smem_u32(&bar_mfull[i]), 1);
     }
     mbar_init(smem_u32(&bar_drain), 1);
@@ -165,79 +172,114 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_tiles = s_tile_off[p.E] * p.n_tiles * p.k_splits;
   const uint64_t tmo = p.timeout_ns;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();
-      const uint64_t pol_a = policy_evict_last();
-      int stage = 0, ds = 0;
-      uint32_t phase = 0, dphase = 0;
-      bool ok = true;
-      // static schedule state: experts handled by this CTA
-      const int G = gridDim.x, c = blockIdx.x;
-      int st_e = G >= p.E ? c % p.E : c;
-      const int st_idx = G >= p.E ? c / p.E : 0;
-      const int st_stride = G >= p.E ? (G - (c % p.E) + p.E - 1) / p.E : 1;
-      int st_lt = st_idx;
-      // queue: CTA c starts with tile c; later tiles come from the counter
-      // (offset by the grid size), claimed one tile ahead so the atomic's
-      // round trip overlaps this tile's loads
-      int queued = p.sched == MOE_SCHED_QUEUE ? c : -1;
-      for (;;) {
-        int t;
-        if (p.sched == MOE_SCHED_QUEUE) {
-          t = queued < total_tiles ? queued : -1;
-          if (t >= 0) queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
-        } else {
-          t = -1;
-          while (st_e < p.E) {
-            const int per_e = (s_tile_off[st_e + 1] - s_tile_off[st_e]) * p.n_tiles * p.k_splits;
-            if (st_lt < per_e) {
-              t = s_tile_off[st_e] * p.n_tiles * p.k_splits + st_lt;
-              st_lt += st_stride;
-              break;
+  if (warp == 0 || warp == kProducer2) {
+    // ------------------------------------------------------------ producers
+    // A warp's bulk-tensor copy instructions are served one after another, at
+    // a bounded rate of instructions rather than bytes.  So two warps fill the
+    // ring, alternating stages (warp 0 the even global stage numbers, the
+    // second producer the odd ones), and within an instruction every box of
+    // the stage goes out from its own lane: lane a < kATiles loads weight
+    // tile a, lane kATiles the activation tile, each box SK K blocks deep.
+    // Warp 0 also runs the tile queue and publishes each tile's descriptor.
+    const int pw = warp == 0 ? 0 : 1;
+    const uint64_t pol_w = policy_evict_first();
+    const uint64_t pol_a = policy_evict_last();
+    int stage = 0, ds = 0, q = 0;   // q: global stage number (both warps count all stages)
+    uint32_t phase = 0, dphase = 0;
+    bool ok = true;
+    // static schedule state: experts handled by this CTA
+    const int G = gridDim.x, c = blockIdx.x;
+    int st_e = G >= p.E ? c % p.E : c;
+    const int st_idx = G >= p.E ? c / p.E : 0;
+    const int st_stride = G >= p.E ? (G - (c % p.E) + p.E - 1) / p.E : 1;
+    int st_lt = st_idx;
+    // queue: CTA c starts with tile c; later tiles come from the counter
+    // (offset by the grid size), claimed one tile ahead so the atomic's
+    // round trip overlaps this tile's loads
+    int queued = p.sched == MOE_SCHED_QUEUE ? c : -1;
+    for (;;) {
+      TileDesc d;
+      bool got = true;
+      if (pw == 0) {
+        int t = -1;
+        if (lane == 0) {
+          if (p.sched == MOE_SCHED_QUEUE) {
+            t = queued < total_tiles ? queued : -1;
+            if (t >= 0) queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
+          } else {
+            while (st_e < p.E) {
+              const int per_e = (s_tile_off[st_e + 1] - s_tile_off[st_e]) * p.n_tiles * p.k_splits;
+              if (st_lt < per_e) {
+                t = s_tile_off[st_e] * p.n_tiles * p.k_splits + st_lt;
+                st_lt += st_stride;
+                break;
+              }
+              if (G >= p.E) { st_e = p.E; break; }
+              st_e += G;
+              st_lt = 0;
             }
-            if (G >= p.E) { st_e = p.E; break; }
-            st_e += G;
-            st_lt = 0;
           }
         }
-        TileDesc d;
+        t = __shfl_sync(0xffffffffu, t, 0);
         if (t >= 0) {
           decode_tile(t, p, s_tile_off, s_off, BM, d);
           if (d.rows <= 0 || d.nkb <= 0) continue;
         } else {
           d.nkb = -1;
         }
-        if (!mbar_wait(smem_u32(&bar_dempty[ds]), dphase ^ 1u, &s_abort, tmo)) { ok = false; break; }
-        s_desc[ds] = d;
-        mbar_arrive(smem_u32(&bar_dfull[ds]));
-        if (++ds == kRing) { ds = 0; dphase ^= 1u; }
-        if (t < 0) break;
-        const int w_row = d.e * p.N + d.n_tile * kTileN;
-        for (int i = 0; i < d.nkb; ++i) {
-          if (!mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, tmo)) { ok = false; break; }
-          if (!p.drop_producer) {
-            const uint32_t full = smem_u32(&bar_full[stage]);
-            const uint32_t sa = smem_base + stage * C::kStageBytes;
-            const int kc = (d.kb0 + i) * (kFP8 ? kRowBytes : kRowBytes / 2);  // element coordinate
-            mbar_arrive_expect_tx(full, C::kStageBytes);
-            tma_load_2d(sa, &tmap_w, full, kc, w_row, pol_w);
-            if constexpr (C::kSwiglu)
-              tma_load_2d(sa + kATileBytes, &tmap_w, full, kc, w_row + p.N / 2, pol_w);
-            tma_load_2d(sa + C::kATiles * kATileBytes, &tmap_a, full, kc, d.m0, pol_a);
+        if (lane == 0) {
+          got = mbar_wait(smem_u32(&bar_dempty[ds]), dphase ^ 1u, &s_abort, tmo);
+          if (got) {
+            s_desc[ds] = d;
+            mbar_arrive(smem_u32(&bar_dfull[ds]));
           }
-          if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
+        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+      } else {
+        if (lane == 0) got = mbar_wait(smem_u32(&bar_dfull[ds]), dphase, &s_abort, tmo);
+        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+        __syncwarp();
+        d = s_desc[ds];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bar_dempty[ds]));
       }
+      if (++ds == kRing) { ds = 0; dphase ^= 1u; }
+      if (d.nkb < 0) break;
+      const int w_row = d.e * p.N + d.n_tile * kTileN;
+      for (int i = 0; i < d.nkb; i += SK) {
+        if (((q ^ pw) & 1) == 0) {
+          const uint32_t full = smem_u32(&bar_full[stage]);
+          if (lane == 0) {
+            got = mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, tmo);
+            if (got && !p.drop_producer) mbar_arrive_expect_tx(full, stage_bytes);
+          }
+          if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+          if (!p.drop_producer) {
+            // one box per lane: weight tile(s), then the activation tile; each
+            // box spans SK K blocks (a box running past K reads the fill value)
+            const uint32_t sa = smem_base + stage * stage_bytes;
+            const int kb = d.kb0 + i;
+            if (lane < C::kATiles)
+              tma_load_3d(sa + lane * SK * kATileBytes, &tmap_w, full, 0, w_row + lane * (p.N / 2),
+                          kb, pol_w);
+            else if (lane == C::kATiles)
+              tma_load_3d(sa + C::kATiles * SK * kATileBytes, &tmap_a, full, 0, d.m0, kb, pol_a);
+          }
+          __syncwarp();
+        }
+        ++q;
+        if (++stage == NST) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+    if (lane == 0) {
       if (!ok) {
         set_error(p.ctrl, MOE_ERR_TIMEOUT, 1);
         s_abort = 1;
       }
-      // Wait (bounded) until every load this thread issued has landed: a
-      // stage's last fill has completed once its "full" phase has flipped.
-      if (!p.drop_producer) {
+      // Warp 0 waits (bounded) until every load of both producers has landed:
+      // a stage's last fill has completed once its "full" phase has flipped.
+      if (pw == 0 && !p.drop_producer) {
         for (int i = 0; i < NST; ++i) {
           // stages [0, stage) were filled in the current pass, the rest in the previous one
           const uint32_t par = (i < stage) ? phase : phase ^ 1u;
@@ -259,8 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++ds == kRing) { ds = 0; dphase ^= 1u; }
         if (d.nkb < 0) break;
         int buf = 0;
-        for (int i = 0; i < d.nkb; ++i) {
-          if (kFP8 || i == 0) {
+        for (int i = 0; i < d.nkb; i += SK) {
+          const int nk = min(SK, d.nkb - i);
+          if (!kFP8 && i == 0) {
             buf = acc_n % C::kNumAcc;
             const uint32_t use = static_cast<uint32_t>(acc_n / C::kNumAcc);
             if (!mbar_wait(smem_u32(&bar_tempty[buf]), (use & 1u) ^ 1u, &s_abort, tmo)) { ok = false; break; }
@@ -268,20 +311,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!mbar_wait(smem_u32(&bar_full[stage]), phase, &s_abort, tmo)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = smem_base + stage * C::kStageBytes;
-          const uint32_t b_addr = a_addr + C::kATiles * kATileBytes;
-          const uint32_t d_tmem = tmem_base + buf * C::kAccCols;
+          const uint32_t sbase = smem_base + stage * stage_bytes;
+          for (int kb = 0; kb < nk; ++kb) {
+            if constexpr (kFP8) {
+              buf = acc_n % C::kNumAcc;
+              const uint32_t use = static_cast<uint32_t>(acc_n / C::kNumAcc);
+              if (!mbar_wait(smem_u32(&bar_tempty[buf]), (use & 1u) ^ 1u, &s_abort, tmo)) { ok = false; break; }
+              tc_fence_after();
+            }
+            const uint32_t a_addr = sbase + kb * kATileBytes;
+            const uint32_t b_addr = sbase + C::kATiles * SK * kATileBytes + kb * (BM * kRowBytes);
+            const uint32_t d_tmem = tmem_base + buf * C::kAccCols;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t acc = kFP8 ? (kk > 0) : (i > 0 || kk > 0);
-            const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32);
-            umma<kFP8>(d_tmem, smem_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
-            if constexpr (C::kSwiglu)
-              umma<kFP8>(d_tmem + BM, smem_desc_sw128(a_addr + kATileBytes + kk * 32), bdesc, idesc,
-                         acc);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = kFP8 ? (kk > 0) : (i > 0 || kb > 0 || kk > 0);
+              const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32);
+              umma<kFP8>(d_tmem, smem_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
+              if constexpr (C::kSwiglu)
+                umma<kFP8>(d_tmem + BM, smem_desc_sw128(a_addr + SK * kATileBytes + kk * 32), bdesc,
+                           idesc, acc);
+            }
+            if constexpr (kFP8) {
+              umma_commit(smem_u32(&bar_tfull[buf]));
+              ++acc_n;
+            }
           }
+          if (!ok) break;
           umma_commit(smem_u32(&bar_empty[stage]));
-          if (kFP8 || i == d.nkb - 1) {
+          if (!kFP8 && i + nk >= d.nkb) {
             umma_commit(smem_u32(&bar_tfull[buf]));
             ++acc_n;
           }
@@ -416,9 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int g = 0; g < C::kKbGroup; ++g) {
               if (g < ng) {
-                const float* scg = sc + (i + g) * BM + c0;
+                // scale products of this K block (16-byte aligned, broadcast reads)
+                const float4* scg = reinterpret_cast<const float4*>(sc + (i + g) * BM + c0);
 #pragma unroll
-                for (int j = 0; j < C::kLdCols; ++j) acc[c0 + j] = fmaf(v[g][j], scg[j], acc[c0 + j]);
+                for (int j = 0; j < C::kLdCols; j += 4) {
+                  const float4 f = scg[j / 4];
+                  acc[c0 + j] = fmaf(v[g][j], f.x, acc[c0 + j]);
+                  acc[c0 + j + 1] = fmaf(v[g][j + 1], f.y, acc[c0 + j + 1]);
+                  acc[c0 + j + 2] = fmaf(v[g][j + 2], f.z, acc[c0 + j + 2]);
+                  acc[c0 + j + 3] = fmaf(v[g][j + 3], f.w, acc[c0 + j + 3]);
+                }
               }
             }
           }
@@ -430,10 +494,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if constexpr (kEpi == MOE_EPI_SCATTER) {
-          float* out = static_cast<float*>(p.out);
+          // tokens and route weights 8 rows at a time (vector loads), then
+          // the 8 row reductions back to back
+          float* out = static_cast<float*>(p.out) + col;
 #pragma unroll
-          for (int s = 0; s < BM; ++s) {
-            if (s < d.rows) red_add_f32(out + static_cast<size_t>(tok[s]) * p.N + col, wt[s] * acc[s]);
+          for (int s0 = 0; s0 < BM; s0 += 8) {
+            if (s0 < d.rows) {
+              const int4 t0 = *reinterpret_cast<const int4*>(tok + s0);
+              const int4 t1 = *reinterpret_cast<const int4*>(tok + s0 + 4);
+              const float4 w0 = *reinterpret_cast<const float4*>(wt + s0);
+              const float4 w1 = *reinterpret_cast<const float4*>(wt + s0 + 4);
+              const int tk[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+              const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (s0 + j < d.rows)
+                  red_add_f32(out + static_cast<size_t>(tk[j]) * p.N, ww[j] * acc[s0 + j]);
+            }
           }
         } else {
           float* out = static_cast<float*>(p.out);
@@ -575,7 +652,8 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
                                 cudaStream_t stream, bool pdl) {
   GemmVariant v;
   if (!select_gemm_variant(fp8, epi, bm, v)) return cudaErrorInvalidValue;
-  const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * v.stage_bytes +
+  if (p.sk < 1 || p.sk > 2) return cudaErrorInvalidValue;
+  const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * p.sk * v.stage_bytes +
                       gemm_meta_bytes(fp8, bm, p.kb_per_split);
   cudaError_t err = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

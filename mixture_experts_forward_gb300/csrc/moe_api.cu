@@ -57,16 +57,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D K-major tensor map: rows of `inner` elements, `outer` rows, 128-byte
 // swizzle, box = 128 bytes x box_rows; out-of-range rows read as zero.
+// Operand view for the grouped GEMM: a row-major [outer, inner] matrix seen
+// as 3-D {128-byte K block slice, row, K block}, so one box brings `sk`
+// consecutive K blocks of `box_rows` rows ([K block][row][128 B] in shared
+// memory, 128-byte swizzle) and each row is read `sk` * 128 bytes at a time.
 bool make_tmap(CUtensorMap* m, const void* base, bool fp8, uint64_t inner, uint64_t outer,
-               uint32_t box_rows) {
+               uint32_t box_rows, uint32_t sk) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const uint32_t esize = fp8 ? 1 : 2;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * esize};
-  cuuint32_t box[2] = {128u / esize, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  const uint64_t kb_elems = 128u / esize;
+  cuuint64_t dims[3] = {kb_elems, outer, inner / kb_elems};
+  cuuint64_t strides[2] = {inner * esize, 128u};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kb_elems), box_rows, sk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -141,13 +146,6 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   const bool fp8 = a->dtype == MOE_DTYPE_FP8_E4M3;
   const int sms = device_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
-  CUtensorMap tw, ta;
-  if (!make_tmap(&tw, a->w, fp8, static_cast<uint64_t>(a->K),
-                 static_cast<uint64_t>(a->E) * a->N, 128u))
-    return MOE_ERR_CUDA;
-  if (!make_tmap(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->R),
-                 static_cast<uint32_t>(a->block_m)))
-    return MOE_ERR_CUDA;
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   p.a_scales = a->a_scales;
@@ -175,10 +173,22 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m);
   if (stage_bytes <= 0) return MOE_ERR_UNSUPPORTED;
   const int meta_bytes = gemm_meta_bytes(fp8, a->block_m, p.kb_per_split);
-  int stages = (232448 - 1024 - 12288 - meta_bytes) / stage_bytes;
+  // Two K blocks per stage (twice the bytes per copy, and 256 contiguous
+  // bytes of every weight row per copy) wherever a split holds whole pairs
+  // and at least three stages still fit.
+  const int avail = 232448 - 1024 - 12288 - meta_bytes;
+  p.sk = (p.kb_per_split % 2 == 0 && avail / (2 * stage_bytes) >= 3) ? 2 : 1;
+  int stages = avail / (p.sk * stage_bytes);
   if (stages > 16) stages = 16;
   if (stages < 2) return MOE_ERR_UNSUPPORTED;
   p.num_stages = stages;
+  CUtensorMap tw, ta;
+  if (!make_tmap(&tw, a->w, fp8, static_cast<uint64_t>(a->K),
+                 static_cast<uint64_t>(a->E) * a->N, 128u, static_cast<uint32_t>(p.sk)))
+    return MOE_ERR_CUDA;
+  if (!make_tmap(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->R),
+                 static_cast<uint32_t>(a->block_m), static_cast<uint32_t>(p.sk)))
+    return MOE_ERR_CUDA;
   const int ctas = a->num_ctas > 0 ? a->num_ctas : sms;
   return cuda_status(launch_grouped_gemm(tw, ta, p, fp8, a->epilogue, a->block_m, ctas, stream,
                                          pdl));

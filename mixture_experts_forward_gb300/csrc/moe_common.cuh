@@ -73,31 +73,34 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// One potentially blocking test of the phase: the thread may sleep until the
+// phase completes, for at most `kSuspendHintNs` (then it returns false).
+// Sleeping rather than polling keeps idle warps from flooding the shared
+// memory pipe that the bulk copies' completions also go through.
+constexpr uint32_t kSuspendHintNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
 
 // Bounded wait for the phase of `parity` to complete.  Gives up (returns
-// false) when `*abort` becomes nonzero or after `timeout_ns` nanoseconds;
-// never spins forever.
+// false) when `*abort` becomes nonzero or after `timeout_ns` nanoseconds
+// (checked between sleeps); never waits forever.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile int* abort, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > timeout_ns) return false;
-    }
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
   }
 }
 
@@ -114,6 +117,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
+// 3-D tiled load {c0, c1, c2} (innermost first).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
       : "memory");
 }
 
@@ -216,9 +229,11 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Vector reduction into global memory (fp32 add, relaxed, GPU scope).
+// Reduction into global memory (fp32 add, relaxed, GPU scope).  No compiler
+// memory clobber: nothing in a kernel reads the reduced values back, so the
+// compiler may keep loads in flight across a run of reductions.
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v));
 }
 
 // Named barrier among `count` threads (multiple of 32).

@@ -34,6 +34,7 @@ struct GemmParams {
   int n_tiles;                  // output tiles of 128 columns
   int sched;
   int num_stages;
+  int sk;                       // K blocks per pipeline stage (1 or 2)
   int drop_producer;
   unsigned long long timeout_ns;
 };
