@@ -43,7 +43,11 @@ constexpr int kTileN = 128;           // weight rows per tile (MMA M)
 constexpr int kRowBytes = 128;        // bytes per K block row (one swizzle atom row)
 constexpr int kATileBytes = kTileN * kRowBytes;
 constexpr int kMaxStages = 16;
-constexpr int kRing = 4;              // tile descriptors (and metadata slots) in flight
+// Tile descriptors (and metadata slots) in flight: 4, or 2 where a slot of
+// FP8 scale products is large (block_m 128) and shared memory is needed for
+// deeper stages.
+constexpr int kMaxRing = 4;
+__host__ __device__ constexpr int ring_slots(bool fp8, int bm) { return fp8 && bm >= 128 ? 2 : 4; }
 constexpr int kThreads = 256;         // 8 warps
 constexpr int kMetaWarp = 6;
 constexpr int kProducer2 = 7;          // second TMA producer warp
@@ -65,6 +69,7 @@ struct Cfg {
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kATiles = kSwiglu ? 2 : 1;
+  static constexpr int kRing = ring_slots(kFP8, BM);
   // bytes of one K block of a stage; a stage holds p.sk K blocks laid out as
   // [kATiles][sk] weight tiles, then [sk] activation tiles
   static constexpr int kStageBytes = kATiles * kATileBytes + BM * kRowBytes;
@@ -113,9 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_tfull[C::kNumAcc], bar_tempty[C::kNumAcc];
-  __shared__ __align__(8) uint64_t bar_dfull[kRing], bar_dempty[kRing], bar_mfull[kRing];
+  __shared__ __align__(8) uint64_t bar_dfull[kMaxRing], bar_dempty[kMaxRing], bar_mfull[kMaxRing];
   __shared__ __align__(8) uint64_t bar_drain;
-  __shared__ TileDesc s_desc[kRing];
+  __shared__ TileDesc s_desc[kMaxRing];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_tile_off[kMaxE + 1];
@@ -128,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int SK = p.sk;                                  // K blocks per stage
   const int stage_bytes = SK * C::kStageBytes;
   const int meta_bytes = meta_slot_bytes(kFP8, BM, p.kb_per_split);
-  uint8_t* s_meta = smem_gen + NST * stage_bytes;       // kRing slots of meta_bytes
+  uint8_t* s_meta = smem_gen + NST * stage_bytes;       // C::kRing slots of meta_bytes
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bar_tfull[i]), 1);
       mbar_init(smem_u32(&bar_tempty[i]), 4);
     }
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < C::kRing; ++i) {
       mbar_init(smem_u32(&bar_dfull[i]), 1);
       mbar_init(smem_u32(&bar_dempty[i]), 6);  // MMA thread, 4 epilogue warps, second producer
       mbar_init(smem_u32(&bar_mfull[i]), 1);
@@ -158,10 +163,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Everything above is independent of the preceding kernel's results.
   pdl_wait();
-  for (int i = threadIdx.x; i <= p.E; i += kThreads) {
-    s_tile_off[i] = __ldg(p.tile_offsets + i);
-    s_off[i] = __ldg(p.offsets + i);
+  for (int i = threadIdx.x; i <= p.E; i += kThreads) {  // all copies in flight, one wait
+    cp_async4(smem_u32(&s_tile_off[i]), p.tile_offsets + i);
+    cp_async4(smem_u32(&s_off[i]), p.offsets + i);
   }
+  cp_async_wait_all();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bar_dempty[ds]));
       }
-      if (++ds == kRing) { ds = 0; dphase ^= 1u; }
+      if (++ds == C::kRing) { ds = 0; dphase ^= 1u; }
       if (d.nkb < 0) break;
       const int w_row = d.e * p.N + d.n_tile * kTileN;
       for (int i = 0; i < d.nkb; i += SK) {
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(smem_u32(&bar_dfull[ds]), dphase, &s_abort, tmo)) { ok = false; break; }
         const TileDesc d = s_desc[ds];
         mbar_arrive(smem_u32(&bar_dempty[ds]));
-        if (++ds == kRing) { ds = 0; dphase ^= 1u; }
+        if (++ds == C::kRing) { ds = 0; dphase ^= 1u; }
         if (d.nkb < 0) break;
         int buf = 0;
         for (int i = 0; i < d.nkb; i += SK) {
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_mfull[ds]));
-      if (++ds == kRing) { ds = 0; dphase ^= 1u; }
+      if (++ds == C::kRing) { ds = 0; dphase ^= 1u; }
       if (d.nkb < 0) break;
     }
   } else {
@@ -567,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this tile's descriptor and metadata slot may now be reused
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_dempty[ds]));
-      if (++ds == kRing) { ds = 0; dphase ^= 1u; }
+      if (++ds == C::kRing) { ds = 0; dphase ^= 1u; }
     }
     if (!ok) {
       set_error(p.ctrl, MOE_ERR_TIMEOUT, 3);
@@ -644,7 +650,7 @@ int gemm_stage_bytes(bool fp8, int epi, int bm) {
 }
 
 int gemm_meta_bytes(bool fp8, int bm, int kb_per_split) {
-  return kRing * meta_slot_bytes(fp8, bm, kb_per_split);
+  return ring_slots(fp8, bm) * meta_slot_bytes(fp8, bm, kb_per_split);
 }
 
 cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_a,

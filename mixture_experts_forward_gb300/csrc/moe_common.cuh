@@ -229,6 +229,18 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Asynchronous global -> shared copies (L2 only, bypassing L1); complete
+// after cp_async_wait_all() in the issuing thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Reduction into global memory (fp32 add, relaxed, GPU scope).  No compiler
 // memory clobber: nothing in a kernel reads the reduced values back, so the
 // compiler may keep loads in flight across a run of reductions.

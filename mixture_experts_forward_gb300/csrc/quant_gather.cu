@@ -152,7 +152,13 @@ __global__ void __launch_bounds__(1024) quant_layout_kernel(
   if (threadIdx.x == 0) s_bad = 0;
 
   pdl_wait();
-  for (int i = threadIdx.x; i < R; i += blockDim.x) s_ids[i] = __ldcg(ids + i);
+  // all expert ids, every copy in flight before one wait
+  if ((R & 3) == 0) {
+    for (int i = 4 * threadIdx.x; i < R; i += 4 * blockDim.x) cp_async16(smem_u32(s_ids + i), ids + i);
+  } else {
+    for (int i = threadIdx.x; i < R; i += blockDim.x) cp_async4(smem_u32(s_ids + i), ids + i);
+  }
+  cp_async_wait_all();
   __syncthreads();
 
   // slots of this CTA's routes: one warp per route

@@ -195,13 +195,13 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 // offsets[e] + cta_base[cta(r)][e] + local_rank[r] — the stable layout by
 // route id.
 template <int NPL>
-__global__ void __launch_bounds__(kLayoutThreads, 1)
+__global__ void __launch_bounds__(kLayoutThreads, NPL <= 8 ? 2 : 1)
     route_rank_kernel(const float* __restrict__ logits, int M, int E, int k, float softcap,
                       int renorm, int32_t* ids, float* __restrict__ weights, int block_m,
                       int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                       int32_t* __restrict__ tile_offsets, Ctrl* ctrl, int32_t* local_rank,
-                      int32_t* cta_hist, int32_t* __restrict__ cta_base) {
-  extern __shared__ int s_tab[];  // [32][E]
+                      int32_t* cta_hist, int32_t* __restrict__ cta_base, int hist_chunk) {
+  extern __shared__ int s_tab[];  // [32][E]; the last CTA: [hist_chunk][E + 4] + [E]
   __shared__ int s_last;
   __shared__ int s_wa[32], s_wb[32];
   pdl_wait();
@@ -243,45 +243,74 @@ __global__ void __launch_bounds__(kLayoutThreads, 1)
   if (!s_last) return;
 
   // ---- last CTA: per-CTA bases, counts, offsets, tile offsets
+  // The [nC][E] histograms are staged in shared memory a chunk of `hist_chunk`
+  // CTAs at a time (16-byte loads, all in flight; rows padded to E + 4 ints
+  // against bank conflicts).  Each expert's column is then scanned in rounds
+  // of G consecutive CTAs, one CTA per lane (a segmented shuffle scan), the
+  // exclusive bases overwrite the chunk in place and go out as 16-byte stores.
   const int nC = gridDim.x;
-  int G = 1;  // threads per expert (a power of two, G * E <= 1024)
-  while (G * 2 * E <= kLayoutThreads && G * 2 <= 128) G *= 2;
-  int* s_part = s_tab;                 // [E][G]
-  int* s_cnt = s_tab + kLayoutThreads; // [E]
+  const int RS = E + 4;  // staged row stride (ints)
+  int G = 1;             // lanes per expert: a power of two, G * E <= 1024, G <= 32
+  while (G * 2 * E <= kLayoutThreads && G * 2 <= 32) G *= 2;
+  int* s_h = s_tab;                      // [hist_chunk][RS]
+  int* s_cnt = s_tab + hist_chunk * RS;  // [E] running totals
+  for (int i = tid; i < E; i += kLayoutThreads) s_cnt[i] = 0;
   const int e = tid / G, g = tid % G;
-  const int chunk = (nC + G - 1) / G;
-  const int c0 = min(nC, g * chunk), c1 = min(nC, c0 + chunk);
-  int part = 0;
-  if (e < E) {
-    for (int cb = c0; cb < c1; cb += 8) {  // 8 loads in flight per step
-      int v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v[u] = cb + u < c1 ? __ldcg(cta_hist + static_cast<size_t>(cb + u) * E + e) : 0;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) part += v[u];
-    }
-  }
-  if (e < E) s_part[e * G + g] = part;
-  __syncthreads();
-  if (e < E) {
-    int start = 0;
-    for (int gg = 0; gg < g; ++gg) start += s_part[e * G + gg];
-    if (g == G - 1) s_cnt[e] = start + part;
-    int run = start;
-    for (int cb = c0; cb < c1; cb += 8) {
-      int v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        v[u] = cb + u < c1 ? __ldcg(cta_hist + static_cast<size_t>(cb + u) * E + e) : 0;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (cb + u < c1) cta_base[static_cast<size_t>(cb + u) * E + e] = run;
-        run += v[u];
+  const bool act = e < E;
+  const bool vec = (E & 3) == 0;
+  for (int cc = 0; cc < nC; cc += hist_chunk) {
+    const int nc = min(hist_chunk, nC - cc);
+    const int32_t* src = cta_hist + static_cast<size_t>(cc) * E;
+    int32_t* dst = cta_base + static_cast<size_t>(cc) * E;
+    // asynchronous copies (no registers held), all in flight, then one wait
+    if (vec) {
+      const int q = E >> 2;
+      for (int i = tid; i < nc * q; i += kLayoutThreads) {
+        const int r = i / q, c4 = i - r * q;
+        cp_async16(smem_u32(s_h + r * RS + 4 * c4), src + static_cast<size_t>(r) * E + 4 * c4);
+      }
+    } else {
+      for (int i = tid; i < nc * E; i += kLayoutThreads) {
+        const int r = i / E, c = i - r * E;
+        cp_async4(smem_u32(s_h + r * RS + c), src + i);
       }
     }
+    cp_async_wait_all();
+    __syncthreads();
+    // every lane takes part in the shuffles (G divides 32, so an expert's
+    // lanes never straddle two warps); lanes past the last expert add 0
+    int run = act ? s_cnt[e] : 0;
+    for (int c0 = 0; c0 < nc; c0 += G) {
+      const int c = c0 + g;
+      const int h = (act && c < nc) ? s_h[c * RS + e] : 0;
+      int inc = h;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        if (off >= G) break;
+        const int y = __shfl_up_sync(0xffffffffu, inc, off, G);
+        if (g >= off) inc += y;
+      }
+      if (act && c < nc) s_h[c * RS + e] = run + inc - h;
+      run += __shfl_sync(0xffffffffu, inc, G - 1, G);
+    }
+    __syncwarp();
+    if (act && g == 0) s_cnt[e] = run;
+    __syncthreads();
+    if (vec) {
+      const int q = E >> 2;
+      for (int i = tid; i < nc * q; i += kLayoutThreads) {
+        const int r = i / q, c4 = i - r * q;
+        reinterpret_cast<int4*>(dst + static_cast<size_t>(r) * E)[c4] =
+            reinterpret_cast<const int4*>(s_h + r * RS)[c4];
+      }
+    } else {
+      for (int i = tid; i < nc * E; i += kLayoutThreads) {
+        const int r = i / E, c = i - r * E;
+        dst[i] = s_h[r * RS + c];
+      }
+    }
+    __syncthreads();
   }
-  __syncthreads();
   int cnt = 0, ntile = 0;
   if (tid < E) {
     cnt = s_cnt[tid];
@@ -360,16 +389,22 @@ cudaError_t launch_route_rank_t(const float* logits, int M, int E, int k, float 
                                 int32_t* counts, int32_t* offsets, int32_t* tile_offsets,
                                 Ctrl* ctrl, int32_t* local_rank, int32_t* cta_hist,
                                 int32_t* cta_base, cudaStream_t stream, bool pdl) {
-  // [32][E] ranking table; the last CTA reuses it for [E][G] partial sums and [E] counts
-  const size_t smem = static_cast<size_t>(32 * E > 2 * kLayoutThreads ? 32 * E : 2 * kLayoutThreads) *
-                      sizeof(int);
+  // [32][E] ranking table; the last CTA reuses it for a chunk of the per-CTA
+  // histograms ([hist_chunk][E + 4], at most 96 KB) and the [E] running totals
+  const int n_ctas = (M + 31) / 32;
+  int hist_chunk = (24576 - E) / (E + 4);
+  if (hist_chunk > n_ctas) hist_chunk = n_ctas;
+  if (hist_chunk < 1) hist_chunk = 1;
+  const int staged = hist_chunk * (E + 4) + E;
+  const int ints = 32 * E > staged ? 32 * E : staged;
+  const size_t smem = static_cast<size_t>(ints) * sizeof(int);
   cudaError_t err = cudaFuncSetAttribute(route_rank_kernel<NPL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err == cudaSuccess) err = prefer_max_shared(route_rank_kernel<NPL>);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((M + 31) / 32);
+  cfg.gridDim = dim3(n_ctas);
   cfg.blockDim = dim3(kLayoutThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -380,7 +415,7 @@ cudaError_t launch_route_rank_t(const float* logits, int M, int E, int k, float 
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, route_rank_kernel<NPL>, logits, M, E, k, softcap, renorm, ids,
                             weights, block_m, counts, offsets, tile_offsets, ctrl, local_rank,
-                            cta_hist, cta_base);
+                            cta_hist, cta_base, hist_chunk);
 }
 
 cudaError_t launch_route_rank(const float* logits, int M, int E, int k, float softcap, int renorm,
