@@ -14,8 +14,8 @@
 // rows of a tile are the MMA's M side and the routed rows (block_m of them,
 // 16..256) are its N side, so a 4-row expert costs a 128x16 MMA instead of a
 // padded 128-row one and the kernel streams each touched weight block once.
-//   warps 0, 7  TMA producers, alternating stages; warp 0 also runs the tile
-//               queue.  A stage holds sk K blocks and each of its 3-D boxes
+//   warps 0, 7+ TMA producers (two or four), taking stages in turn; warp 0
+//               also runs the tile queue.  A stage holds sk K blocks and each of its 3-D boxes
 //               (weight and activation tiles, sk K blocks deep) has its own lane
 //   warp 1      one thread issues tcgen05.mma into TMEM, commits to mbarriers;
 //               the warp owns the TMEM allocation
@@ -48,9 +48,9 @@ constexpr int kMaxStages = 16;
 // deeper stages.
 constexpr int kMaxRing = 4;
 __host__ __device__ constexpr int ring_slots(bool fp8, int bm) { return fp8 && bm >= 128 ? 2 : 4; }
-constexpr int kThreads = 256;         // 8 warps
+constexpr int kMaxThreads = 320;      // up to 10 warps
 constexpr int kMetaWarp = 6;
-constexpr int kProducer2 = 7;          // second TMA producer warp
+constexpr int kFirstExtraProducer = 7;  // warps 7.. are the extra TMA producers
 constexpr int kMaxE = 1024;
 
 struct TileDesc {
@@ -70,6 +70,10 @@ struct Cfg {
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kATiles = kSwiglu ? 2 : 1;
   static constexpr int kRing = ring_slots(kFP8, BM);
+  // TMA producer warps (warp 0 plus warps 7..): two measured best (four were
+  // no faster on any workload and slower on the BF16 FFN)
+  static constexpr int kProducers = 2;
+  static constexpr int kThreads = 32 * (kFirstExtraProducer + kProducers - 1);
   // bytes of one K block of a stage; a stage holds p.sk K blocks laid out as
   // [kATiles][sk] weight tiles, then [sk] activation tiles
   static constexpr int kStageBytes = kATiles * kATileBytes + BM * kRowBytes;
@@ -111,7 +115,7 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const in
 }
 
 template <int BM, bool kFP8, int kEpi>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_a, const GemmParams p) {
   using C = Cfg<BM, kFP8, kEpi>;
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < C::kRing; ++i) {
       mbar_init(smem_u32(&bar_dfull[i]), 1);
-      mbar_init(smem_u32(&bar_dempty[i]), 6);  // MMA thread, 4 epilogue warps, second producer
+      mbar_init(smem_u32(&bar_dempty[i]), 5 + C::kProducers - 1);  // MMA, 4 epilogue warps, extra producers
       mbar_init(smem_u32(&bar_mfull[i]), 1);
     }
     mbar_init(smem_u32(&bar_drain), 1);
@@ -163,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Everything above is independent of the preceding kernel's results.
   pdl_wait();
-  for (int i = threadIdx.x; i <= p.E; i += kThreads) {  // all copies in flight, one wait
+  for (int i = threadIdx.x; i <= p.E; i += C::kThreads) {  // all copies in flight, one wait
     cp_async4(smem_u32(&s_tile_off[i]), p.tile_offsets + i);
     cp_async4(smem_u32(&s_off[i]), p.offsets + i);
   }
@@ -178,19 +182,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_tiles = s_tile_off[p.E] * p.n_tiles * p.k_splits;
   const uint64_t tmo = p.timeout_ns;
 
-  if (warp == 0 || warp == kProducer2) {
+  if (warp == 0 || warp >= kFirstExtraProducer) {
     // ------------------------------------------------------------ producers
     // A warp's bulk-tensor copy instructions are served one after another, at
-    // a bounded rate of instructions rather than bytes.  So two warps fill the
-    // ring, alternating stages (warp 0 the even global stage numbers, the
-    // second producer the odd ones), and within an instruction every box of
-    // the stage goes out from its own lane: lane a < kATiles loads weight
+    // a bounded rate of instructions rather than bytes.  So kProducers warps
+    // fill the ring in turn (global stage q goes to producer q % kProducers),
+    // and within an instruction every box of the stage goes out from its own
+    // lane: lane a < kATiles loads weight
     // tile a, lane kATiles the activation tile, each box SK K blocks deep.
     // Warp 0 also runs the tile queue and publishes each tile's descriptor.
-    const int pw = warp == 0 ? 0 : 1;
-    const uint64_t pol_w = policy_evict_first();
+    const int pw = warp == 0 ? 0 : warp - kFirstExtraProducer + 1;
+    // weights: evict-first when each expert's tile is read once (small
+    // batches stream every touched expert once), evict-last when several row
+    // tiles of an expert reuse it; routed rows: evict-last (every N tile of a
+    // row tile reads them)
+    const uint64_t pol_w = p.w_reuse ? policy_evict_last() : policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
-    int stage = 0, ds = 0, q = 0;   // q: global stage number (both warps count all stages)
+    int stage = 0, ds = 0, q = 0;   // q: global stage number (every producer counts all stages)
+    // Producers in use: at most one per stage.  A producer waits on a slot's
+    // "empty" barrier by phase parity, which is only unambiguous while the
+    // slot's previous fill (issued by another producer) cannot lag by a whole
+    // ring; with nprod <= NST it cannot.
+    const int nprod = min(C::kProducers, NST);
+    int q_own = -1;                 // last global stage this warp filled
     uint32_t phase = 0, dphase = 0;
     bool ok = true;
     // static schedule state: experts handled by this CTA
@@ -253,13 +267,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (d.nkb < 0) break;
       const int w_row = d.e * p.N + d.n_tile * kTileN;
       for (int i = 0; i < d.nkb; i += SK) {
-        if (((q ^ pw) & 1) == 0) {
+        if (q % nprod == pw) {
           const uint32_t full = smem_u32(&bar_full[stage]);
           if (lane == 0) {
             got = mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, tmo);
             if (got && !p.drop_producer) mbar_arrive_expect_tx(full, stage_bytes);
           }
           if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+          q_own = q;
           if (!p.drop_producer) {
             // one box per lane: weight tile(s), then the activation tile; each
             // box spans SK K blocks (a box running past K reads the fill value)
@@ -283,14 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         set_error(p.ctrl, MOE_ERR_TIMEOUT, 1);
         s_abort = 1;
       }
-      // Warp 0 waits (bounded) until every load of both producers has landed:
-      // a stage's last fill has completed once its "full" phase has flipped.
-      if (pw == 0 && !p.drop_producer) {
-        for (int i = 0; i < NST; ++i) {
-          // stages [0, stage) were filled in the current pass, the rest in the previous one
-          const uint32_t par = (i < stage) ? phase : phase ^ 1u;
-          mbar_wait(smem_u32(&bar_full[i]), par, &s_abort, tmo);
-        }
+      // Each producer waits (bounded by time, also after an abort) until the
+      // loads it issued into the ring's last pass (global stages after
+      // q - NST, whose slots are not refilled) have landed, so no copy is
+      // still writing shared memory when the CTA exits.
+      if (!p.drop_producer) {
+        for (int qq = q_own; qq >= 0 && qq > q - NST; qq -= nprod)
+          mbar_wait_drain(smem_u32(&bar_full[qq % NST]), static_cast<uint32_t>(qq / NST) & 1u, tmo);
       }
     }
   } else if (warp == 1) {
@@ -607,13 +621,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 struct GemmVariant {
   const void* fn;
   int stage_bytes;
+  int threads;
 };
 
 template <int BM, bool kFP8, int kEpi>
 GemmVariant variant() {
   using C = Cfg<BM, kFP8, kEpi>;
   return GemmVariant{reinterpret_cast<const void*>(&grouped_gemm_kernel<BM, kFP8, kEpi>),
-                     C::kStageBytes};
+                     C::kStageBytes, C::kThreads};
 }
 
 template <bool kFP8, int kEpi>
@@ -669,7 +684,7 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(v.threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

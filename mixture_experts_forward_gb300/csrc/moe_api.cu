@@ -168,6 +168,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   p.kb_per_split = (p.KB + p.k_splits - 1) / p.k_splits;
   p.n_tiles = (a->epilogue == MOE_EPI_SWIGLU ? a->N / 2 : a->N) / 128;
   p.sched = a->sched;
+  p.w_reuse = 2LL * a->R >= static_cast<long long>(a->block_m) * a->E ? 1 : 0;
   p.drop_producer = g_drop_producer;
   p.timeout_ns = g_timeout_ns;
   const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m);

@@ -104,6 +104,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Bounded wait that ignores the abort flag: for draining this thread's own
+// in-flight copies before exit.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
 // ----------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) — 2-D tiled loads into shared memory, completing
 // on an mbarrier with a transaction-byte count.

@@ -35,6 +35,7 @@ struct GemmParams {
   int sched;
   int num_stages;
   int sk;                       // K blocks per pipeline stage (1 or 2)
+  int w_reuse;                  // experts average more than one row tile: keep weights in L2
   int drop_producer;
   unsigned long long timeout_ns;
 };
