@@ -92,8 +92,25 @@ __host__ __device__ inline int meta_slot_bytes(bool fp8, int bm, int kb_per_spli
   return (n * 4 + 15) & ~15;
 }
 
+// Work items of the queue: with a split tail (p.tail_tiles > 0, one K split)
+// the last tail_tiles output tiles are handed out as two K halves each, so
+// the final wave of work is half as long; the other items are whole tiles.
+__device__ __forceinline__ int work_items(const GemmParams& p, const int* s_tile_off) {
+  const int T = s_tile_off[p.E] * p.n_tiles * p.k_splits;
+  return T + min(p.tail_tiles, T);
+}
+
 __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const int* s_tile_off,
                                             const int* s_off, int BM, TileDesc& d) {
+  int half = -1;  // >= 0: K half of a split tail tile
+  if (p.tail_tiles > 0) {
+    const int T = s_tile_off[p.E] * p.n_tiles;
+    const int F = T - min(p.tail_tiles, T);
+    if (t >= F) {
+      half = (t - F) & 1;
+      t = F + ((t - F) >> 1);
+    }
+  }
   const int per_m = p.n_tiles * p.k_splits;
   const int mt = t / per_m;
   const int r = t - mt * per_m;
@@ -112,6 +129,10 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const in
   const int ks = r - d.n_tile * p.k_splits;
   d.kb0 = ks * p.kb_per_split;
   d.nkb = min(p.kb_per_split, p.KB - d.kb0);
+  if (half >= 0) {  // split point on a stage boundary (tail_halfkb is a multiple of sk)
+    d.kb0 = half * p.tail_halfkb;
+    d.nkb = half ? p.KB - p.tail_halfkb : p.tail_halfkb;
+  }
 }
 
 template <int BM, bool kFP8, int kEpi>
@@ -179,7 +200,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
   // its griddepcontrol.wait still waits for this grid to complete.
   pdl_launch_dependents();
   const uint32_t tmem_base = s_tmem;
-  const int total_tiles = s_tile_off[p.E] * p.n_tiles * p.k_splits;
+  const int total_tiles = work_items(p, s_tile_off);
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0 || warp >= kFirstExtraProducer) {

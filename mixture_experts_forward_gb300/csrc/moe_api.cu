@@ -183,6 +183,13 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   if (stages > 16) stages = 16;
   if (stages < 2) return MOE_ERR_UNSUPPORTED;
   p.num_stages = stages;
+  // FP8 scatter through the queue: split the last wave (one tile per CTA) in
+  // K halves, so CTAs finish within half a tile of one another
+  const int ctas = a->num_ctas > 0 ? a->num_ctas : sms;
+  p.tail_halfkb = (p.KB / 2) / p.sk * p.sk;
+  if (fp8 && a->epilogue == MOE_EPI_SCATTER && p.k_splits == 1 && a->sched == MOE_SCHED_QUEUE &&
+      p.tail_halfkb >= p.sk && p.KB - p.tail_halfkb >= p.sk)
+    p.tail_tiles = ctas;
   CUtensorMap tw, ta;
   if (!make_tmap(&tw, a->w, fp8, static_cast<uint64_t>(a->K),
                  static_cast<uint64_t>(a->E) * a->N, 128u, static_cast<uint32_t>(p.sk)))
@@ -190,7 +197,6 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   if (!make_tmap(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->R),
                  static_cast<uint32_t>(a->block_m), static_cast<uint32_t>(p.sk)))
     return MOE_ERR_CUDA;
-  const int ctas = a->num_ctas > 0 ? a->num_ctas : sms;
   return cuda_status(launch_grouped_gemm(tw, ta, p, fp8, a->epilogue, a->block_m, ctas, stream,
                                          pdl));
 }

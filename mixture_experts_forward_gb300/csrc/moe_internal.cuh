@@ -36,6 +36,8 @@ struct GemmParams {
   int num_stages;
   int sk;                       // K blocks per pipeline stage (1 or 2)
   int w_reuse;                  // experts average more than one row tile: keep weights in L2
+  int tail_tiles;               // queue, FP8 scatter, one K split: last tiles split in K halves
+  int tail_halfkb;              // K blocks of a split tile's first half (a multiple of sk)
   int drop_producer;
   unsigned long long timeout_ns;
 };

@@ -118,8 +118,9 @@ __device__ int block_exclusive_scan(int* v, int n, int* s_tmp) {
 // route's expert id into shared memory and finds its own routes' slots
 // directly: slot(r) = #{routes with a smaller expert id} + #{earlier routes of
 // the same expert} — the same stable layout the layout kernel builds, without
-// a device-wide handoff.  CTA 0 also writes counts, offsets and tile offsets
-// and re-zeroes the tile-queue counters.  Used when M * top_k is small.
+// a device-wide handoff.  One extra CTA (the last; it has no tokens) writes
+// counts, offsets and tile offsets and re-zeroes the tile-queue counters.
+// Used when M * top_k is small.
 __global__ void __launch_bounds__(1024) quant_layout_kernel(
     const __nv_bfloat16* __restrict__ x, int M, int K, int k, int E, int block_m,
     const int32_t* __restrict__ ids, uint8_t* __restrict__ a_q, float* __restrict__ a_scales,
@@ -203,8 +204,9 @@ __global__ void __launch_bounds__(1024) quant_layout_kernel(
   }
   if (threadIdx.x == 0 && s_bad) set_error(ctrl, MOE_ERR_DEVICE_FAULT, 2);
 
-  if (blockIdx.x == 0) {
-    // counts, offsets and tile offsets of all experts
+  if (blockIdx.x == gridDim.x - 1) {
+    // counts, offsets and tile offsets of all experts (the extra CTA, in
+    // parallel with the others' slot search)
     for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
     if (threadIdx.x == 0 && ctrl != nullptr) {
       ctrl->queue = 0;
@@ -292,7 +294,7 @@ cudaError_t launch_quant_layout(const void* x, int M, int K, int k, int E, int b
   if (err == cudaSuccess) err = prefer_max_shared(quant_layout_kernel);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((M + tpc - 1) / tpc);
+  cfg.gridDim = dim3((M + tpc - 1) / tpc + 1);  // + the counts / offsets CTA
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
