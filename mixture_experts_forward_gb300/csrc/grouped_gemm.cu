@@ -148,8 +148,6 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
   __shared__ TileDesc s_desc[kMaxRing];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int s_tile_off[kMaxE + 1];
-  __shared__ int s_off[kMaxE + 1];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -159,6 +157,9 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
   const int stage_bytes = SK * C::kStageBytes;
   const int meta_bytes = meta_slot_bytes(kFP8, BM, p.kb_per_split);
   uint8_t* s_meta = smem_gen + NST * stage_bytes;       // C::kRing slots of meta_bytes
+  // tile offsets and row offsets of the experts ([E + 1] each) after the ring
+  int* s_tile_off = reinterpret_cast<int*>(s_meta + C::kRing * meta_bytes);
+  int* s_off = s_tile_off + (p.E + 1);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -685,6 +686,8 @@ int gemm_stage_bytes(bool fp8, int epi, int bm) {
   return v.stage_bytes;
 }
 
+int gemm_table_bytes(int E) { return (2 * (E + 1) * 4 + 15) & ~15; }
+
 int gemm_meta_bytes(bool fp8, int bm, int kb_per_split) {
   return ring_slots(fp8, bm) * meta_slot_bytes(fp8, bm, kb_per_split);
 }
@@ -694,9 +697,9 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
                                 cudaStream_t stream, bool pdl) {
   GemmVariant v;
   if (!select_gemm_variant(fp8, epi, bm, v)) return cudaErrorInvalidValue;
-  if (p.sk < 1 || p.sk > 2) return cudaErrorInvalidValue;
+  if (p.sk != 1 && p.sk != 2 && p.sk != 4) return cudaErrorInvalidValue;
   const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * p.sk * v.stage_bytes +
-                      gemm_meta_bytes(fp8, bm, p.kb_per_split);
+                      gemm_meta_bytes(fp8, bm, p.kb_per_split) + gemm_table_bytes(p.E);
   cudaError_t err = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err == cudaSuccess)

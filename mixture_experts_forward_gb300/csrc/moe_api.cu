@@ -174,11 +174,13 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m);
   if (stage_bytes <= 0) return MOE_ERR_UNSUPPORTED;
   const int meta_bytes = gemm_meta_bytes(fp8, a->block_m, p.kb_per_split);
-  // Two K blocks per stage (twice the bytes per copy, and 256 contiguous
-  // bytes of every weight row per copy) wherever a split holds whole pairs
-  // and at least three stages still fit.
-  const int avail = 232448 - 1024 - 12288 - meta_bytes;
-  p.sk = (p.kb_per_split % 2 == 0 && avail / (2 * stage_bytes) >= 3) ? 2 : 1;
+  // Several K blocks per stage (more bytes per copy instruction, and 128 *
+  // sk contiguous bytes of every weight row per copy): the largest of 4, 2, 1
+  // that divides a split and still leaves at least three stages.
+  const int avail = 232448 - 1024 - 2048 - meta_bytes - gemm_table_bytes(a->E);
+  p.sk = 1;
+  for (int sk = 4; sk >= 2; sk /= 2)
+    if (p.kb_per_split % sk == 0 && avail / (sk * stage_bytes) >= 3) { p.sk = sk; break; }
   int stages = avail / (p.sk * stage_bytes);
   if (stages > 16) stages = 16;
   if (stages < 2) return MOE_ERR_UNSUPPORTED;

@@ -34,7 +34,7 @@ struct GemmParams {
   int n_tiles;                  // output tiles of 128 columns
   int sched;
   int num_stages;
-  int sk;                       // K blocks per pipeline stage (1 or 2)
+  int sk;                       // K blocks per pipeline stage (1, 2 or 4)
   int w_reuse;                  // experts average more than one row tile: keep weights in L2
   int tail_tiles;               // queue, FP8 scatter, one K split: last tiles split in K halves
   int tail_halfkb;              // K blocks of a split tile's first half (a multiple of sk)
@@ -93,5 +93,6 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
                                 cudaStream_t stream, bool pdl);
 int gemm_stage_bytes(bool fp8, int epi, int bm);
 int gemm_meta_bytes(bool fp8, int bm, int kb_per_split);
+int gemm_table_bytes(int E);
 
 }  // namespace moe
