@@ -485,54 +485,113 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
         float acc[BM];
 #pragma unroll
         for (int s = 0; s < BM; ++s) acc[s] = 0.0f;
-        for (int i = 0; i < d.nkb && ok; i += C::kKbGroup) {
-          const int ng = min(C::kKbGroup, d.nkb - i);
-          // wait for the partials of K blocks i .. i+ng-1
-          bool got = true;
-          for (int g = 0; g < ng; ++g) {
-            const int a = acc_n + g;
-            got = got && mbar_wait(smem_u32(&bar_tfull[a % C::kNumAcc]),
-                                   static_cast<uint32_t>(a / C::kNumAcc) & 1u, &s_abort, tmo);
-          }
-          if (!__all_sync(0xffffffffu, got)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        if constexpr (C::kKbGroup == 1 && BM >= 64) {
+          // One K block per TMEM buffer, read in 32-column chunks with two
+          // register buffers: the next chunk's load is in flight while this
+          // chunk is folded in, and the buffer is released as soon as its last
+          // chunk has arrived (before that chunk's multiply-adds).
+          constexpr int kCh = 32, kNCh = BM / kCh;
+          for (int i = 0; i < d.nkb && ok; ++i) {
+            const int a = acc_n;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(smem_u32(&bar_tfull[a % C::kNumAcc]),
+                                      static_cast<uint32_t>(a / C::kNumAcc) & 1u, &s_abort, tmo))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t base = lane_addr + (a % C::kNumAcc) * C::kAccCols;
+            const float4* scb = reinterpret_cast<const float4*>(sc + i * BM);
+            float va[kCh], vb[kCh];
+            tmem_ld16(base, *reinterpret_cast<float(*)[16]>(&va[0]));
+            tmem_ld16(base + 16, *reinterpret_cast<float(*)[16]>(&va[16]));
+            tmem_ld_wait(*reinterpret_cast<float(*)[16]>(&va[0]));
+            tmem_ld_wait(*reinterpret_cast<float(*)[16]>(&va[16]));
 #pragma unroll
-          for (int c0 = 0; c0 < BM; c0 += C::kLdCols) {
-            float v[C::kKbGroup][C::kLdCols];
+            for (int ch = 0; ch < kNCh; ++ch) {
+              float* cur = (ch & 1) ? vb : va;
+              float* nxt = (ch & 1) ? va : vb;
+              if (ch + 1 < kNCh) {
+                tmem_ld16(base + (ch + 1) * kCh, *reinterpret_cast<float(*)[16]>(nxt));
+                tmem_ld16(base + (ch + 1) * kCh + 16, *reinterpret_cast<float(*)[16]>(nxt + 16));
+              } else {
+                // every chunk of this K block is in registers: hand the buffer back
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[a % C::kNumAcc]));
+              }
 #pragma unroll
-            for (int g = 0; g < C::kKbGroup; ++g) {
-              if (g < ng) {
-                const uint32_t base = lane_addr + ((acc_n + g) % C::kNumAcc) * C::kAccCols + c0;
-#pragma unroll
-                for (int j = 0; j < C::kLdCols; j += 16)
-                  tmem_ld16(base + j, *reinterpret_cast<float(*)[16]>(&v[g][j]));
+              for (int j = 0; j < kCh; j += 4) {
+                const float4 f = scb[(ch * kCh + j) / 4];
+                acc[ch * kCh + j] = fmaf(cur[j], f.x, acc[ch * kCh + j]);
+                acc[ch * kCh + j + 1] = fmaf(cur[j + 1], f.y, acc[ch * kCh + j + 1]);
+                acc[ch * kCh + j + 2] = fmaf(cur[j + 2], f.z, acc[ch * kCh + j + 2]);
+                acc[ch * kCh + j + 3] = fmaf(cur[j + 3], f.w, acc[ch * kCh + j + 3]);
+              }
+              if (ch + 1 < kNCh) {
+                tmem_ld_wait(*reinterpret_cast<float(*)[16]>(nxt));
+                tmem_ld_wait(*reinterpret_cast<float(*)[16]>(nxt + 16));
               }
             }
-            tmem_ld_wait();
+            ++acc_n;
+          }
+        } else {
+          for (int i = 0; i < d.nkb && ok; i += C::kKbGroup) {
+            const int ng = min(C::kKbGroup, d.nkb - i);
+            // wait for the partials of K blocks i .. i+ng-1
+            bool got = true;
+            for (int g = 0; g < ng; ++g) {
+              const int a = acc_n + g;
+              got = got && mbar_wait(smem_u32(&bar_tfull[a % C::kNumAcc]),
+                                     static_cast<uint32_t>(a / C::kNumAcc) & 1u, &s_abort, tmo);
+            }
+            if (!__all_sync(0xffffffffu, got)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-            for (int g = 0; g < C::kKbGroup; ++g) {
-              if (g < ng) {
-                // scale products of this K block (16-byte aligned, broadcast reads)
-                const float4* scg = reinterpret_cast<const float4*>(sc + (i + g) * BM + c0);
+            for (int c0 = 0; c0 < BM; c0 += C::kLdCols) {
+              float v[C::kKbGroup][C::kLdCols];
 #pragma unroll
-                for (int j = 0; j < C::kLdCols; j += 4) {
-                  const float4 f = scg[j / 4];
-                  acc[c0 + j] = fmaf(v[g][j], f.x, acc[c0 + j]);
-                  acc[c0 + j + 1] = fmaf(v[g][j + 1], f.y, acc[c0 + j + 1]);
-                  acc[c0 + j + 2] = fmaf(v[g][j + 2], f.z, acc[c0 + j + 2]);
-                  acc[c0 + j + 3] = fmaf(v[g][j + 3], f.w, acc[c0 + j + 3]);
+              for (int g = 0; g < C::kKbGroup; ++g) {
+                if (g < ng) {
+                  const uint32_t base = lane_addr + ((acc_n + g) % C::kNumAcc) * C::kAccCols + c0;
+#pragma unroll
+                  for (int j = 0; j < C::kLdCols; j += 16)
+                    tmem_ld16(base + j, *reinterpret_cast<float(*)[16]>(&v[g][j]));
+                }
+              }
+#pragma unroll
+              for (int g = 0; g < C::kKbGroup; ++g) {
+                if (g < ng) {
+#pragma unroll
+                  for (int j = 0; j < C::kLdCols; j += 16)
+                    tmem_ld_wait(*reinterpret_cast<float(*)[16]>(&v[g][j]));
+                }
+              }
+#pragma unroll
+              for (int g = 0; g < C::kKbGroup; ++g) {
+                if (g < ng) {
+                  // scale products of this K block (16-byte aligned, broadcast reads)
+                  const float4* scg = reinterpret_cast<const float4*>(sc + (i + g) * BM + c0);
+#pragma unroll
+                  for (int j = 0; j < C::kLdCols; j += 4) {
+                    const float4 f = scg[j / 4];
+                    acc[c0 + j] = fmaf(v[g][j], f.x, acc[c0 + j]);
+                    acc[c0 + j + 1] = fmaf(v[g][j + 1], f.y, acc[c0 + j + 1]);
+                    acc[c0 + j + 2] = fmaf(v[g][j + 2], f.z, acc[c0 + j + 2]);
+                    acc[c0 + j + 3] = fmaf(v[g][j + 3], f.w, acc[c0 + j + 3]);
+                  }
                 }
               }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+              for (int g = 0; g < ng; ++g) mbar_arrive(smem_u32(&bar_tempty[(acc_n + g) % C::kNumAcc]));
+            acc_n += ng;
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0)
-            for (int g = 0; g < ng; ++g) mbar_arrive(smem_u32(&bar_tempty[(acc_n + g) % C::kNumAcc]));
-          acc_n += ng;
         }
         if (!ok) break;
         if constexpr (kEpi == MOE_EPI_SCATTER) {
@@ -576,7 +635,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
           if constexpr (C::kSwiglu) {
             float u[16];
             tmem_ld16(lane_addr + buf * C::kAccCols + BM + c0, u);
-            tmem_ld_wait();
+            tmem_ld_wait(v);
+            tmem_ld_wait(u);
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
             const int I = p.N / 2;
 #pragma unroll
@@ -588,7 +648,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
               }
             }
           } else {
-            tmem_ld_wait();
+            tmem_ld_wait(v);
             float* out = static_cast<float*>(p.out);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
