@@ -642,8 +642,11 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               if (c0 + j < d.rows) {
+                // silu(g) * u with the fast exponential and division (relative
+                // error ~1e-6, far inside the bf16 rounding of h); for very
+                // negative g the denominator overflows and silu -> 0
                 const float g = v[j];
-                const float h = __fdiv_rn(g, 1.0f + expf(-g)) * u[j];
+                const float h = __fdividef(g, 1.0f + __expf(-g)) * u[j];
                 out[static_cast<size_t>(d.m0 + c0 + j) * I + col] = __float2bfloat16_rn(h);
               }
             }
