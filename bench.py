@@ -302,19 +302,26 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
     if kind == "fp8":
         M, K, N, E, k = c["M"], c["K"], c["N"], c["E"], c["k"]
         _, wts = L.route(d["logits"].to(dev), k, softcap=c["softcap"])
-        acc = torch.zeros(M, N, dtype=torch.float32, device=dev)
-        a_q, a_s = L.quant_gather(d["x"].to(dev), k, lay["route_slot"], zero_acc=acc)
+        R = M * k
+        # the forward's epilogue: weighted fp32 scatter-add (small batches) or
+        # bf16 expert-compact rows (large batches, reduced afterwards)
+        small = M * N * 4 <= (112 << 20)   # the forward's choice (fp32 accumulator on chip)
+        acc = torch.zeros(M, N, dtype=torch.float32, device=dev) if small else \
+            torch.zeros(R, N, dtype=torch.bfloat16, device=dev)
+        a_q, a_s = L.quant_gather(d["x"].to(dev), k, lay["route_slot"],
+                                  zero_acc=acc if small else None)
         w, w_s = d["w_q"].to(dev), d["w_scales"].to(dev)
 
         def launch():
-            L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_SCATTER, a=a_q, a_scales=a_s, w=w,
+            L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_SCATTER if small else L.EPI_STORE_BF16,
+                           a=a_q, a_scales=a_s, w=w,
                            w_scales=w_s, offsets=lay["offsets"], tile_offsets=lay["tile_offsets"],
                            out=acc, ws=ws, block_m=block_m, sorted_route_ids=lay["sorted_route_ids"],
                            route_weights=wts, M=M, top_k=k, sched=sched, k_splits=k_splits)
-        R = M * k
-        alg = touched * (N * K + (N // 128) * (K // 128) * 4) + R * K + (K // 128) * R * 4 + M * N * 4
+        out_bytes = M * N * 4 if small else R * N * 2
+        alg = touched * (N * K + (N // 128) * (K // 128) * 4) + R * K + (K // 128) * R * 4 + out_bytes
         fl = 2.0 * R * N * K
-        name = "grouped_gemm_kernel<fp8, scatter>"
+        name = "grouped_gemm_kernel<fp8, scatter>" if small else "grouped_gemm_kernel<fp8, store_bf16>"
         src = "grouped_gemm.cu"
     else:
         return None

@@ -52,7 +52,10 @@ typedef enum { MOE_DTYPE_FP8_E4M3 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype_t;
 typedef enum {
   MOE_EPI_SCATTER = 0,  /* out f32 [M,N] += route_weight * row   (weighted scatter-add) */
   MOE_EPI_STORE = 1,    /* out f32 [R,N]  = row                   (expert-compact rows) */
-  MOE_EPI_SWIGLU = 2    /* out bf16 [R,N/2] = silu(gate) * up; weight rows [0,N/2) gate, [N/2,N) up */
+  MOE_EPI_SWIGLU = 2,   /* out bf16 [R,N/2] = silu(gate) * up; weight rows [0,N/2) gate, [N/2,N) up */
+  MOE_EPI_STORE_BF16 = 3 /* out bf16 [R,N] = bf16(row)            (expert-compact rows; the
+                            forward's large-batch path reduces them with the route weights
+                            afterwards instead of scatter-adding into an fp32 accumulator) */
 } moe_epilogue_t;
 
 typedef enum {
@@ -120,7 +123,7 @@ moe_status_t moe_quant_gather(const void* x, int M, int K, int top_k,
 /* Arguments of one grouped GEMM launch (see moe_grouped_gemm). */
 typedef struct {
   moe_dtype_t dtype;          /* FP8_E4M3 (blockwise scales) or BF16 */
-  moe_epilogue_t epilogue;    /* SCATTER, STORE or SWIGLU */
+  moe_epilogue_t epilogue;    /* SCATTER, STORE, SWIGLU or STORE_BF16 */
   moe_sched_t sched;          /* QUEUE or STATIC */
   int block_m;                /* routed rows per tile: 16..256, multiple of 16
                                  (FP8: at most 128) */
@@ -146,7 +149,8 @@ typedef struct {
  *   FP8:  Y[s,n] = sum_b a_scales[b,s] * w_scales[e,n/128,b] *
  *                  sum_{k in block b} a[s,k] * w[e,n,k]       (fp32 accumulation)
  *   BF16: Y[s,n] = sum_k a[s,k] * w[e,n,k]
- * and the epilogue stores Y (STORE), applies silu(gate)*up (SWIGLU) or adds
+ * and the epilogue stores Y (STORE; STORE_BF16 rounds it to bf16), applies
+ * silu(gate)*up (SWIGLU) or adds
  * route_weights[r] * Y[s,:] to out[r / top_k, :] for r = sorted_route_ids[s]
  * (SCATTER; out must be zeroed or hold a partial sum).
  * Runs on tcgen05 tensor cores (TMEM accumulators, TMA-fed shared memory).
@@ -189,11 +193,17 @@ size_t moe_workspace_size(const moe_forward_args* args);
 
 /* The tile rows (block_m) and FP8 K split that moe_forward uses for these
  * arguments, so a caller can reproduce its grouped GEMM with
- * moe_grouped_gemm (k_splits is 1 on the BF16 path). */
+ * moe_grouped_gemm (k_splits is 1 on the BF16 path and whenever the forward
+ * stores bf16 rows instead of scatter-adding). */
 moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k_splits);
 
 /* Fused forward: route -> layout -> quantise+gather (FP8) or gather (BF16)
- * -> grouped GEMM(s) with the weighted scatter fused -> bf16 output.
+ * -> grouped GEMM(s) -> weighted scatter -> bf16 output.  While the fp32
+ * output accumulator (M x out x 4 bytes) is at most 112 MiB the weighted
+ * scatter is fused into the last GEMM's epilogue (fp32 reductions into the
+ * accumulator, then one bf16 rounding); above that the GEMM stores each
+ * routed row in bf16 and a reduction kernel sums each token's top_k rows
+ * with the route weights in fp32 (in route order) before the bf16 rounding.
  * out: bf16 [M, N] (FP8) or [M, K] (BF16).  ws: device workspace of
  * moe_workspace_size() bytes, 256-byte aligned, control block zeroed once.
  * With use_graph = 1 the launch sequence is captured (on a private stream) on

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_FAULT = 4, 5, 6
 DTYPE_FP8, DTYPE_BF16 = 0, 1
-EPI_SCATTER, EPI_STORE, EPI_SWIGLU = 0, 1, 2
+EPI_SCATTER, EPI_STORE, EPI_SWIGLU, EPI_STORE_BF16 = 0, 1, 2, 3
 SCHED_QUEUE, SCHED_STATIC = 0, 1
 CTRL_BYTES = 256
 

@@ -613,6 +613,13 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
                   red_add_f32(out + static_cast<size_t>(tk[j]) * p.N, ww[j] * acc[s0 + j]);
             }
           }
+        } else if constexpr (kEpi == MOE_EPI_STORE_BF16) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+          for (int s = 0; s < BM; ++s) {
+            if (s < d.rows)
+              out[static_cast<size_t>(d.m0 + s) * p.N + col] = __float2bfloat16_rn(acc[s]);
+          }
         } else {
           float* out = static_cast<float*>(p.out);
 #pragma unroll
@@ -652,14 +659,17 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
             }
           } else {
             tmem_ld_wait(v);
-            float* out = static_cast<float*>(p.out);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               if (c0 + j < d.rows) {
+                const size_t r = static_cast<size_t>(d.m0 + c0 + j);
                 if constexpr (kEpi == MOE_EPI_SCATTER)
-                  red_add_f32(out + static_cast<size_t>(tok[c0 + j]) * p.N + col, wt[c0 + j] * v[j]);
+                  red_add_f32(static_cast<float*>(p.out) + static_cast<size_t>(tok[c0 + j]) * p.N + col,
+                              wt[c0 + j] * v[j]);
+                else if constexpr (kEpi == MOE_EPI_STORE_BF16)
+                  static_cast<__nv_bfloat16*>(p.out)[r * p.N + col] = __float2bfloat16_rn(v[j]);
                 else
-                  out[static_cast<size_t>(d.m0 + c0 + j) * p.N + col] = v[j];
+                  static_cast<float*>(p.out)[r * p.N + col] = v[j];
               }
             }
           }
@@ -735,10 +745,12 @@ bool select_gemm_variant(bool fp8, int epi, int bm, GemmVariant& v) {
   if (fp8) {
     if (epi == MOE_EPI_SCATTER) return pick_bm<true, MOE_EPI_SCATTER>(bm, v);
     if (epi == MOE_EPI_STORE) return pick_bm<true, MOE_EPI_STORE>(bm, v);
+    if (epi == MOE_EPI_STORE_BF16) return pick_bm<true, MOE_EPI_STORE_BF16>(bm, v);
     return false;
   }
   if (epi == MOE_EPI_SCATTER) return pick_bm<false, MOE_EPI_SCATTER>(bm, v);
   if (epi == MOE_EPI_STORE) return pick_bm<false, MOE_EPI_STORE>(bm, v);
+  if (epi == MOE_EPI_STORE_BF16) return pick_bm<false, MOE_EPI_STORE_BF16>(bm, v);
   if (epi == MOE_EPI_SWIGLU) return pick_bm<false, MOE_EPI_SWIGLU>(bm, v);
   return false;
 }

@@ -101,7 +101,7 @@ moe_status_t check_gemm(const moe_gemm_args* a) {
   if (a == nullptr) return MOE_ERR_INVALID_ARG;
   const bool fp8 = a->dtype == MOE_DTYPE_FP8_E4M3;
   if (a->dtype != MOE_DTYPE_FP8_E4M3 && a->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
-  if (a->epilogue < MOE_EPI_SCATTER || a->epilogue > MOE_EPI_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (a->epilogue < MOE_EPI_SCATTER || a->epilogue > MOE_EPI_STORE_BF16) return MOE_ERR_INVALID_ARG;
   if (a->sched != MOE_SCHED_QUEUE && a->sched != MOE_SCHED_STATIC) return MOE_ERR_INVALID_ARG;
   if (a->E <= 0 || a->N <= 0 || a->K <= 0 || a->R <= 0) return MOE_ERR_INVALID_ARG;
   if (a->a == nullptr || a->w == nullptr || a->offsets == nullptr || a->tile_offsets == nullptr ||
@@ -218,6 +218,17 @@ bool forward_shape_ok(const moe_forward_args* f) {
   return f != nullptr && f->M > 0 && f->K > 0 && f->N > 0 && f->E > 0 && f->top_k > 0;
 }
 
+// The weighted scatter's form: while the fp32 output accumulator fits well
+// inside L2 the last GEMM scatter-adds into it (reductions stay on chip and
+// one conversion pass follows); a larger accumulator would be read and
+// written back to HBM by the reductions, so the GEMM stores each routed row
+// in bf16 instead and one kernel reduces every token's rows (streaming).
+constexpr long long kAccOnChipBytes = 112ll << 20;
+bool rows_path(const moe_forward_args* f) {
+  const long long out_cols = f->dtype == MOE_DTYPE_FP8_E4M3 ? f->N : f->K;
+  return static_cast<long long>(f->M) * out_cols * 4 > kAccOnChipBytes;
+}
+
 WsLayout ws_layout(const moe_forward_args* f) {
   WsLayout L;
   std::memset(&L, 0, sizeof(L));
@@ -244,7 +255,12 @@ WsLayout ws_layout(const moe_forward_args* f) {
   L.a = take(fp8 ? R * K : R * K * 2);
   L.a_scales = fp8 ? take((K / 128) * R * 4) : 0;
   const size_t out_cols = fp8 ? N : K;
-  L.acc = take(M * out_cols * 4);
+  // fp32 accumulator [M, out] for the scatter-add, or bf16 expert-compact rows
+  // [R, out] reduced afterwards (see rows_path)
+  if (rows_path(f))
+    L.acc = take(R * out_cols * 2);
+  else
+    L.acc = take(M * out_cols * 4);
   L.h = fp8 ? 0 : take(R * N * 2);
   L.st_logits = take(M * E * 4);
   L.st_x = take(M * K * 2);
@@ -343,6 +359,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     if (fs != MOE_OK) return fs;
   }
   const bool small = fp8 && quant_layout_fits(M, K, k, E);
+  const bool rows = !small && rows_path(f);
   if (small) {
     // small batch: route, then quantise + layout + gather in one kernel
     e = launch_route(logits, M, E, k, f->softcap, f->renorm, ids, wts, stream, false);
@@ -369,12 +386,13 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
       e = launch_quant_layout(x, M, K, k, E, bm, ids, a_q, a_s, acc, N, counts, offsets, sorted,
                               slot, tile_off, ctrl, stream, pdl);
     else
-      e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, acc, N, pl, stream, pdl);
+      e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, rows ? nullptr : acc, N, pl, stream,
+                              pdl);
     if (e != cudaSuccess) return cuda_status(e);
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));
     g.dtype = MOE_DTYPE_FP8_E4M3;
-    g.epilogue = MOE_EPI_SCATTER;
+    g.epilogue = rows ? MOE_EPI_STORE_BF16 : MOE_EPI_SCATTER;
     g.sched = f->sched;
     g.block_m = bm;
     g.E = E;
@@ -392,19 +410,22 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     g.sorted_route_ids = sorted;
     g.route_weights = wts;
     g.out = acc;
-    g.k_splits = f->k_splits;
+    g.k_splits = rows ? 1 : f->k_splits;
     moe_status_t s = run_gemm(&g, ctrl, false, stream, pdl);
     if (s != MOE_OK) return s;
-    s = cuda_status(launch_finalize(acc, out, static_cast<size_t>(M) * N, device_sms(), stream,
-                                    pdl));
+    if (rows)
+      s = cuda_status(launch_reduce_rows(acc, slot, wts, M, N, k, out, device_sms(), stream, pdl));
+    else
+      s = cuda_status(launch_finalize(acc, out, static_cast<size_t>(M) * N, device_sms(), stream,
+                                      pdl));
     if (s != MOE_OK) return s;
     return pf_bytes > 0 ? side.join(stream) : MOE_OK;
   }
   // BF16 gated FFN: (route + rank above) -> gather, placing the routes -> up (SwiGLU)
-  // -> down (scatter) -> finalize
+  // -> down (scatter-add, or bf16 rows) -> finalize (or weighted row reduction)
   void* a = ws + L.a;
   void* h = ws + L.h;
-  e = launch_gather_rows_bf16(x, M, K, k, slot, a, acc, K, pl, stream, pdl);
+  e = launch_gather_rows_bf16(x, M, K, k, slot, a, rows ? nullptr : acc, K, pl, stream, pdl);
   if (e != cudaSuccess) return cuda_status(e);
   moe_gemm_args g;
   std::memset(&g, 0, sizeof(g));
@@ -426,7 +447,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   g.k_splits = 1;
   moe_status_t s = run_gemm(&g, ctrl, false, stream, pdl);
   if (s != MOE_OK) return s;
-  g.epilogue = MOE_EPI_SCATTER;
+  g.epilogue = rows ? MOE_EPI_STORE_BF16 : MOE_EPI_SCATTER;
   g.N = K;
   g.K = N;
   g.a = h;
@@ -436,6 +457,8 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   g.out = acc;
   s = run_gemm(&g, ctrl, true, stream, pdl);
   if (s != MOE_OK) return s;
+  if (rows)
+    return cuda_status(launch_reduce_rows(acc, slot, wts, M, K, k, out, device_sms(), stream, pdl));
   return cuda_status(launch_finalize(acc, out, static_cast<size_t>(M) * K, device_sms(), stream,
                                      pdl));
 }
@@ -629,7 +652,8 @@ moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k
   const int R = args->M * args->top_k;
   *block_m = args->block_m > 0 ? args->block_m : auto_block_m(fp8, R, args->E);
   *k_splits = 1;
-  if (fp8) {
+  // the scatter-add GEMM may split K; the bf16-rows form uses one split
+  if (fp8 && !rows_path(args)) {
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));
     g.dtype = MOE_DTYPE_FP8_E4M3;

@@ -83,6 +83,10 @@ cudaError_t launch_finalize(const float* acc, void* out, size_t n, int num_sms,
 cudaError_t launch_quant_gather(const void* x, int M, int K, int k, int32_t* route_slot,
                                 uint8_t* a_q, float* a_scales, float* zero_acc, int zero_cols,
                                 const Placement& pl, cudaStream_t stream, bool pdl);
+// out bf16 [M,N] = weighted sum over each token's k bf16 rows (N % 8 == 0).
+cudaError_t launch_reduce_rows(const void* rows, const int32_t* route_slot, const float* weights,
+                               int M, int N, int k, void* out, int num_sms, cudaStream_t stream,
+                               bool pdl);
 cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const float* weights,
                            int M, int N, int k, void* out, cudaStream_t stream);
 cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, int32_t* route_slot,

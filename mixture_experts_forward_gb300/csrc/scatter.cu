@@ -71,6 +71,49 @@ __global__ void __launch_bounds__(256) scatter_kernel(const float* __restrict__ 
   }
 }
 
+// Weighted reduction of bf16 expert-compact rows back to token order (the
+// forward's large-batch form of the weighted scatter): out[t, :] =
+// bf16( sum_j weights[t*k+j] * rows[route_slot[t*k+j], :] ), the sum in j order
+// in fp32.  One thread per token and 8 columns (16-byte loads and stores).
+__global__ void __launch_bounds__(256) reduce_rows_kernel(const uint4* __restrict__ rows,
+                                                          const int32_t* __restrict__ route_slot,
+                                                          const float* __restrict__ weights,
+                                                          int M, int n8, int k,
+                                                          uint4* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int R = M * k;
+  const size_t total = static_cast<size_t>(M) * n8;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
+       i += stride) {
+    const int t = static_cast<int>(i / n8);
+    const int c = static_cast<int>(i - static_cast<size_t>(t) * n8);
+    float acc[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc[u] = 0.0f;
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const int slot = __ldg(route_slot + static_cast<size_t>(t) * k + j);
+      if (slot < 0 || slot >= R) continue;
+      const float w = __ldg(weights + static_cast<size_t>(t) * k + j);
+      const uint4 v = __ldcs(rows + static_cast<size_t>(slot) * n8 + c);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 f = __bfloat1622float2(h[u]);
+        acc[2 * u] = __fmaf_rn(w, f.x, acc[2 * u]);
+        acc[2 * u + 1] = __fmaf_rn(w, f.y, acc[2 * u + 1]);
+      }
+    }
+    uint4 o;
+    __nv_bfloat162* ho = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ho[u] = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
+    out[i] = o;
+  }
+}
+
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, int M,
                                                           int row_vecs, int k, int32_t* route_slot,
                                                           uint4* __restrict__ a,
@@ -145,6 +188,20 @@ cudaError_t launch_finalize(const float* acc, void* out, size_t n, int num_sms,
   cudaLaunchConfig_t cfg = make_cfg(dim3(blocks), dim3(256), stream, pdl, attr);
   return cudaLaunchKernelEx(&cfg, finalize_kernel, reinterpret_cast<const float4*>(acc),
                             static_cast<uint2*>(out), n4);
+}
+
+cudaError_t launch_reduce_rows(const void* rows, const int32_t* route_slot, const float* weights,
+                               int M, int N, int k, void* out, int num_sms, cudaStream_t stream,
+                               bool pdl) {
+  const size_t total = static_cast<size_t>(M) * (N / 8);
+  int blocks = static_cast<int>(std::min<size_t>((total + 255) / 256, static_cast<size_t>(num_sms) * 8));
+  if (blocks < 1) blocks = 1;
+  cudaError_t err = prefer_max_shared(reduce_rows_kernel);
+  if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(blocks), dim3(256), stream, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, reduce_rows_kernel, static_cast<const uint4*>(rows), route_slot,
+                            weights, M, N / 8, k, static_cast<uint4*>(out));
 }
 
 cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const float* weights,

@@ -86,6 +86,8 @@ def _gemm(**kw):
     (dict(epilogue=L.EPI_STORE, k_splits=2), L.MOE_ERR_UNSUPPORTED),
     (dict(dtype=7), L.MOE_ERR_INVALID_ARG), (dict(out=FAKE + 8), L.MOE_ERR_INVALID_ARG),
     (dict(dtype=L.DTYPE_BF16, epilogue=L.EPI_SWIGLU, N=384), L.MOE_ERR_UNSUPPORTED),
+    (dict(epilogue=4), L.MOE_ERR_INVALID_ARG), (dict(epilogue=-1), L.MOE_ERR_INVALID_ARG),
+    (dict(epilogue=L.EPI_STORE_BF16, k_splits=2), L.MOE_ERR_UNSUPPORTED),
 ])
 def test_gemm_argument_errors(lib, kw, code):
     g = _gemm(**kw)

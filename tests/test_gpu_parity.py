@@ -129,7 +129,16 @@ def _fp8_gemm_case(M, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, k_splits=0,
     cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     ws = L.new_workspace(L.CTRL_BYTES)
     R = M * k
-    if epilogue == L.EPI_STORE:
+    if epilogue == L.EPI_STORE_BF16:
+        out = torch.zeros(R, N, dtype=torch.bfloat16, device="cuda")
+        L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_STORE_BF16, a=cu(a_q), a_scales=cu(a_s),
+                       w=d["w_q"].cuda(), w_scales=d["w_scales"].cuda(), offsets=cu(lay["offsets"]),
+                       tile_offsets=cu(lay["tile_offsets"]), out=out, ws=ws, block_m=bm,
+                       sched=sched, num_ctas=num_ctas)
+        torch.cuda.synchronize()
+        assert L.get_error(ws) == L.MOE_OK
+        assert_close(out, Y, "fp8 store bf16")
+    elif epilogue == L.EPI_STORE:
         out = torch.zeros(R, N, device="cuda")
         L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_STORE, a=cu(a_q), a_scales=cu(a_s),
                        w=d["w_q"].cuda(), w_scales=d["w_scales"].cuda(), offsets=cu(lay["offsets"]),
@@ -154,6 +163,12 @@ def _fp8_gemm_case(M, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, k_splits=0,
 @pytest.mark.parametrize("bm", [16, 32, 64, 128])
 def test_gemm_fp8_store_tiles_and_ragged_tail(bm):
     _fp8_gemm_case(M=300, K=512, N=256, E=16, k=4, bm=bm, epilogue=L.EPI_STORE)
+
+
+@pytest.mark.parametrize("bm", [16, 128])
+def test_gemm_fp8_store_bf16_rows(bm):
+    """Expert-compact rows rounded to bf16 (the large-batch forward's epilogue)."""
+    _fp8_gemm_case(M=300, K=1024, N=256, E=16, k=4, bm=bm, epilogue=L.EPI_STORE_BF16, skew=1.0)
 
 
 @pytest.mark.parametrize("bm,sched,ks", [(16, L.SCHED_QUEUE, 1), (64, L.SCHED_STATIC, 1),
@@ -203,7 +218,8 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
         torch.cuda.synchronize()
         assert_close(out, oracle.scatter(Y, lay["route_slot"], rw), "bf16 scatter")
     else:
-        out = torch.zeros(M * k, N, device="cuda")
+        dt = torch.bfloat16 if epilogue == L.EPI_STORE_BF16 else torch.float32
+        out = torch.zeros(M * k, N, dtype=dt, device="cuda")
         L.grouped_gemm(dtype=L.DTYPE_BF16, epilogue=epilogue, a=a.cuda(), w=w.cuda(),
                        offsets=cu(lay["offsets"]), tile_offsets=cu(lay["tile_offsets"]), out=out,
                        ws=ws, block_m=bm, sched=sched)
@@ -213,7 +229,7 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
 
 
 @pytest.mark.parametrize("bm", [16, 64, 128, 256])
-@pytest.mark.parametrize("epi", [L.EPI_STORE, L.EPI_SWIGLU, L.EPI_SCATTER])
+@pytest.mark.parametrize("epi", [L.EPI_STORE, L.EPI_SWIGLU, L.EPI_SCATTER, L.EPI_STORE_BF16])
 def test_gemm_bf16(bm, epi):
     _bf16_gemm_case(R_tokens=200, K=320, N=256, E=8, k=2, bm=bm, epilogue=epi)
 
@@ -270,6 +286,20 @@ def test_forward_skewed_large_batch_fp8_sampled():
     counts = r["counts"]
     assert counts.max() >= 10 * max(1, counts[counts > 0].min())   # skew as specified
     assert_close(out[torch.from_numpy(tok).long().cuda()], r["out"], "skewed")
+
+
+def test_forward_fp8_bf16_rows_path_sampled():
+    """An FP8 forward whose fp32 output accumulator (8192 x 4096 x 4 B) is too
+    large to keep on chip: the GEMM stores bf16 rows and a reduction kernel
+    applies the route weights."""
+    cfg = dict(M=8192, K=256, N=4096, E=8, k=2, softcap=30.0, zipf_bias=0.5)
+    d = inputs.make_fp8_inputs(cfg, seed=5)
+    dev = fp8_device_inputs(d)
+    out, _, _ = run_forward_fp8(dev, d["cfg"])
+    tok = sample_tokens(cfg["M"], 64)
+    r = oracle.forward_fp8(d["logits"].numpy(), bits(d["x"]), d["w_q"].numpy(),
+                           d["w_scales"].numpy(), k=2, softcap=30.0, tokens=tok, threads=THREADS)
+    assert_close(out[torch.from_numpy(tok).long().cuda()], r["out"], "fp8 bf16-rows path")
 
 
 def _bf16_forward_case(cfg_name, routing, rho=1.0, n_tok=32, block_m=0, sched=L.SCHED_QUEUE,
