@@ -244,9 +244,8 @@ __global__ void __launch_bounds__(kLayoutThreads, NPL <= 8 ? 2 : 1)
 
   // ---- last CTA: per-CTA bases, counts, offsets, tile offsets
   // The [nC][E] histograms are staged in shared memory a chunk of `hist_chunk`
-  // CTAs at a time (16-byte loads, all in flight; rows padded to E + 4 ints
-  // against bank conflicts).  Each expert's column is then scanned in rounds
-  // of G consecutive CTAs, one CTA per lane (a segmented shuffle scan), the
+  // CTAs at a time (asynchronous 16-byte copies, all in flight; rows padded to
+  // E + 4 ints), each expert's column is scanned there by G lanes, and the
   // exclusive bases overwrite the chunk in place and go out as 16-byte stores.
   const int nC = gridDim.x;
   const int RS = E + 4;  // staged row stride (ints)
@@ -277,24 +276,53 @@ __global__ void __launch_bounds__(kLayoutThreads, NPL <= 8 ? 2 : 1)
     }
     cp_async_wait_all();
     __syncthreads();
-    // every lane takes part in the shuffles (G divides 32, so an expert's
-    // lanes never straddle two warps); lanes past the last expert add 0
-    int run = act ? s_cnt[e] : 0;
-    for (int c0 = 0; c0 < nc; c0 += G) {
-      const int c = c0 + g;
-      const int h = (act && c < nc) ? s_h[c * RS + e] : 0;
-      int inc = h;
+    // Each of an expert's G lanes takes a contiguous run of L CTAs (L odd,
+    // so the lanes' rows fall in different banks): it sums its run (loads
+    // 8 at a time), a segmented shuffle scan over the G lanes gives the run's
+    // start, and a second pass writes the exclusive bases.  Every lane takes
+    // part in the shuffles (G divides 32, so an expert's lanes never straddle
+    // two warps); lanes past the last expert have empty runs.
+    {
+      const int L = ((nc + G - 1) / G) | 1;
+      const int c0 = min(nc, g * L), c1 = act ? min(nc, c0 + L) : c0;
+      int part = 0;
+      int c = c0;
+      for (; c + 8 <= c1; c += 8) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = s_h[(c + u) * RS + e];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) part += v[u];
+      }
+      for (; c < c1; ++c) part += s_h[c * RS + e];
+      int inc = part;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         if (off >= G) break;
         const int y = __shfl_up_sync(0xffffffffu, inc, off, G);
         if (g >= off) inc += y;
       }
-      if (act && c < nc) s_h[c * RS + e] = run + inc - h;
-      run += __shfl_sync(0xffffffffu, inc, G - 1, G);
+      const int total = __shfl_sync(0xffffffffu, inc, G - 1, G);
+      int run = (act ? s_cnt[e] : 0) + inc - part;
+      c = c0;
+      for (; c + 8 <= c1; c += 8) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = s_h[(c + u) * RS + e];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          s_h[(c + u) * RS + e] = run;
+          run += v[u];
+        }
+      }
+      for (; c < c1; ++c) {
+        const int v = s_h[c * RS + e];
+        s_h[c * RS + e] = run;
+        run += v;
+      }
+      __syncwarp();
+      if (act && g == G - 1) s_cnt[e] += total;
     }
-    __syncwarp();
-    if (act && g == 0) s_cnt[e] = run;
     __syncthreads();
     if (vec) {
       const int q = E >> 2;
@@ -390,9 +418,16 @@ cudaError_t launch_route_rank_t(const float* logits, int M, int E, int k, float 
                                 Ctrl* ctrl, int32_t* local_rank, int32_t* cta_hist,
                                 int32_t* cta_base, cudaStream_t stream, bool pdl) {
   // [32][E] ranking table; the last CTA reuses it for a chunk of the per-CTA
-  // histograms ([hist_chunk][E + 4], at most 96 KB) and the [E] running totals
+  // histograms ([hist_chunk][E + 4]) and the [E] running totals
   const int n_ctas = (M + 31) / 32;
-  int hist_chunk = (24576 - E) / (E + 4);
+  // staging budget: up to 200 KB when the grid fits one CTA per SM anyway,
+  // else 96 KB so that two CTAs still fit on an SM
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 0;
+  const int budget = (sms > 0 && n_ctas <= sms) ? 51200 : 24576;  // ints
+  int hist_chunk = (budget - E) / (E + 4);
   if (hist_chunk > n_ctas) hist_chunk = n_ctas;
   if (hist_chunk < 1) hist_chunk = 1;
   const int staged = hist_chunk * (E + 4) + E;
