@@ -21,8 +21,6 @@ using namespace moe;
 namespace {
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
-// L2 prefetch of FP8 expert weights issued at the start of a forward (bytes).
-constexpr long long kPrefetchBytes = 64ll << 20;
 int g_drop_producer = 0;
 unsigned long long g_timeout_ns = kDefaultTimeoutNs;
 
@@ -290,41 +288,6 @@ moe_status_t check_forward(const moe_forward_args* f) {
   return MOE_OK;
 }
 
-// A second stream for work that runs beside the forward's chain (captured
-// into the same graph as a parallel branch): fork() makes it wait for
-// `origin`, record_join() marks the end of its work, join() makes `origin`
-// wait for that end.  One stream and two events per device, created once.
-struct SideBranch {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
-  moe_status_t fork(cudaStream_t origin) {
-    static cudaStream_t streams[64] = {};
-    static cudaEvent_t forks[64] = {}, joins[64] = {};
-    static std::mutex mu;
-    int dev = 0;
-    moe_status_t s = cuda_status(cudaGetDevice(&dev));
-    if (s != MOE_OK) return s;
-    if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED;
-    {
-      std::lock_guard<std::mutex> lock(mu);
-      if (streams[dev] == nullptr) {
-        s = cuda_status(cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking));
-        if (s == MOE_OK) s = cuda_status(cudaEventCreateWithFlags(&forks[dev], cudaEventDisableTiming));
-        if (s == MOE_OK) s = cuda_status(cudaEventCreateWithFlags(&joins[dev], cudaEventDisableTiming));
-        if (s != MOE_OK) return s;
-      }
-    }
-    stream = streams[dev];
-    fork_ev = forks[dev];
-    join_ev = joins[dev];
-    s = cuda_status(cudaEventRecord(fork_ev, origin));
-    if (s != MOE_OK) return s;
-    return cuda_status(cudaStreamWaitEvent(stream, fork_ev, 0));
-  }
-  moe_status_t record_join() { return cuda_status(cudaEventRecord(join_ev, stream)); }
-  moe_status_t join(cudaStream_t origin) { return cuda_status(cudaStreamWaitEvent(origin, join_ev, 0)); }
-};
-
 // The launch sequence of one forward (no host synchronisation).
 moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, const void* x,
                              void* out, uint8_t* ws, cudaStream_t stream) {
@@ -344,20 +307,6 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   const bool pdl = true;
   cudaError_t e;
 
-  // FP8: prefetch the first weights the GEMM will stream (expert order) into L2
-  // on a side branch (fork here, join after the finalize) while routing,
-  // layout and quantisation run.
-  const long long w_bytes = static_cast<long long>(E) * N * K;
-  const long long pf_bytes = fp8 ? (w_bytes < kPrefetchBytes ? w_bytes : kPrefetchBytes) : 0;
-  SideBranch side;
-  if (pf_bytes > 0) {
-    moe_status_t fs = side.fork(stream);
-    if (fs != MOE_OK) return fs;
-    e = launch_prefetch_l2(f->w, pf_bytes, side.stream);
-    if (e != cudaSuccess) return cuda_status(e);
-    fs = side.record_join();
-    if (fs != MOE_OK) return fs;
-  }
   const bool small = fp8 && quant_layout_fits(M, K, k, E);
   const bool rows = !small && rows_path(f);
   if (small) {
@@ -419,7 +368,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
       s = cuda_status(launch_finalize(acc, out, static_cast<size_t>(M) * N, device_sms(), stream,
                                       pdl));
     if (s != MOE_OK) return s;
-    return pf_bytes > 0 ? side.join(stream) : MOE_OK;
+    return MOE_OK;
   }
   // BF16 gated FFN: (route + rank above) -> gather, placing the routes -> up (SwiGLU)
   // -> down (scatter-add, or bf16 rows) -> finalize (or weighted row reduction)

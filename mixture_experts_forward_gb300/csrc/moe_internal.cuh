@@ -68,7 +68,6 @@ struct Placement {
   int E = 0;
 };
 constexpr int kRankTokensPerCta = 32;
-cudaError_t launch_prefetch_l2(const void* base, long long bytes, cudaStream_t stream);
 // Largest M * top_k for which the forward folds the layout into the
 // quantise/gather kernel (every CTA scans all routes' expert ids).
 constexpr int kQuantLayoutMaxRoutes = 4096;

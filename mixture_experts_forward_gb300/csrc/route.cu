@@ -394,22 +394,6 @@ cudaError_t launch_route(const float* logits, int M, int E, int k, float softcap
   return cudaLaunchKernelEx(&cfg, route_kernel<32>, logits, M, E, k, softcap, renorm, ids, weights);
 }
 
-// Speculative L2 prefetch of the first `bytes` of the expert weights.  The
-// grouped GEMM hands out tiles in expert order, so these are the first
-// weights it streams; the forward runs this kernel on a side branch while
-// routing, layout and quantisation run, so HBM is busy from the start.
-__global__ void __launch_bounds__(32) prefetch_l2_kernel(const uint8_t* __restrict__ base,
-                                                         long long bytes) {
-  constexpr long long kChunk = 64 * 1024;
-  const long long nthreads = static_cast<long long>(gridDim.x) * blockDim.x;
-  const long long per = (bytes / nthreads + kChunk - 1) / kChunk * kChunk;
-  const long long begin = per * (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
-  const long long end = min(bytes, begin + per);
-  for (long long off = begin; off < end; off += kChunk) {
-    const unsigned n = static_cast<unsigned>(min(kChunk, end - off));
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(n) : "memory");
-  }
-}
 
 template <int NPL>
 cudaError_t launch_route_rank_t(const float* logits, int M, int E, int k, float softcap,
@@ -472,12 +456,5 @@ cudaError_t launch_route_rank(const float* logits, int M, int E, int k, float so
 #undef MOE_RR
 }
 
-cudaError_t launch_prefetch_l2(const void* base, long long bytes, cudaStream_t stream) {
-  if (bytes <= 0) return cudaSuccess;
-  cudaError_t err = prefer_max_shared(prefetch_l2_kernel);
-  if (err != cudaSuccess) return err;
-  prefetch_l2_kernel<<<8, 32, 0, stream>>>(static_cast<const uint8_t*>(base), bytes & ~15ll);
-  return cudaGetLastError();
-}
 
 }  // namespace moe
