@@ -63,8 +63,11 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="qwen_small_batch_fp8",
                     choices=list(inputs.FP8_CONFIGS) + list(inputs.BF16_CONFIGS))
-    ap.add_argument("--routing", default="uniform")
-    ap.add_argument("--rho", type=float, default=1.0)
+    ap.add_argument("--routing", default=None,
+                    help="BF16 routing: balanced | uniform | zipf1.2 | loads "
+                         "(default: loads for imbalance_bf16, else uniform)")
+    ap.add_argument("--rho", type=float, default=None,
+                    help="max/min expert load for --routing loads (default 40)")
     ap.add_argument("--block-m", type=int, default=0)
     ap.add_argument("--k-splits", type=int, default=0)
     ap.add_argument("--sched", choices=["queue", "static"], default="queue")
@@ -110,10 +113,12 @@ def workload(cfg_name, args, seed):
         desc = (f"{cfg_name} M={c['M']} K={c['K']} N={c['N']} E={c['E']} top{c['k']} "
                 f"softcap={c['softcap']:g} fp8-e4m3 128x128/1x128 blocks")
         return "fp8", d, desc
-    d = inputs.make_bf16_inputs(cfg_name, routing=args.routing, rho=args.rho, seed=seed)
+    routing = args.routing or ("loads" if cfg_name == "imbalance_bf16" else "uniform")
+    rho = args.rho if args.rho is not None else (40.0 if routing == "loads" else 1.0)
+    d = inputs.make_bf16_inputs(cfg_name, routing=routing, rho=rho, seed=seed)
     c = d["cfg"]
     desc = (f"{cfg_name} T={c['T']} H={c['H']} I={c['I']} E={c['E']} top{c['k']} "
-            f"routing={args.routing} rho={args.rho:g} bf16 gated FFN")
+            f"routing={routing} rho={rho:g} bf16 gated FFN")
     return "bf16", d, desc
 
 
