@@ -236,9 +236,11 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
     const int st_stride = G >= p.E ? (G - (c % p.E) + p.E - 1) / p.E : 1;
     int st_lt = st_idx;
     // queue: CTA c starts with tile c; later tiles come from the counter
-    // (offset by the grid size), claimed one tile ahead so the atomic's
-    // round trip overlaps this tile's loads
+    // (offset by the grid size), claimed one tile ahead — after the current
+    // tile's first stage has been issued, so the atomic's round trip overlaps
+    // that tile's loads instead of delaying them
     int queued = p.sched == MOE_SCHED_QUEUE ? c : -1;
+    bool claim = false;             // lane 0 of warp 0: the next tile is still to be claimed
     for (;;) {
       TileDesc d;
       bool got = true;
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
         if (lane == 0) {
           if (p.sched == MOE_SCHED_QUEUE) {
             t = queued < total_tiles ? queued : -1;
-            if (t >= 0) queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
+            claim = t >= 0;
           } else {
             while (st_e < p.E) {
               const int per_e = (s_tile_off[st_e + 1] - s_tile_off[st_e]) * p.n_tiles * p.k_splits;
@@ -265,7 +267,13 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
         t = __shfl_sync(0xffffffffu, t, 0);
         if (t >= 0) {
           decode_tile(t, p, s_tile_off, s_off, BM, d);
-          if (d.rows <= 0 || d.nkb <= 0) continue;
+          if (d.rows <= 0 || d.nkb <= 0) {
+            if (lane == 0 && claim) {
+              queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
+              claim = false;
+            }
+            continue;
+          }
         } else {
           d.nkb = -1;
         }
@@ -309,6 +317,10 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
               tma_load_3d(sa + C::kATiles * SK * kATileBytes, &tmap_a, full, 0, d.m0, kb, pol_a);
           }
           __syncwarp();
+        }
+        if (pw == 0 && lane == 0 && claim) {  // the next tile, now that this one is under way
+          queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
+          claim = false;
         }
         ++q;
         if (++stage == NST) { stage = 0; phase ^= 1u; }
