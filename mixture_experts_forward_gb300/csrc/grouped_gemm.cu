@@ -114,13 +114,26 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const in
   const int per_m = p.n_tiles * p.k_splits;
   const int mt = t / per_m;
   const int r = t - mt * per_m;
-  // expert: last e with tile_off[e] <= mt
-  int lo = 0, hi = p.E;  // invariant: tile_off[lo] <= mt < tile_off[hi]
-  while (hi - lo > 1) {
-    int mid = (lo + hi) >> 1;
-    if (s_tile_off[mid] <= mt) lo = mid; else hi = mid;
+  // expert: last e with tile_off[e] <= mt (tile_off[E] > mt).  The whole warp
+  // searches: each lane tests one entry of a stride-spaced sample, then one
+  // entry of the chosen stride (two ballots instead of log2(E) dependent
+  // loads); the caller's 32 lanes are converged.
+  const int lane = threadIdx.x & 31;
+  const int stride = (p.E + 32) / 32;  // ceil((E + 1) / 32)
+  int e;
+  if (stride <= 32) {
+    unsigned m = __ballot_sync(0xffffffffu, s_tile_off[min(p.E, lane * stride)] <= mt);
+    const int base = (31 - __clz(m)) * stride;
+    m = __ballot_sync(0xffffffffu, lane < stride && s_tile_off[min(p.E, base + lane)] <= mt);
+    e = base + 31 - __clz(m);
+  } else {
+    int lo = 0, hi = p.E;  // invariant: tile_off[lo] <= mt < tile_off[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_tile_off[mid] <= mt) lo = mid; else hi = mid;
+    }
+    e = lo;
   }
-  const int e = lo;
   const int seg_begin = s_off[e], seg_end = s_off[e + 1];
   d.e = e;
   d.m0 = seg_begin + (mt - s_tile_off[e]) * BM;
