@@ -21,12 +21,15 @@
 //               the warp owns the TMEM allocation
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (thread = weight row),
 //               FP8: per K block, acc += partial * (a_scale * w_scale) in fp32
-//               registers ("promotion"; each K block has its own TMEM buffer),
-//               then weighted red.global.add into the fp32 output, a plain
-//               store, or silu(gate)*up to bf16
+//               registers ("promotion"; each K block has its own TMEM buffer;
+//               packed f32x2 multiply-adds), then weighted red.global.add into
+//               the fp32 output, a plain store, or silu(gate)*up to bf16.
+//               FP8 tiles of 64+ routed rows add warps 8..11: two warps per
+//               TMEM lane quadrant, each promoting half of the tile's columns
 //   warp 6      tile metadata: routed-row tokens, route weights and the FP8
 //               scale products of each tile, staged into a shared ring ahead
-//               of the epilogue
+//               of the epilogue (loads issued in dependency order, about
+//               three memory round trips per tile)
 // Every wait is bounded (mbar_wait): on a time-out the CTA records
 // MOE_ERR_TIMEOUT in the workspace status word, raises a shared abort flag so
 // the other roles stop too, waits (bounded) for its own in-flight copies and
@@ -48,9 +51,12 @@ constexpr int kMaxStages = 16;
 // deeper stages.
 constexpr int kMaxRing = 4;
 __host__ __device__ constexpr int ring_slots(bool fp8, int bm) { return fp8 && bm >= 128 ? 2 : 4; }
-constexpr int kMaxThreads = 320;      // up to 10 warps
 constexpr int kMetaWarp = 6;
 constexpr int kFirstExtraProducer = 7;  // warps 7.. are the extra TMA producers
+// Warp roles: 0 producer + tile queue, 1 MMA, 2..5 epilogue (quadrant =
+// warp & 3), 6 metadata, 7 .. 7 + kProducers - 2 extra producers, and with a
+// second epilogue group the four warps after those (their warp & 3 again
+// covers the four quadrants, since the second group starts at warp 8).
 constexpr int kMaxE = 1024;
 
 struct TileDesc {
@@ -73,7 +79,14 @@ struct Cfg {
   // TMA producer warps (warp 0 plus warps 7..): two measured best (four were
   // no faster on any workload and slower on the BF16 FFN)
   static constexpr int kProducers = 2;
-  static constexpr int kThreads = 32 * (kFirstExtraProducer + kProducers - 1);
+  // FP8 with block_m >= 64: two epilogue warps per TMEM lane quadrant, each
+  // promoting half of the tile's columns (routed rows), so two warps on every
+  // scheduler share the per-K-block promotion; otherwise one per quadrant
+  static constexpr int kEpiGroups = kFP8 && BM >= 64 ? 2 : 1;
+  static constexpr int kEpiWarps = 4 * kEpiGroups;
+  static constexpr int kEpiCols = BM / kEpiGroups;  // columns promoted by one epilogue warp
+  static constexpr int kWarps = kFirstExtraProducer + kProducers - 1 + 4 * (kEpiGroups - 1);
+  static constexpr int kThreads = 32 * kWarps;
   // bytes of one K block of a stage; a stage holds p.sk K blocks laid out as
   // [kATiles][sk] weight tiles, then [sk] activation tiles
   static constexpr int kStageBytes = kATiles * kATileBytes + BM * kRowBytes;
@@ -181,11 +194,12 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
     }
     for (int i = 0; i < C::kNumAcc; ++i) {
       mbar_init(smem_u32(&bar_tfull[i]), 1);
-      mbar_init(smem_u32(&bar_tempty[i]), 4);
+      mbar_init(smem_u32(&bar_tempty[i]), C::kEpiWarps);
     }
     for (int i = 0; i < C::kRing; ++i) {
       mbar_init(smem_u32(&bar_dfull[i]), 1);
-      mbar_init(smem_u32(&bar_dempty[i]), 5 + C::kProducers - 1);  // MMA, 4 epilogue warps, extra producers
+      // MMA, the epilogue warps, the extra producers
+      mbar_init(smem_u32(&bar_dempty[i]), 1 + C::kEpiWarps + C::kProducers - 1);
       mbar_init(smem_u32(&bar_mfull[i]), 1);
     }
     mbar_init(smem_u32(&bar_drain), 1);
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
   const int total_tiles = work_items(p, s_tile_off);
   const uint64_t tmo = p.timeout_ns;
 
-  if (warp == 0 || warp >= kFirstExtraProducer) {
+  if (warp == 0 || (warp >= kFirstExtraProducer && warp < kFirstExtraProducer + C::kProducers - 1)) {
     // ------------------------------------------------------------ producers
     // A warp's bulk-tensor copy instructions are served one after another, at
     // a bounded rate of instructions rather than bytes.  So kProducers warps
@@ -437,22 +451,18 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
         float* sc = reinterpret_cast<float*>(s_meta + ds * meta_bytes);
         int* tok = reinterpret_cast<int*>(sc + (kFP8 ? p.kb_per_split * BM : 0));
         float* wt = reinterpret_cast<float*>(tok + BM);
-        if constexpr (kEpi == MOE_EPI_SCATTER) {
-          for (int s = lane; s < BM; s += 32) {
-            int tk = 0;
-            float w = 0.0f;
-            if (s < d.rows) {
-              const int r = __ldg(p.sorted_route_ids + d.m0 + s);
-              tk = r / p.top_k;
-              w = __ldg(p.route_weights + r);
-            }
-            tok[s] = tk;
-            wt[s] = w;
-          }
+        // Loads are issued in dependency order across the whole tile — every
+        // route id, then every scale, then every route weight (which needs its
+        // route id) — so a tile costs about three memory round trips.
+        constexpr int kRows = (BM + 31) / 32;  // rows of the tile per lane
+        int rid[kRows];
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+          const int s = lane + 32 * j;
+          rid[j] = (kEpi == MOE_EPI_SCATTER && s < d.rows) ? __ldg(p.sorted_route_ids + d.m0 + s) : -1;
         }
         if constexpr (kFP8) {
           // scale products for up to 16 K blocks at a time, all loads in flight together
-          constexpr int kRows = (BM + 31) / 32;  // rows of the tile per lane
           const float* wsc = p.w_scales + (static_cast<size_t>(d.e) * NB + d.n_tile) * p.KB + d.kb0;
           const float* asc = p.a_scales + static_cast<size_t>(d.kb0) * p.R + d.m0;
           for (int kb0 = 0; kb0 < d.nkb; kb0 += 16) {
@@ -479,6 +489,19 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
             }
           }
         }
+        if constexpr (kEpi == MOE_EPI_SCATTER) {
+          float w[kRows];
+#pragma unroll
+          for (int j = 0; j < kRows; ++j) w[j] = rid[j] >= 0 ? __ldg(p.route_weights + rid[j]) : 0.0f;
+#pragma unroll
+          for (int j = 0; j < kRows; ++j) {
+            const int s = lane + 32 * j;
+            if (s < BM) {
+              tok[s] = rid[j] >= 0 ? rid[j] / p.top_k : 0;
+              wt[s] = w[j];
+            }
+          }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_mfull[ds]));
@@ -487,9 +510,13 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    static_assert(C::kEpiGroups == 1 || kFirstExtraProducer + C::kProducers - 1 == 8,
+                  "the second epilogue group starts at warp 8");
     const int quad = warp & 3;                     // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;              // weight row within the tile
-    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    // first column (routed row) of this warp's share of the tile
+    const int c_lo = warp >= 8 ? C::kEpiCols : 0;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + c_lo;
     int ds = 0, acc_n = 0;
     uint32_t dphase = 0;
     bool ok = true;
@@ -507,15 +534,18 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
       const int col = d.n_tile * kTileN + row;
 
       if constexpr (kFP8) {
-        float acc[BM];
+        constexpr int CW = C::kEpiCols;
+        float acc[CW];
 #pragma unroll
-        for (int s = 0; s < BM; ++s) acc[s] = 0.0f;
+        for (int s = 0; s < CW; ++s) acc[s] = 0.0f;
         if constexpr (C::kKbGroup == 1 && BM >= 64) {
-          // One K block per TMEM buffer, read in 32-column chunks with two
-          // register buffers: the next chunk's load is in flight while this
-          // chunk is folded in, and the buffer is released as soon as its last
-          // chunk has arrived (before that chunk's multiply-adds).
-          constexpr int kCh = 32, kNCh = BM / kCh;
+          // One K block per TMEM buffer; this warp's columns are read in
+          // 32-column chunks with two register buffers: the next chunk's load
+          // is in flight while this chunk is folded in, and the buffer is
+          // released as soon as the last chunk has arrived (before that
+          // chunk's multiply-adds).  Two columns per packed multiply-add.
+          constexpr int kCh = 32, kNCh = CW / kCh;
+          static_assert(CW % kCh == 0, "chunks");
           for (int i = 0; i < d.nkb && ok; ++i) {
             const int a = acc_n;
             if (!__all_sync(0xffffffffu,
@@ -526,7 +556,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
             }
             tc_fence_after();
             const uint32_t base = lane_addr + (a % C::kNumAcc) * C::kAccCols;
-            const float4* scb = reinterpret_cast<const float4*>(sc + i * BM);
+            const float4* scb = reinterpret_cast<const float4*>(sc + i * BM + c_lo);
             float va[kCh], vb[kCh];
             tmem_ld16(base, *reinterpret_cast<float(*)[16]>(&va[0]));
             tmem_ld16(base + 16, *reinterpret_cast<float(*)[16]>(&va[16]));
@@ -548,10 +578,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
 #pragma unroll
               for (int j = 0; j < kCh; j += 4) {
                 const float4 f = scb[(ch * kCh + j) / 4];
-                acc[ch * kCh + j] = fmaf(cur[j], f.x, acc[ch * kCh + j]);
-                acc[ch * kCh + j + 1] = fmaf(cur[j + 1], f.y, acc[ch * kCh + j + 1]);
-                acc[ch * kCh + j + 2] = fmaf(cur[j + 2], f.z, acc[ch * kCh + j + 2]);
-                acc[ch * kCh + j + 3] = fmaf(cur[j + 3], f.w, acc[ch * kCh + j + 3]);
+                fma2(acc[ch * kCh + j], acc[ch * kCh + j + 1], cur[j], cur[j + 1], f.x, f.y);
+                fma2(acc[ch * kCh + j + 2], acc[ch * kCh + j + 3], cur[j + 2], cur[j + 3], f.z, f.w);
               }
               if (ch + 1 < kNCh) {
                 tmem_ld_wait(*reinterpret_cast<float(*)[16]>(nxt));
@@ -624,32 +652,32 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
           // the 8 row reductions back to back
           float* out = static_cast<float*>(p.out) + col;
 #pragma unroll
-          for (int s0 = 0; s0 < BM; s0 += 8) {
-            if (s0 < d.rows) {
-              const int4 t0 = *reinterpret_cast<const int4*>(tok + s0);
-              const int4 t1 = *reinterpret_cast<const int4*>(tok + s0 + 4);
-              const float4 w0 = *reinterpret_cast<const float4*>(wt + s0);
-              const float4 w1 = *reinterpret_cast<const float4*>(wt + s0 + 4);
+          for (int s0 = 0; s0 < CW; s0 += 8) {
+            if (c_lo + s0 < d.rows) {
+              const int4 t0 = *reinterpret_cast<const int4*>(tok + c_lo + s0);
+              const int4 t1 = *reinterpret_cast<const int4*>(tok + c_lo + s0 + 4);
+              const float4 w0 = *reinterpret_cast<const float4*>(wt + c_lo + s0);
+              const float4 w1 = *reinterpret_cast<const float4*>(wt + c_lo + s0 + 4);
               const int tk[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
               const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
               for (int j = 0; j < 8; ++j)
-                if (s0 + j < d.rows)
+                if (c_lo + s0 + j < d.rows)
                   red_add_f32(out + static_cast<size_t>(tk[j]) * p.N, ww[j] * acc[s0 + j]);
             }
           }
         } else if constexpr (kEpi == MOE_EPI_STORE_BF16) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
-          for (int s = 0; s < BM; ++s) {
-            if (s < d.rows)
-              out[static_cast<size_t>(d.m0 + s) * p.N + col] = __float2bfloat16_rn(acc[s]);
+          for (int s = 0; s < CW; ++s) {
+            if (c_lo + s < d.rows)
+              out[static_cast<size_t>(d.m0 + c_lo + s) * p.N + col] = __float2bfloat16_rn(acc[s]);
           }
         } else {
           float* out = static_cast<float*>(p.out);
 #pragma unroll
-          for (int s = 0; s < BM; ++s) {
-            if (s < d.rows) out[static_cast<size_t>(d.m0 + s) * p.N + col] = acc[s];
+          for (int s = 0; s < CW; ++s) {
+            if (c_lo + s < d.rows) out[static_cast<size_t>(d.m0 + c_lo + s) * p.N + col] = acc[s];
           }
         }
       } else {
