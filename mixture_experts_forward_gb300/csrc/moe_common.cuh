@@ -22,7 +22,8 @@ struct Ctrl {
   unsigned queue2;       // second GEMM of a forward (BF16 FFN down projection)
   unsigned done2;
   unsigned route_done;   // CTAs of the fused route+layout kernel that have finished routing
-  int pad[57];
+  unsigned scan_done;    // its column-scanning CTAs that have finished their experts
+  int pad[56];
 };
 static_assert(sizeof(Ctrl) == MOE_CTRL_BYTES, "control block size");
 

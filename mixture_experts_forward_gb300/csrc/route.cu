@@ -188,20 +188,29 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 // its expert e is the number of earlier tokens of the CTA that chose e: a
 // per-warp 0/1 row of a [32][E] shared table, prefix-summed over the warps.
 // The CTA publishes its per-expert totals (cta_hist[cta][E]) and the ranks
-// (local_rank[R]).  The CTA that arrives last (acq_rel counter) turns the
-// totals into per-CTA bases (cta_base[cta][E], exclusive over the CTAs, several
-// threads per expert), counts, offsets and tile offsets.  The quantise/gather
-// kernel then places route r of expert e at
+// (local_rank[R]), then takes an arrival number from an acq_rel counter.  The
+// last S = ceil(E / 32) CTAs to arrive scan the totals, each for its own
+// block of up to 32 experts: they wait (bounded) until every CTA has arrived —
+// the others have all finished or are still running, so the wait ends — and
+// turn their experts' columns into per-CTA bases (cta_base[cta][E], exclusive
+// over the CTAs) and counts.  The last of them to finish (a second counter)
+// scans the counts over the experts into offsets and tile offsets.  The
+// quantise/gather kernel then places route r of expert e at
 // offsets[e] + cta_base[cta(r)][e] + local_rank[r] — the stable layout by
 // route id.
+// Bound on the scanning CTAs' wait for the other CTAs' totals.
+constexpr uint64_t kScanWaitNs = 2000000000ull;
+
+// Two CTAs per SM where E is small (the router keeps few registers);
+// 32-token groups with many experts keep one CTA per SM and 64 registers.
 template <int NPL>
-__global__ void __launch_bounds__(kLayoutThreads, NPL <= 8 ? 2 : 1)
+__global__ void __launch_bounds__(kLayoutThreads, NPL <= 4 ? 2 : 1)
     route_rank_kernel(const float* __restrict__ logits, int M, int E, int k, float softcap,
                       int renorm, int32_t* ids, float* __restrict__ weights, int block_m,
                       int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                       int32_t* __restrict__ tile_offsets, Ctrl* ctrl, int32_t* local_rank,
-                      int32_t* cta_hist, int32_t* __restrict__ cta_base, int hist_chunk) {
-  extern __shared__ int s_tab[];  // [32][E]; the last CTA: [hist_chunk][E + 4] + [E]
+                      int32_t* cta_hist, int32_t* __restrict__ cta_base) {
+  extern __shared__ int s_tab[];  // [32][E] ranking table (at least 1024 ints: the scanners' [32][32] sums)
   __shared__ int s_last;
   __shared__ int s_wa[32], s_wb[32];
   pdl_wait();
@@ -237,117 +246,81 @@ __global__ void __launch_bounds__(kLayoutThreads, NPL <= 8 ? 2 : 1)
                  : "=r"(prev)
                  : "l"(&ctrl->route_done)
                  : "memory");
-    s_last = prev == gridDim.x - 1;
+    s_last = static_cast<int>(prev);  // arrival number
+  }
+  __syncthreads();
+  const int nC = gridDim.x;
+  const int S = min(nC, (E + 31) / 32);  // column-scanning CTAs
+  const int scan = s_last - (nC - S);    // this CTA's scanner index, or < 0
+  if (scan < 0) return;
+
+  // ---- scanners: wait until every CTA has published its totals
+  if (tid == 0) {
+    const uint64_t t0 = global_timer_ns();
+    int ok = 1;
+    for (;;) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&ctrl->route_done) : "memory");
+      if (v >= static_cast<unsigned>(nC)) break;
+      if (global_timer_ns() - t0 > kScanWaitNs) { ok = 0; break; }
+      __nanosleep(64);
+    }
+    if (!ok) set_error(ctrl, MOE_ERR_TIMEOUT, 6);
+    s_wa[0] = ok;
+  }
+  __syncthreads();
+  if (!s_wa[0]) return;
+
+  // Experts [e0, e1) of this scanner, 32 at a time: lane = expert, warp w
+  // takes a contiguous run of CTAs (rows) and sums it; the exclusive prefix
+  // of the run sums over the warps gives each run's start; a second pass over
+  // the run writes the bases.  Row loads are 128-byte coalesced.
+  const int per = (E + S - 1) / S;
+  const int e0 = scan * per, e1 = min(E, e0 + per);
+  const int L = (nC + 31) / 32;  // rows per warp
+  const int r0 = min(nC, w * L), r1 = min(nC, r0 + L);
+  int* s_sum = s_tab;            // [32 warps][32 lanes]
+  for (int eb = e0; eb < e1; eb += 32) {
+    const int e = eb + lane;
+    const bool act = e < e1;
+    int part = 0;
+    if (act)
+      for (int r = r0; r < r1; ++r) part += __ldcg(cta_hist + static_cast<size_t>(r) * E + e);
+    s_sum[w * 32 + lane] = part;
+    __syncthreads();
+    int run = 0;
+    for (int ww = 0; ww < w; ++ww) run += s_sum[ww * 32 + lane];
+    if (act) {
+      for (int r = r0; r < r1; ++r) {
+        const int v = __ldcg(cta_hist + static_cast<size_t>(r) * E + e);
+        cta_base[static_cast<size_t>(r) * E + e] = run;
+        run += v;
+      }
+      if (w == 31) counts[e] = run;  // warp 31 holds the column total
+    }
+    __syncthreads();
+  }
+
+  // ---- the last scanner: offsets and tile offsets over all experts
+  __syncthreads();
+  if (tid == 0) {
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev)
+                 : "l"(&ctrl->scan_done)
+                 : "memory");
+    s_last = prev == static_cast<unsigned>(S - 1);
   }
   __syncthreads();
   if (!s_last) return;
-
-  // ---- last CTA: per-CTA bases, counts, offsets, tile offsets
-  // The [nC][E] histograms are staged in shared memory a chunk of `hist_chunk`
-  // CTAs at a time (asynchronous 16-byte copies, all in flight; rows padded to
-  // E + 4 ints), each expert's column is scanned there by G lanes, and the
-  // exclusive bases overwrite the chunk in place and go out as 16-byte stores.
-  const int nC = gridDim.x;
-  const int RS = E + 4;  // staged row stride (ints)
-  int G = 1;             // lanes per expert: a power of two, G * E <= 1024, G <= 32
-  while (G * 2 * E <= kLayoutThreads && G * 2 <= 32) G *= 2;
-  int* s_h = s_tab;                      // [hist_chunk][RS]
-  int* s_cnt = s_tab + hist_chunk * RS;  // [E] running totals
-  for (int i = tid; i < E; i += kLayoutThreads) s_cnt[i] = 0;
-  const int e = tid / G, g = tid % G;
-  const bool act = e < E;
-  const bool vec = (E & 3) == 0;
-  for (int cc = 0; cc < nC; cc += hist_chunk) {
-    const int nc = min(hist_chunk, nC - cc);
-    const int32_t* src = cta_hist + static_cast<size_t>(cc) * E;
-    int32_t* dst = cta_base + static_cast<size_t>(cc) * E;
-    // asynchronous copies (no registers held), all in flight, then one wait
-    if (vec) {
-      const int q = E >> 2;
-      for (int i = tid; i < nc * q; i += kLayoutThreads) {
-        const int r = i / q, c4 = i - r * q;
-        cp_async16(smem_u32(s_h + r * RS + 4 * c4), src + static_cast<size_t>(r) * E + 4 * c4);
-      }
-    } else {
-      for (int i = tid; i < nc * E; i += kLayoutThreads) {
-        const int r = i / E, c = i - r * E;
-        cp_async4(smem_u32(s_h + r * RS + c), src + i);
-      }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    // Each of an expert's G lanes takes a contiguous run of L CTAs (L odd,
-    // so the lanes' rows fall in different banks): it sums its run (loads
-    // 8 at a time), a segmented shuffle scan over the G lanes gives the run's
-    // start, and a second pass writes the exclusive bases.  Every lane takes
-    // part in the shuffles (G divides 32, so an expert's lanes never straddle
-    // two warps); lanes past the last expert have empty runs.
-    {
-      const int L = ((nc + G - 1) / G) | 1;
-      const int c0 = min(nc, g * L), c1 = act ? min(nc, c0 + L) : c0;
-      int part = 0;
-      int c = c0;
-      for (; c + 8 <= c1; c += 8) {
-        int v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = s_h[(c + u) * RS + e];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) part += v[u];
-      }
-      for (; c < c1; ++c) part += s_h[c * RS + e];
-      int inc = part;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        if (off >= G) break;
-        const int y = __shfl_up_sync(0xffffffffu, inc, off, G);
-        if (g >= off) inc += y;
-      }
-      const int total = __shfl_sync(0xffffffffu, inc, G - 1, G);
-      int run = (act ? s_cnt[e] : 0) + inc - part;
-      c = c0;
-      for (; c + 8 <= c1; c += 8) {
-        int v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = s_h[(c + u) * RS + e];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          s_h[(c + u) * RS + e] = run;
-          run += v[u];
-        }
-      }
-      for (; c < c1; ++c) {
-        const int v = s_h[c * RS + e];
-        s_h[c * RS + e] = run;
-        run += v;
-      }
-      __syncwarp();
-      if (act && g == G - 1) s_cnt[e] += total;
-    }
-    __syncthreads();
-    if (vec) {
-      const int q = E >> 2;
-      for (int i = tid; i < nc * q; i += kLayoutThreads) {
-        const int r = i / q, c4 = i - r * q;
-        reinterpret_cast<int4*>(dst + static_cast<size_t>(r) * E)[c4] =
-            reinterpret_cast<const int4*>(s_h + r * RS)[c4];
-      }
-    } else {
-      for (int i = tid; i < nc * E; i += kLayoutThreads) {
-        const int r = i / E, c = i - r * E;
-        dst[i] = s_h[r * RS + c];
-      }
-    }
-    __syncthreads();
-  }
   int cnt = 0, ntile = 0;
   if (tid < E) {
-    cnt = s_cnt[tid];
+    cnt = __ldcg(counts + tid);
     ntile = (cnt + block_m - 1) / block_m;
   }
   int inc_c = cnt, inc_t = ntile;
   block_scan2(inc_c, inc_t, s_wa, s_wb);
   if (tid < E) {
-    counts[tid] = cnt;
     offsets[tid] = inc_c - cnt;
     tile_offsets[tid] = inc_t - ntile;
     if (tid == E - 1) {
@@ -361,6 +334,7 @@ __global__ void __launch_bounds__(kLayoutThreads, NPL <= 8 ? 2 : 1)
     ctrl->queue2 = 0;
     ctrl->done2 = 0;
     ctrl->route_done = 0u;
+    ctrl->scan_done = 0u;
   }
 }
 
@@ -401,21 +375,9 @@ cudaError_t launch_route_rank_t(const float* logits, int M, int E, int k, float 
                                 int32_t* counts, int32_t* offsets, int32_t* tile_offsets,
                                 Ctrl* ctrl, int32_t* local_rank, int32_t* cta_hist,
                                 int32_t* cta_base, cudaStream_t stream, bool pdl) {
-  // [32][E] ranking table; the last CTA reuses it for a chunk of the per-CTA
-  // histograms ([hist_chunk][E + 4]) and the [E] running totals
+  // [32][E] ranking table; the scanning CTAs reuse it for [32][32] run sums
   const int n_ctas = (M + 31) / 32;
-  // staging budget: up to 200 KB when the grid fits one CTA per SM anyway,
-  // else 96 KB so that two CTAs still fit on an SM
-  int sms = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 0;
-  const int budget = (sms > 0 && n_ctas <= sms) ? 51200 : 24576;  // ints
-  int hist_chunk = (budget - E) / (E + 4);
-  if (hist_chunk > n_ctas) hist_chunk = n_ctas;
-  if (hist_chunk < 1) hist_chunk = 1;
-  const int staged = hist_chunk * (E + 4) + E;
-  const int ints = 32 * E > staged ? 32 * E : staged;
+  const int ints = 32 * E > 1024 ? 32 * E : 1024;
   const size_t smem = static_cast<size_t>(ints) * sizeof(int);
   cudaError_t err = cudaFuncSetAttribute(route_rank_kernel<NPL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -434,7 +396,7 @@ cudaError_t launch_route_rank_t(const float* logits, int M, int E, int k, float 
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, route_rank_kernel<NPL>, logits, M, E, k, softcap, renorm, ids,
                             weights, block_m, counts, offsets, tile_offsets, ctrl, local_rank,
-                            cta_hist, cta_base, hist_chunk);
+                            cta_hist, cta_base);
 }
 
 cudaError_t launch_route_rank(const float* logits, int M, int E, int k, float softcap, int renorm,
