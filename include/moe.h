@@ -141,6 +141,14 @@ typedef struct {
   void* out;                  /* see moe_epilogue_t */
   int k_splits;               /* FP8 SCATTER: K split into this many tiles (0 = auto) */
   int num_ctas;               /* persistent CTAs (0 = one per SM) */
+  int gather_rows;            /* 0: `a` holds the expert-compact rows [R, K] (FP8 a_scales
+                                 [K/128, R]).  1: `a` is token-major [M, K] and the kernel
+                                 gathers compact slot s from row sorted_route_ids[s] / top_k
+                                 (FP8 a_scales token-major [K/128, M]); sorted_route_ids, M
+                                 and top_k are then required for every epilogue, and an
+                                 empty slot (id < 0) reads row 0 (its result is dropped).
+                                 Built for FP8 (every epilogue) and the BF16 SWIGLU
+                                 epilogue; other BF16 epilogues: MOE_ERR_UNSUPPORTED */
 } moe_gemm_args;
 
 /* Grouped GEMM — "Fused MoE FP8" section "Baseline: 7 kernels" item 6, with
@@ -185,6 +193,13 @@ typedef struct {
   int k_splits;           /* FP8: 0 = auto */
   int use_graph;          /* 1: capture the launch sequence once per argument set and
                              replay it as a CUDA graph; 0: plain launches */
+  int gather_rows;        /* large batches (more than 4096 routes, or BF16): 1 = the
+                             first grouped GEMM gathers each routed row from the
+                             token-major activations (moe_gemm_args.gather_rows) instead
+                             of reading an expert-compact copy; the workspace then holds
+                             no [R, K] copy (FP8 keeps one token-major [M, K] code matrix).
+                             0 (default) = write the compact copy, which is faster on
+                             GB300 at the benchmark shapes; same results either way */
 } moe_forward_args;
 
 /* Workspace bytes needed by moe_forward / moe_forward_host for these

@@ -43,7 +43,8 @@ class GemmArgs(ctypes.Structure):
                 ("w", ctypes.c_void_p), ("w_scales", ctypes.c_void_p),
                 ("offsets", ctypes.c_void_p), ("tile_offsets", ctypes.c_void_p),
                 ("sorted_route_ids", ctypes.c_void_p), ("route_weights", ctypes.c_void_p),
-                ("out", ctypes.c_void_p), ("k_splits", ctypes.c_int), ("num_ctas", ctypes.c_int)]
+                ("out", ctypes.c_void_p), ("k_splits", ctypes.c_int), ("num_ctas", ctypes.c_int),
+                ("gather_rows", ctypes.c_int)]
 
 
 class ForwardArgs(ctypes.Structure):
@@ -53,7 +54,7 @@ class ForwardArgs(ctypes.Structure):
                 ("logits", ctypes.c_void_p), ("x", ctypes.c_void_p), ("w", ctypes.c_void_p),
                 ("w_scales", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("block_m", ctypes.c_int), ("sched", ctypes.c_int), ("k_splits", ctypes.c_int),
-                ("use_graph", ctypes.c_int)]
+                ("use_graph", ctypes.c_int), ("gather_rows", ctypes.c_int)]
 
 
 _lib = None
@@ -158,16 +159,21 @@ def quant_gather(x: torch.Tensor, k: int, route_slot: torch.Tensor, zero_acc=Non
 
 def grouped_gemm(*, dtype, epilogue, a, w, offsets, tile_offsets, out, ws, block_m,
                  a_scales=None, w_scales=None, sorted_route_ids=None, route_weights=None,
-                 M=0, top_k=0, sched=SCHED_QUEUE, k_splits=0, num_ctas=0, stream=None):
+                 M=0, top_k=0, sched=SCHED_QUEUE, k_splits=0, num_ctas=0, gather_rows=0,
+                 stream=None):
+    """moe_grouped_gemm.  gather_rows=1: `a` (and FP8 a_scales) are token-major
+    and compact slot s reads row sorted_route_ids[s] // top_k."""
     E, N, K = w.shape
+    R = sorted_route_ids.numel() if gather_rows else a.shape[0]
     g = GemmArgs(dtype=dtype, epilogue=epilogue, sched=sched, block_m=block_m, E=E, N=N, K=K,
-                 R=a.shape[0], M=M, top_k=top_k, a=a.data_ptr(),
+                 R=R, M=M, top_k=top_k, a=a.data_ptr(),
                  a_scales=None if a_scales is None else a_scales.data_ptr(), w=w.data_ptr(),
                  w_scales=None if w_scales is None else w_scales.data_ptr(),
                  offsets=offsets.data_ptr(), tile_offsets=tile_offsets.data_ptr(),
                  sorted_route_ids=None if sorted_route_ids is None else sorted_route_ids.data_ptr(),
                  route_weights=None if route_weights is None else route_weights.data_ptr(),
-                 out=out.data_ptr(), k_splits=k_splits, num_ctas=num_ctas)
+                 out=out.data_ptr(), k_splits=k_splits, num_ctas=num_ctas,
+                 gather_rows=gather_rows)
     _check(lib().moe_grouped_gemm(ctypes.byref(g), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_grouped_gemm")
     return out
@@ -204,14 +210,14 @@ def scatter(rows: torch.Tensor, route_slot: torch.Tensor, weights: torch.Tensor,
 # ------------------------------------------------------------------ forward
 def forward_args(*, dtype, M, K, N, E, top_k, softcap=0.0, renorm=1, logits=None, x=None, w=None,
                  w_scales=None, w2=None, block_m=0, sched=SCHED_QUEUE, k_splits=0,
-                 use_graph=1) -> ForwardArgs:
+                 use_graph=1, gather_rows=0) -> ForwardArgs:
     return ForwardArgs(dtype=dtype, M=M, K=K, N=N, E=E, top_k=top_k, softcap=float(softcap),
                        renorm=int(renorm), logits=None if logits is None else logits.data_ptr(),
                        x=None if x is None else x.data_ptr(),
                        w=None if w is None else w.data_ptr(),
                        w_scales=None if w_scales is None else w_scales.data_ptr(),
                        w2=None if w2 is None else w2.data_ptr(), block_m=block_m, sched=sched,
-                       k_splits=k_splits, use_graph=use_graph)
+                       k_splits=k_splits, use_graph=use_graph, gather_rows=gather_rows)
 
 
 def workspace_size(args: ForwardArgs) -> int:

@@ -161,7 +161,82 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const in
   }
 }
 
-template <int BM, bool kFP8, int kEpi>
+// One tile's metadata, filled by the 32 lanes of the metadata warp: FP8
+// scale products sc[kb][row] = a_scale * w_scale, and for the scatter the
+// row's token tok[row] and route weight wt[row].  Loads are issued in
+// dependency order across the whole tile — every route id, then every scale,
+// then every route weight (which needs its route id) — so a tile costs about
+// three memory round trips.  kGather: the route ids come from the tile's
+// ring slot (rr) and the activation scales are token-major ([KB, M]);
+// otherwise the ids are loaded from sorted_route_ids and the scales are
+// compact ([KB, R]), their addresses independent of the ids.
+template <int BM, bool kFP8, int kEpi, bool kGather>
+__device__ __forceinline__ void meta_fill(const GemmParams& p, const TileDesc& d, int lane,
+                                          const int* rr, float* sc, int* tok, float* wt) {
+  constexpr int kRows = (BM + 31) / 32;  // rows of the tile per lane
+  const int NB = p.N / kTileN;
+  int rid[kRows];
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
+    const int s = lane + 32 * j;
+    if constexpr (kGather)
+      rid[j] = s < BM ? rr[s] : -1;
+    else
+      rid[j] = (kEpi == MOE_EPI_SCATTER && s < d.rows) ? __ldg(p.sorted_route_ids + d.m0 + s) : -1;
+  }
+  if constexpr (kFP8) {
+    // scale products for up to 16 K blocks at a time, all loads in flight together
+    const float* wsc = p.w_scales + (static_cast<size_t>(d.e) * NB + d.n_tile) * p.KB + d.kb0;
+    const size_t a_ld = kGather ? static_cast<size_t>(p.M) : static_cast<size_t>(p.R);
+    const float* asc = p.a_scales + static_cast<size_t>(d.kb0) * a_ld + (kGather ? 0 : d.m0);
+    int arow[kRows];  // column of each row in the scale matrix
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      if constexpr (kGather)
+        arow[j] = rid[j] >= 0 ? rid[j] / p.top_k : -1;
+      else
+        arow[j] = lane + 32 * j;
+    }
+    for (int kb0 = 0; kb0 < d.nkb; kb0 += 16) {
+      float va[16][kRows];
+      float vb[16];
+#pragma unroll
+      for (int kb = 0; kb < 16; ++kb) {
+        vb[kb] = kb0 + kb < d.nkb ? __ldg(wsc + kb0 + kb) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+          const int s = lane + 32 * j;
+          va[kb][j] = (kb0 + kb < d.nkb && s < d.rows && arow[j] >= 0)
+                          ? __ldg(asc + static_cast<size_t>(kb0 + kb) * a_ld + arow[j])
+                          : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int kb = 0; kb < 16; ++kb) {
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+          const int s = lane + 32 * j;
+          if (kb0 + kb < d.nkb && s < BM) sc[(kb0 + kb) * BM + s] = va[kb][j] * vb[kb];
+        }
+      }
+    }
+  }
+  if constexpr (kEpi == MOE_EPI_SCATTER) {
+    float w[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) w[j] = rid[j] >= 0 ? __ldg(p.route_weights + rid[j]) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      const int s = lane + 32 * j;
+      if (s < BM) {
+        tok[s] = rid[j] >= 0 ? rid[j] / p.top_k : 0;
+        wt[s] = w[j];
+      }
+    }
+  }
+}
+
+template <int BM, bool kFP8, int kEpi, bool kGather>
 __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_a, const GemmParams p) {
@@ -186,6 +261,9 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
   // tile offsets and row offsets of the experts ([E + 1] each) after the ring
   int* s_tile_off = reinterpret_cast<int*>(s_meta + C::kRing * meta_bytes);
   int* s_off = s_tile_off + (p.E + 1);
+  // gathered-rows mode: route id of every routed row of each ring slot's tile
+  // ([kRing][BM], -1 past the tile's rows), after the tables
+  int* s_rows = s_tile_off + ((2 * (p.E + 1) + 3) & ~3);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -268,58 +346,88 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
     // that tile's loads instead of delaying them
     int queued = p.sched == MOE_SCHED_QUEUE ? c : -1;
     bool claim = false;             // lane 0 of warp 0: the next tile is still to be claimed
+    // Gathered rows: warp 0 loads each tile's route ids (kRpl per lane) and
+    // puts them in the tile's ring slot with its descriptor.  The queue's next
+    // tile is decoded and its ids loaded halfway through the current tile
+    // ("pre"), so the loads' round trip overlaps the current tile's copies.
+    constexpr int kRpl = (BM + 31) / 32;
+    int nr[kRpl];
+    TileDesc dn;
+    bool pre = false;
     for (;;) {
       TileDesc d;
       bool got = true;
       if (pw == 0) {
-        int t = -1;
-        if (lane == 0) {
-          if (p.sched == MOE_SCHED_QUEUE) {
-            t = queued < total_tiles ? queued : -1;
-            claim = t >= 0;
-          } else {
-            while (st_e < p.E) {
-              const int per_e = (s_tile_off[st_e + 1] - s_tile_off[st_e]) * p.n_tiles * p.k_splits;
-              if (st_lt < per_e) {
-                t = s_tile_off[st_e] * p.n_tiles * p.k_splits + st_lt;
-                st_lt += st_stride;
-                break;
-              }
-              if (G >= p.E) { st_e = p.E; break; }
-              st_e += G;
-              st_lt = 0;
-            }
-          }
-        }
-        t = __shfl_sync(0xffffffffu, t, 0);
-        if (t >= 0) {
-          decode_tile(t, p, s_tile_off, s_off, BM, d);
-          if (d.rows <= 0 || d.nkb <= 0) {
-            if (lane == 0 && claim) {
-              queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
-              claim = false;
-            }
-            continue;
-          }
+        if (pre) {
+          d = dn;
+          pre = false;
+          if (lane == 0) claim = true;
         } else {
-          d.nkb = -1;
-        }
-        if (lane == 0) {
-          got = mbar_wait(smem_u32(&bar_dempty[ds]), dphase ^ 1u, &s_abort, tmo);
-          if (got) {
-            s_desc[ds] = d;
-            mbar_arrive(smem_u32(&bar_dfull[ds]));
+          int t = -1;
+          if (lane == 0) {
+            if (p.sched == MOE_SCHED_QUEUE) {
+              t = queued < total_tiles ? queued : -1;
+              claim = t >= 0;
+            } else {
+              while (st_e < p.E) {
+                const int per_e = (s_tile_off[st_e + 1] - s_tile_off[st_e]) * p.n_tiles * p.k_splits;
+                if (st_lt < per_e) {
+                  t = s_tile_off[st_e] * p.n_tiles * p.k_splits + st_lt;
+                  st_lt += st_stride;
+                  break;
+                }
+                if (G >= p.E) { st_e = p.E; break; }
+                st_e += G;
+                st_lt = 0;
+              }
+            }
+          }
+          t = __shfl_sync(0xffffffffu, t, 0);
+          if (t >= 0) {
+            decode_tile(t, p, s_tile_off, s_off, BM, d);
+            if (d.rows <= 0 || d.nkb <= 0) {
+              if (lane == 0 && claim) {
+                queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
+                claim = false;
+              }
+              continue;
+            }
+            if constexpr (kGather) {
+#pragma unroll
+              for (int j = 0; j < kRpl; ++j) {
+                const int s = lane + 32 * j;
+                nr[j] = s < d.rows ? __ldg(p.sorted_route_ids + d.m0 + s) : -1;
+              }
+            }
+          } else {
+            d.nkb = -1;
           }
         }
+        if (lane == 0) got = mbar_wait(smem_u32(&bar_dempty[ds]), dphase ^ 1u, &s_abort, tmo);
         if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+        if (kGather && d.nkb >= 0) {
+#pragma unroll
+          for (int j = 0; j < kRpl; ++j) {
+            const int s = lane + 32 * j;
+            if (s < BM) s_rows[ds * BM + s] = nr[j];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          s_desc[ds] = d;
+          mbar_arrive(smem_u32(&bar_dfull[ds]));
+        }
       } else {
         if (lane == 0) got = mbar_wait(smem_u32(&bar_dfull[ds]), dphase, &s_abort, tmo);
         if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
         __syncwarp();
         d = s_desc[ds];
         __syncwarp();
+        // (the slot's route ids stay valid until the epilogue has finished
+        // this tile, long after its last copy is issued)
         if (lane == 0) mbar_arrive(smem_u32(&bar_dempty[ds]));
       }
+      const int* rr = s_rows + ds * BM;   // this tile's route ids (gathered rows)
       if (++ds == C::kRing) { ds = 0; dphase ^= 1u; }
       if (d.nkb < 0) break;
       const int w_row = d.e * p.N + d.n_tile * kTileN;
@@ -337,17 +445,57 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
             // box spans SK K blocks (a box running past K reads the fill value)
             const uint32_t sa = smem_base + stage * stage_bytes;
             const int kb = d.kb0 + i;
-            if (lane < C::kATiles)
-              tma_load_3d(sa + lane * SK * kATileBytes, &tmap_w, full, 0, w_row + lane * (p.N / 2),
-                          kb, pol_w);
-            else if (lane == C::kATiles)
-              tma_load_3d(sa + C::kATiles * SK * kATileBytes, &tmap_a, full, 0, d.m0, kb, pol_a);
+            if constexpr (!kGather) {
+              // one if / else-if chain: the boxes go out from their lanes as one instruction
+              if (lane < C::kATiles)
+                tma_load_3d(sa + lane * SK * kATileBytes, &tmap_w, full, 0, w_row + lane * (p.N / 2),
+                            kb, pol_w);
+              else if (lane == C::kATiles)
+                tma_load_3d(sa + C::kATiles * SK * kATileBytes, &tmap_a, full, 0, d.m0, kb, pol_a);
+            } else {
+              if (lane < C::kATiles)
+                tma_load_3d(sa + lane * SK * kATileBytes, &tmap_w, full, 0, w_row + lane * (p.N / 2),
+                            kb, pol_w);
+              // the routed rows, four per copy (SK * BM / 4 copies over the
+              // warp's lanes); a K block past the tile's end reloads its last
+              // one, which the MMA does not read; an empty row reads token 0
+              const int nk = min(SK, d.nkb - i);
+              constexpr int kG = BM / 4;
+              for (int g = lane; g < SK * kG; g += 32) {
+                const int kbl = g / kG, g4 = g - kbl * kG;
+                const int4 r4 = *reinterpret_cast<const int4*>(rr + 4 * g4);
+                const int kc = (kb + min(kbl, nk - 1)) * (kFP8 ? 128 : 64);
+                tma_gather4(sa + C::kATiles * SK * kATileBytes + kbl * (BM * kRowBytes) + g4 * 512,
+                            &tmap_a, full, kc, max(r4.x, 0) / p.top_k, max(r4.y, 0) / p.top_k,
+                            max(r4.z, 0) / p.top_k, max(r4.w, 0) / p.top_k);
+              }
+            }
           }
           __syncwarp();
         }
         if (pw == 0 && lane == 0 && claim) {  // the next tile, now that this one is under way
           queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
           claim = false;
+        }
+        if (kGather && pw == 0 && i > 0 && i == ((d.nkb / SK) / 2) * SK &&
+            p.sched == MOE_SCHED_QUEUE) {
+          // halfway through the tile the claim has returned: decode the claimed
+          // tile and start its id loads (reading the claim any earlier would
+          // stall this warp on the atomic's round trip)
+          const int nt = __shfl_sync(0xffffffffu, queued, 0);
+          if (nt < total_tiles) {
+            decode_tile(nt, p, s_tile_off, s_off, BM, dn);
+            if (dn.rows > 0 && dn.nkb > 0) {
+              {
+#pragma unroll
+                for (int j = 0; j < kRpl; ++j) {
+                  const int s = lane + 32 * j;
+                  nr[j] = s < dn.rows ? __ldg(p.sorted_route_ids + dn.m0 + s) : -1;
+                }
+              }
+              pre = true;
+            }
+          }
         }
         ++q;
         if (++stage == NST) { stage = 0; phase ^= 1u; }
@@ -439,7 +587,6 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
     // ------------------------------------------------------------ tile metadata
     int ds = 0;
     uint32_t dphase = 0;
-    const int NB = p.N / kTileN;
     for (;;) {
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_dfull[ds]), dphase, &s_abort, tmo))) {
         set_error(p.ctrl, MOE_ERR_TIMEOUT, 4);
@@ -451,57 +598,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
         float* sc = reinterpret_cast<float*>(s_meta + ds * meta_bytes);
         int* tok = reinterpret_cast<int*>(sc + (kFP8 ? p.kb_per_split * BM : 0));
         float* wt = reinterpret_cast<float*>(tok + BM);
-        // Loads are issued in dependency order across the whole tile — every
-        // route id, then every scale, then every route weight (which needs its
-        // route id) — so a tile costs about three memory round trips.
-        constexpr int kRows = (BM + 31) / 32;  // rows of the tile per lane
-        int rid[kRows];
-#pragma unroll
-        for (int j = 0; j < kRows; ++j) {
-          const int s = lane + 32 * j;
-          rid[j] = (kEpi == MOE_EPI_SCATTER && s < d.rows) ? __ldg(p.sorted_route_ids + d.m0 + s) : -1;
-        }
-        if constexpr (kFP8) {
-          // scale products for up to 16 K blocks at a time, all loads in flight together
-          const float* wsc = p.w_scales + (static_cast<size_t>(d.e) * NB + d.n_tile) * p.KB + d.kb0;
-          const float* asc = p.a_scales + static_cast<size_t>(d.kb0) * p.R + d.m0;
-          for (int kb0 = 0; kb0 < d.nkb; kb0 += 16) {
-            float va[16][kRows];
-            float vb[16];
-#pragma unroll
-            for (int kb = 0; kb < 16; ++kb) {
-              vb[kb] = kb0 + kb < d.nkb ? __ldg(wsc + kb0 + kb) : 0.0f;
-#pragma unroll
-              for (int j = 0; j < kRows; ++j) {
-                const int s = lane + 32 * j;
-                va[kb][j] = (kb0 + kb < d.nkb && s < d.rows)
-                                ? __ldg(asc + static_cast<size_t>(kb0 + kb) * p.R + s)
-                                : 0.0f;
-              }
-            }
-#pragma unroll
-            for (int kb = 0; kb < 16; ++kb) {
-#pragma unroll
-              for (int j = 0; j < kRows; ++j) {
-                const int s = lane + 32 * j;
-                if (kb0 + kb < d.nkb && s < BM) sc[(kb0 + kb) * BM + s] = va[kb][j] * vb[kb];
-              }
-            }
-          }
-        }
-        if constexpr (kEpi == MOE_EPI_SCATTER) {
-          float w[kRows];
-#pragma unroll
-          for (int j = 0; j < kRows; ++j) w[j] = rid[j] >= 0 ? __ldg(p.route_weights + rid[j]) : 0.0f;
-#pragma unroll
-          for (int j = 0; j < kRows; ++j) {
-            const int s = lane + 32 * j;
-            if (s < BM) {
-              tok[s] = rid[j] >= 0 ? rid[j] / p.top_k : 0;
-              wt[s] = w[j];
-            }
-          }
-        }
+        meta_fill<BM, kFP8, kEpi, kGather>(p, d, lane, s_rows + ds * BM, sc, tok, wt);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_mfull[ds]));
@@ -772,49 +869,64 @@ struct GemmVariant {
   int threads;
 };
 
-template <int BM, bool kFP8, int kEpi>
+template <int BM, bool kFP8, int kEpi, bool kGather>
 GemmVariant variant() {
   using C = Cfg<BM, kFP8, kEpi>;
-  return GemmVariant{reinterpret_cast<const void*>(&grouped_gemm_kernel<BM, kFP8, kEpi>),
+  return GemmVariant{reinterpret_cast<const void*>(&grouped_gemm_kernel<BM, kFP8, kEpi, kGather>),
                      C::kStageBytes, C::kThreads};
 }
 
-template <bool kFP8, int kEpi>
+template <bool kFP8, int kEpi, bool kGather>
 bool pick_bm(int bm, GemmVariant& v) {
   switch (bm) {
-    case 16: v = variant<16, kFP8, kEpi>(); return true;
-    case 32: v = variant<32, kFP8, kEpi>(); return true;
-    case 64: v = variant<64, kFP8, kEpi>(); return true;
-    case 128: v = variant<128, kFP8, kEpi>(); return true;
+    case 16: v = variant<16, kFP8, kEpi, kGather>(); return true;
+    case 32: v = variant<32, kFP8, kEpi, kGather>(); return true;
+    case 64: v = variant<64, kFP8, kEpi, kGather>(); return true;
+    case 128: v = variant<128, kFP8, kEpi, kGather>(); return true;
     default: break;
   }
   if constexpr (!kFP8) {
-    if (bm == 256) { v = variant<256, kFP8, kEpi>(); return true; }
+    if (bm == 256) { v = variant<256, kFP8, kEpi, kGather>(); return true; }
   }
   return false;
 }
 
-bool select_gemm_variant(bool fp8, int epi, int bm, GemmVariant& v) {
+// Gathered rows are built for the FP8 GEMM (every epilogue) and the BF16
+// gated up projection (the first GEMM of the BF16 forward).
+bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, GemmVariant& v) {
   if (fp8) {
-    if (epi == MOE_EPI_SCATTER) return pick_bm<true, MOE_EPI_SCATTER>(bm, v);
-    if (epi == MOE_EPI_STORE) return pick_bm<true, MOE_EPI_STORE>(bm, v);
-    if (epi == MOE_EPI_STORE_BF16) return pick_bm<true, MOE_EPI_STORE_BF16>(bm, v);
+    if (epi == MOE_EPI_SCATTER)
+      return gather ? pick_bm<true, MOE_EPI_SCATTER, true>(bm, v)
+                    : pick_bm<true, MOE_EPI_SCATTER, false>(bm, v);
+    if (epi == MOE_EPI_STORE)
+      return gather ? pick_bm<true, MOE_EPI_STORE, true>(bm, v)
+                    : pick_bm<true, MOE_EPI_STORE, false>(bm, v);
+    if (epi == MOE_EPI_STORE_BF16)
+      return gather ? pick_bm<true, MOE_EPI_STORE_BF16, true>(bm, v)
+                    : pick_bm<true, MOE_EPI_STORE_BF16, false>(bm, v);
     return false;
   }
-  if (epi == MOE_EPI_SCATTER) return pick_bm<false, MOE_EPI_SCATTER>(bm, v);
-  if (epi == MOE_EPI_STORE) return pick_bm<false, MOE_EPI_STORE>(bm, v);
-  if (epi == MOE_EPI_STORE_BF16) return pick_bm<false, MOE_EPI_STORE_BF16>(bm, v);
-  if (epi == MOE_EPI_SWIGLU) return pick_bm<false, MOE_EPI_SWIGLU>(bm, v);
+  if (epi == MOE_EPI_SWIGLU)
+    return gather ? pick_bm<false, MOE_EPI_SWIGLU, true>(bm, v)
+                  : pick_bm<false, MOE_EPI_SWIGLU, false>(bm, v);
+  if (gather) return false;
+  if (epi == MOE_EPI_SCATTER) return pick_bm<false, MOE_EPI_SCATTER, false>(bm, v);
+  if (epi == MOE_EPI_STORE) return pick_bm<false, MOE_EPI_STORE, false>(bm, v);
+  if (epi == MOE_EPI_STORE_BF16) return pick_bm<false, MOE_EPI_STORE_BF16, false>(bm, v);
   return false;
 }
+
+bool gemm_gather_supported(bool fp8, int epi) { return fp8 || epi == MOE_EPI_SWIGLU; }
 
 int gemm_stage_bytes(bool fp8, int epi, int bm) {
   GemmVariant v;
-  if (!select_gemm_variant(fp8, epi, bm, v)) return 0;
+  if (!select_gemm_variant(fp8, epi, bm, false, v)) return 0;
   return v.stage_bytes;
 }
 
 int gemm_table_bytes(int E) { return (2 * (E + 1) * 4 + 15) & ~15; }
+
+int gemm_rows_bytes(bool fp8, int bm) { return ring_slots(fp8, bm) * bm * 4; }
 
 int gemm_meta_bytes(bool fp8, int bm, int kb_per_split) {
   return ring_slots(fp8, bm) * meta_slot_bytes(fp8, bm, kb_per_split);
@@ -824,10 +936,11 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
                                 const GemmParams& p, bool fp8, int epi, int bm, int num_ctas,
                                 cudaStream_t stream, bool pdl) {
   GemmVariant v;
-  if (!select_gemm_variant(fp8, epi, bm, v)) return cudaErrorInvalidValue;
+  if (!select_gemm_variant(fp8, epi, bm, p.gather != 0, v)) return cudaErrorInvalidValue;
   if (p.sk != 1 && p.sk != 2 && p.sk != 4) return cudaErrorInvalidValue;
   const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * p.sk * v.stage_bytes +
-                      gemm_meta_bytes(fp8, bm, p.kb_per_split) + gemm_table_bytes(p.E);
+                      gemm_meta_bytes(fp8, bm, p.kb_per_split) + gemm_table_bytes(p.E) +
+                      (p.gather ? gemm_rows_bytes(fp8, bm) : 0);
   cudaError_t err = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err == cudaSuccess)

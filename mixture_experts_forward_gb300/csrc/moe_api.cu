@@ -76,6 +76,24 @@ bool make_tmap(CUtensorMap* m, const void* base, bool fp8, uint64_t inner, uint6
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over token-major rows [rows, inner] for the gathered-rows mode:
+// one-row boxes of 128 bytes (tile::gather4 loads four rows per copy), with
+// the same 128-byte swizzle as the tiled operand boxes.
+bool make_tmap_rows(CUtensorMap* m, const void* base, bool fp8, uint64_t inner, uint64_t rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const uint32_t esize = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {128u / esize, 1u};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 thread_local char g_last_error[256] = "";
 
 moe_status_t cuda_status(cudaError_t e) {
@@ -125,6 +143,12 @@ moe_status_t check_gemm(const moe_gemm_args* a) {
   }
   if (a->k_splits < 0) return MOE_ERR_INVALID_ARG;
   if (a->k_splits > 1 && !(fp8 && a->epilogue == MOE_EPI_SCATTER)) return MOE_ERR_UNSUPPORTED;
+  if (a->gather_rows != 0) {
+    if (a->gather_rows != 1 || a->sorted_route_ids == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!gemm_gather_supported(fp8, a->epilogue)) return MOE_ERR_UNSUPPORTED;
+    if (a->M <= 0 || a->top_k <= 0 || static_cast<long long>(a->M) * a->top_k != a->R)
+      return MOE_ERR_INVALID_ARG;
+  }
   return MOE_OK;
 }
 
@@ -172,10 +196,13 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m);
   if (stage_bytes <= 0) return MOE_ERR_UNSUPPORTED;
   const int meta_bytes = gemm_meta_bytes(fp8, a->block_m, p.kb_per_split);
+  p.gather = a->gather_rows;
+  p.M = a->M;
+  const int rows_bytes = p.gather ? gemm_rows_bytes(fp8, a->block_m) : 0;
   // Several K blocks per stage (more bytes per copy instruction, and 128 *
   // sk contiguous bytes of every weight row per copy): the largest of 4, 2, 1
   // that divides a split and still leaves at least three stages.
-  const int avail = 232448 - 1024 - 2048 - meta_bytes - gemm_table_bytes(a->E);
+  const int avail = 232448 - 1024 - 2048 - meta_bytes - gemm_table_bytes(a->E) - rows_bytes;
   p.sk = 1;
   for (int sk = 4; sk >= 2; sk /= 2)
     if (p.kb_per_split % sk == 0 && avail / (sk * stage_bytes) >= 3) { p.sk = sk; break; }
@@ -194,9 +221,13 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   if (!make_tmap(&tw, a->w, fp8, static_cast<uint64_t>(a->K),
                  static_cast<uint64_t>(a->E) * a->N, 128u, static_cast<uint32_t>(p.sk)))
     return MOE_ERR_CUDA;
-  if (!make_tmap(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->R),
-                 static_cast<uint32_t>(a->block_m), static_cast<uint32_t>(p.sk)))
+  if (p.gather) {
+    if (!make_tmap_rows(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->M)))
+      return MOE_ERR_CUDA;
+  } else if (!make_tmap(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->R),
+                        static_cast<uint32_t>(a->block_m), static_cast<uint32_t>(p.sk))) {
     return MOE_ERR_CUDA;
+  }
   return cuda_status(launch_grouped_gemm(tw, ta, p, fp8, a->epilogue, a->block_m, ctas, stream,
                                          pdl));
 }
@@ -227,6 +258,13 @@ bool rows_path(const moe_forward_args* f) {
   return static_cast<long long>(f->M) * out_cols * 4 > kAccOnChipBytes;
 }
 
+// The forward's large-batch path with gather_rows set gathers the routed rows
+// inside the first grouped GEMM.
+bool forward_gathers(const moe_forward_args* f) {
+  const bool fp8 = f->dtype == MOE_DTYPE_FP8_E4M3;
+  return f->gather_rows == 1 && !(fp8 && quant_layout_fits(f->M, f->K, f->top_k, f->E));
+}
+
 WsLayout ws_layout(const moe_forward_args* f) {
   WsLayout L;
   std::memset(&L, 0, sizeof(L));
@@ -250,8 +288,12 @@ WsLayout ws_layout(const moe_forward_args* f) {
   L.local_rank = take(R * 4);
   L.cta_hist = take(n_rank_ctas * E * 4);
   L.cta_base = take(n_rank_ctas * E * 4);
-  L.a = take(fp8 ? R * K : R * K * 2);
-  L.a_scales = fp8 ? take((K / 128) * R * 4) : 0;
+  // gathered rows (large batches): FP8 codes and scales token-major, BF16 rows
+  // read straight from x; otherwise the expert-compact copy
+  const bool gather = forward_gathers(f);
+  const size_t a_rows = gather ? M : R;
+  L.a = (gather && !fp8) ? 0 : take(fp8 ? a_rows * K : a_rows * K * 2);
+  L.a_scales = fp8 ? take((K / 128) * a_rows * 4) : 0;
   const size_t out_cols = fp8 ? N : K;
   // fp32 accumulator [M, out] for the scatter-add, or bf16 expert-compact rows
   // [R, out] reduced afterwards (see rows_path)
@@ -276,6 +318,7 @@ moe_status_t check_forward(const moe_forward_args* f) {
   if (static_cast<long long>(f->M) * f->top_k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
   if (f->K % 128 != 0 || f->N % 128 != 0 || f->K > 16384) return MOE_ERR_UNSUPPORTED;
   if (!(f->softcap >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (f->gather_rows != 0 && f->gather_rows != 1) return MOE_ERR_INVALID_ARG;
   if (f->block_m != 0 && (f->block_m < 16 || f->block_m > 256 || (f->block_m & (f->block_m - 1))))
     return MOE_ERR_UNSUPPORTED;
   if (f->dtype == MOE_DTYPE_FP8_E4M3) {
@@ -309,6 +352,9 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
 
   const bool small = fp8 && quant_layout_fits(M, K, k, E);
   const bool rows = !small && rows_path(f);
+  // gather_rows: the (first) grouped GEMM gathers its routed rows from the
+  // token-major activations, so no expert-compact copy is written
+  const bool gather = forward_gathers(f);
   if (small) {
     // small batch: route, then quantise + layout + gather in one kernel
     e = launch_route(logits, M, E, k, f->softcap, f->renorm, ids, wts, stream, false);
@@ -336,7 +382,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
                               slot, tile_off, ctrl, stream, pdl);
     else
       e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, rows ? nullptr : acc, N, pl, stream,
-                              pdl);
+                              pdl, gather);
     if (e != cudaSuccess) return cuda_status(e);
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));
@@ -360,6 +406,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     g.route_weights = wts;
     g.out = acc;
     g.k_splits = rows ? 1 : f->k_splits;
+    g.gather_rows = gather ? 1 : 0;
     moe_status_t s = run_gemm(&g, ctrl, false, stream, pdl);
     if (s != MOE_OK) return s;
     if (rows)
@@ -374,7 +421,10 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   // -> down (scatter-add, or bf16 rows) -> finalize (or weighted row reduction)
   void* a = ws + L.a;
   void* h = ws + L.h;
-  e = launch_gather_rows_bf16(x, M, K, k, slot, a, rows ? nullptr : acc, K, pl, stream, pdl);
+  if (gather)
+    e = launch_place_routes(M, k, slot, rows ? nullptr : acc, K, pl, stream, pdl);
+  else
+    e = launch_gather_rows_bf16(x, M, K, k, slot, a, rows ? nullptr : acc, K, pl, stream, pdl);
   if (e != cudaSuccess) return cuda_status(e);
   moe_gemm_args g;
   std::memset(&g, 0, sizeof(g));
@@ -388,14 +438,17 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   g.R = R;
   g.M = M;
   g.top_k = k;
-  g.a = a;
+  g.a = gather ? x : a;
   g.w = f->w;
   g.offsets = offsets;
   g.tile_offsets = tile_off;
+  g.sorted_route_ids = sorted;
   g.out = h;
   g.k_splits = 1;
+  g.gather_rows = gather ? 1 : 0;
   moe_status_t s = run_gemm(&g, ctrl, false, stream, pdl);
   if (s != MOE_OK) return s;
+  g.gather_rows = 0;
   g.epilogue = rows ? MOE_EPI_STORE_BF16 : MOE_EPI_SCATTER;
   g.N = K;
   g.K = N;

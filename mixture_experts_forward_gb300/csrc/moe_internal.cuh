@@ -38,6 +38,8 @@ struct GemmParams {
   int w_reuse;                  // experts average more than one row tile: keep weights in L2
   int tail_tiles;               // queue, FP8 scatter, one K split: last tiles split in K halves
   int tail_halfkb;              // K blocks of a split tile's first half (a multiple of sk)
+  int gather;                   // A rows gathered from token-major rows (see moe_gemm_args)
+  int M;                        // gather: rows of the token-major A (tokens)
   int drop_producer;
   unsigned long long timeout_ns;
 };
@@ -79,8 +81,15 @@ cudaError_t launch_quant_layout(const void* x, int M, int K, int k, int E, int b
                                 int32_t* tile_offsets, Ctrl* ctrl, cudaStream_t stream, bool pdl);
 cudaError_t launch_finalize(const float* acc, void* out, size_t n, int num_sms,
                             cudaStream_t stream, bool pdl);
+// token_major: write each token's codes once ([M, K], scales [K/128, M]) and
+// only place the routes, for a grouped GEMM that gathers its rows.
 cudaError_t launch_quant_gather(const void* x, int M, int K, int k, int32_t* route_slot,
                                 uint8_t* a_q, float* a_scales, float* zero_acc, int zero_cols,
+                                const Placement& pl, cudaStream_t stream, bool pdl,
+                                bool token_major = false);
+// Large-batch placement without a row copy (the GEMM gathers rows): zero the
+// accumulator rows, then write route_slot and sorted_route_ids.
+cudaError_t launch_place_routes(int M, int k, int32_t* route_slot, float* zero_acc, int zero_cols,
                                 const Placement& pl, cudaStream_t stream, bool pdl);
 // out bf16 [M,N] = weighted sum over each token's k bf16 rows (N % 8 == 0).
 cudaError_t launch_reduce_rows(const void* rows, const int32_t* route_slot, const float* weights,
@@ -96,6 +105,8 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
                                 cudaStream_t stream, bool pdl);
 int gemm_stage_bytes(bool fp8, int epi, int bm);
 int gemm_meta_bytes(bool fp8, int bm, int kb_per_split);
+int gemm_rows_bytes(bool fp8, int bm);   // the route-id ring of the gathered-rows mode
+bool gemm_gather_supported(bool fp8, int epi);
 int gemm_table_bytes(int E);
 
 }  // namespace moe

@@ -34,10 +34,14 @@ __device__ __forceinline__ int route_slot_of(int r, int t, const int32_t* route_
   return slot;
 }
 
+// token_major = 1 (the grouped GEMM gathers rows itself): each token's codes
+// and scales are written once, token-major (a_q [M, K], a_scales [K/128, M]),
+// before the wait for the router; after it the kernel only places the routes
+// (route_slot, sorted_route_ids).
 __global__ void __launch_bounds__(1024) quant_gather_kernel(
     const __nv_bfloat16* __restrict__ x, int M, int K, int k, int32_t* route_slot,
     uint8_t* __restrict__ a_q, float* __restrict__ a_scales, float* __restrict__ zero_acc,
-    int zero_cols, const Placement pl) {
+    int zero_cols, const Placement pl, int token_major) {
   __shared__ int s_slot[1024];
   const int G = K >> 4;                            // threads per token
   const int tpc = max(1, static_cast<int>(blockDim.x) / G);  // tokens per CTA
@@ -59,6 +63,15 @@ __global__ void __launch_bounds__(1024) quant_gather_kernel(
   uint4 q;
   float s;
   quantize16(x + static_cast<size_t>(valid ? t : 0) * K, c, valid, q, s);
+  if (token_major) {
+    if (valid) {
+      *reinterpret_cast<uint4*>(a_q + static_cast<size_t>(t) * K + 16 * c) = q;
+      if ((c & 7) == 0) a_scales[static_cast<size_t>(c >> 3) * M + t] = s;
+    }
+    pdl_wait();
+    if (valid && c < k) route_slot_of(t * k + c, t, route_slot, route_slot, pl, R);
+    return;
+  }
   pdl_wait();
 
   if (valid && c < k) s_slot[lt * k + c] = route_slot_of(t * k + c, t, route_slot, route_slot, pl, R);
@@ -241,7 +254,8 @@ __global__ void __launch_bounds__(1024) quant_layout_kernel(
 
 cudaError_t launch_quant_gather(const void* x, int M, int K, int k, int32_t* route_slot,
                                 uint8_t* a_q, float* a_scales, float* zero_acc, int zero_cols,
-                                const Placement& pl, cudaStream_t stream, bool pdl) {
+                                const Placement& pl, cudaStream_t stream, bool pdl,
+                                bool token_major) {
   const int G = K / 16;
   int threads, tpc;
   if (G <= 256) {
@@ -263,7 +277,8 @@ cudaError_t launch_quant_gather(const void* x, int M, int K, int k, int32_t* rou
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, quant_gather_kernel, static_cast<const __nv_bfloat16*>(x), M, K,
-                            k, route_slot, a_q, a_scales, zero_acc, zero_cols, pl);
+                            k, route_slot, a_q, a_scales, zero_acc, zero_cols, pl,
+                            token_major ? 1 : 0);
 }
 
 bool quant_layout_fits(int M, int K, int k, int E) {

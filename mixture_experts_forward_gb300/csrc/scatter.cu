@@ -161,6 +161,37 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   }
 }
 
+// Large-batch placement for a GEMM that gathers rows itself: 32 tokens per
+// CTA; their accumulator rows are cleared before the wait for the router, then
+// each route's slot is placed (route_slot, sorted_route_ids) as
+// offsets[e] + cta_base[t / 32][e] + local_rank[r].
+__global__ void __launch_bounds__(256) place_routes_kernel(int M, int k, int32_t* route_slot,
+                                                           float* __restrict__ zero_acc,
+                                                           int zero_cols, const Placement pl) {
+  pdl_launch_dependents();
+  const int t0 = blockIdx.x * 32;
+  const int nt = min(32, M - t0);
+  const int R = M * k;
+  if (zero_acc != nullptr) {
+    const int q = zero_cols >> 2;
+    float4* rows = reinterpret_cast<float4*>(zero_acc + static_cast<size_t>(t0) * zero_cols);
+    for (int i = threadIdx.x; i < nt * q; i += blockDim.x) rows[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  pdl_wait();
+  for (int i = threadIdx.x; i < nt * k; i += blockDim.x) {
+    const int r = t0 * k + i;
+    const int t = r / k;
+    const int e = __ldg(pl.ids + r);
+    if (e < 0 || e >= pl.E) continue;
+    const int slot = __ldg(pl.offsets + e) +
+                     __ldg(pl.cta_base + static_cast<size_t>(t / kRankTokensPerCta) * pl.E + e) +
+                     __ldg(pl.local_rank + r);
+    if (slot < 0 || slot >= R) continue;
+    route_slot[r] = slot;
+    pl.sorted_route_ids[slot] = r;
+  }
+}
+
 cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t stream, bool pdl,
                             cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
@@ -210,6 +241,15 @@ cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const f
   cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(256), stream, false, attr);
   return cudaLaunchKernelEx(&cfg, scatter_kernel, rows, route_slot, weights, M, N, k,
                             static_cast<__nv_bfloat16*>(out));
+}
+
+cudaError_t launch_place_routes(int M, int k, int32_t* route_slot, float* zero_acc, int zero_cols,
+                                const Placement& pl, cudaStream_t stream, bool pdl) {
+  cudaError_t err = prefer_max_shared(place_routes_kernel);
+  if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3((M + 31) / 32), dim3(256), stream, pdl, attr);
+  return cudaLaunchKernelEx(&cfg, place_routes_kernel, M, k, route_slot, zero_acc, zero_cols, pl);
 }
 
 cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, int32_t* route_slot,

@@ -52,14 +52,15 @@ def fp8_device_inputs(d):
 
 
 def run_forward_fp8(dev, cfg, block_m=0, sched=L.SCHED_QUEUE, k_splits=0, use_graph=1,
-                    renorm=1, softcap=None):
+                    renorm=1, softcap=None, gather_rows=0):
     M, E = dev["logits"].shape
     K = dev["x"].shape[1]
     N = dev["w_q"].shape[1]
     args = L.forward_args(dtype=L.DTYPE_FP8, M=M, K=K, N=N, E=E, top_k=cfg["k"],
                           softcap=cfg["softcap"] if softcap is None else softcap, renorm=renorm,
                           logits=dev["logits"], x=dev["x"], w=dev["w_q"], w_scales=dev["w_scales"],
-                          block_m=block_m, sched=sched, k_splits=k_splits, use_graph=use_graph)
+                          block_m=block_m, sched=sched, k_splits=k_splits, use_graph=use_graph,
+                          gather_rows=gather_rows)
     ws = L.new_workspace(L.workspace_size(args))
     out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     L.forward(args, out, ws)
@@ -68,13 +69,14 @@ def run_forward_fp8(dev, cfg, block_m=0, sched=L.SCHED_QUEUE, k_splits=0, use_gr
     return out, args, ws
 
 
-def run_forward_bf16(dev, cfg, block_m=0, sched=L.SCHED_QUEUE, use_graph=1):
+def run_forward_bf16(dev, cfg, block_m=0, sched=L.SCHED_QUEUE, use_graph=1, gather_rows=0):
     T, E = dev["logits"].shape
     H = dev["x"].shape[1]
     I = dev["w_dn"].shape[2]
     args = L.forward_args(dtype=L.DTYPE_BF16, M=T, K=H, N=I, E=E, top_k=cfg["k"], softcap=0.0,
                           logits=dev["logits"], x=dev["x"], w=dev["w_up"], w2=dev["w_dn"],
-                          block_m=block_m, sched=sched, use_graph=use_graph)
+                          block_m=block_m, sched=sched, use_graph=use_graph,
+                          gather_rows=gather_rows)
     ws = L.new_workspace(L.workspace_size(args))
     out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
     L.forward(args, out, ws)

@@ -239,6 +239,94 @@ def test_gemm_bf16_static_schedule():
                     sched=L.SCHED_STATIC)
 
 
+def _gather_gemm_fp8_case(M, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, k_splits=0, seed=0,
+                          skew=0.0, num_ctas=0):
+    """gather_rows=1: the GEMM reads each routed row from the token-major
+    codes (row sorted_route_ids[s] // k) and its scales from [K/128, M]."""
+    d = inputs.make_fp8_inputs(dict(M=M, K=K, N=N, E=E, k=k, softcap=0.0, zipf_bias=skew),
+                               seed=seed)
+    rid, rw = oracle.route(d["logits"].numpy(), k)
+    lay = oracle.layout(rid, E, block_m=bm)
+    a_q, a_s = oracle.quant_gather(bits(d["x"]), k, lay["route_slot"])       # compact (reference)
+    a_tok, s_tok = oracle.quant_gather(bits(d["x"]), 1, np.arange(M, dtype=np.int32))  # token-major
+    Y = oracle.grouped_gemm_fp8(a_q, a_s, d["w_q"].numpy(), d["w_scales"].numpy(),
+                                lay["offsets"], threads=THREADS)
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    ws = L.new_workspace(L.CTRL_BYTES)
+    common = dict(dtype=L.DTYPE_FP8, a=cu(a_tok), a_scales=cu(s_tok), w=d["w_q"].cuda(),
+                  w_scales=d["w_scales"].cuda(), offsets=cu(lay["offsets"]),
+                  tile_offsets=cu(lay["tile_offsets"]), ws=ws, block_m=bm, sched=sched,
+                  num_ctas=num_ctas, sorted_route_ids=cu(lay["sorted_route_ids"]), M=M, top_k=k,
+                  gather_rows=1)
+    if epilogue == L.EPI_SCATTER:
+        out = torch.zeros(M, N, device="cuda")
+        L.grouped_gemm(epilogue=epilogue, out=out, route_weights=cu(rw), k_splits=k_splits,
+                       **common)
+        ref = oracle.scatter(Y, lay["route_slot"], rw)
+    else:
+        out = torch.zeros(M * k, N, device="cuda")
+        L.grouped_gemm(epilogue=epilogue, out=out, **common)
+        ref = Y
+    torch.cuda.synchronize()
+    assert L.get_error(ws) == L.MOE_OK
+    assert_close(out, ref, "fp8 gathered rows")
+
+
+@pytest.mark.parametrize("bm,epi,sched,ks", [
+    (16, L.EPI_SCATTER, L.SCHED_QUEUE, 1), (64, L.EPI_SCATTER, L.SCHED_STATIC, 1),
+    (128, L.EPI_SCATTER, L.SCHED_QUEUE, 0), (32, L.EPI_SCATTER, L.SCHED_QUEUE, 4),
+    (128, L.EPI_STORE, L.SCHED_QUEUE, 1), (64, L.EPI_STORE, L.SCHED_STATIC, 1)])
+def test_gemm_fp8_gathered_rows(bm, epi, sched, ks):
+    """Ragged tails, empty experts (skewed loads), K splits and both schedulers."""
+    _gather_gemm_fp8_case(M=300, K=1024, N=384, E=16, k=4, bm=bm, epilogue=epi, sched=sched,
+                          k_splits=ks, skew=1.5)
+
+
+def test_gemm_fp8_gathered_rows_few_ctas():
+    """Eight CTAs loop over many tiles: the route-id ring wraps many times."""
+    _gather_gemm_fp8_case(M=700, K=2048, N=512, E=4, k=2, bm=128, epilogue=L.EPI_SCATTER,
+                          num_ctas=8)
+
+
+@pytest.mark.parametrize("bm,epi", [(16, L.EPI_SWIGLU), (64, L.EPI_SWIGLU), (256, L.EPI_SWIGLU),
+                                    (128, L.EPI_SCATTER)])
+def test_gemm_bf16_gathered_rows(bm, epi):
+    """The gated up projection gathers x's rows; other BF16 epilogues do not
+    gather (MOE_ERR_UNSUPPORTED)."""
+    g = torch.Generator().manual_seed(3)
+    M, K, N, E, k = 230, 320, 256, 8, 2
+    rid, rw = oracle.route(torch.randn(M, E, generator=g).numpy(), k)
+    lay = oracle.layout(rid, E, block_m=bm)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    w = (torch.randn(E, N, K, generator=g) / np.sqrt(K)).to(torch.bfloat16)
+    A = x[torch.from_numpy(lay["sorted_route_ids"] // k).long()].double().numpy()
+    W = w.double().numpy()
+    Y = np.zeros((M * k, N))
+    for e in range(E):
+        s0, s1 = lay["offsets"][e], lay["offsets"][e + 1]
+        Y[s0:s1] = A[s0:s1] @ W[e].T
+    cu = lambda t: torch.from_numpy(np.ascontiguousarray(t)).cuda()
+    ws = L.new_workspace(L.CTRL_BYTES)
+    common = dict(dtype=L.DTYPE_BF16, epilogue=epi, a=x.cuda(), w=w.cuda(),
+                  offsets=cu(lay["offsets"]), tile_offsets=cu(lay["tile_offsets"]), ws=ws,
+                  block_m=bm, sorted_route_ids=cu(lay["sorted_route_ids"]), M=M, top_k=k,
+                  gather_rows=1)
+    if epi == L.EPI_SWIGLU:
+        out = torch.zeros(M * k, N // 2, dtype=torch.bfloat16, device="cuda")
+        L.grouped_gemm(out=out, **common)
+        gate, up = Y[:, :N // 2], Y[:, N // 2:]
+        ref = gate / (1.0 + np.exp(-gate)) * up
+    else:
+        out = torch.zeros(M, N, device="cuda")
+        with pytest.raises(L.MoeError) as err:
+            L.grouped_gemm(out=out, route_weights=cu(rw), **common)
+        assert err.value.code == L.MOE_ERR_UNSUPPORTED
+        return
+    torch.cuda.synchronize()
+    assert L.get_error(ws) == L.MOE_OK
+    assert_close(out, ref, "bf16 gathered rows")
+
+
 # ------------------------------------------------------------------ fused forward
 @pytest.mark.parametrize("softcap", [0.0, 30.0])
 @pytest.mark.parametrize("use_graph", [0, 1])
@@ -303,11 +391,12 @@ def test_forward_fp8_bf16_rows_path_sampled():
 
 
 def _bf16_forward_case(cfg_name, routing, rho=1.0, n_tok=32, block_m=0, sched=L.SCHED_QUEUE,
-                       overrides=None):
+                       overrides=None, gather_rows=0):
     d = inputs.make_bf16_inputs(cfg_name, routing=routing, rho=rho, seed=0, **(overrides or {}))
     dev = dict(logits=d["logits"].cuda(), x=d["x"].cuda(), w_up=d["w_up"].cuda(),
                w_dn=d["w_dn"].cuda())
-    out, _, _ = run_forward_bf16(dev, d["cfg"], block_m=block_m, sched=sched)
+    out, _, _ = run_forward_bf16(dev, d["cfg"], block_m=block_m, sched=sched,
+                                 gather_rows=gather_rows)
     k = d["cfg"]["k"]
     ids, w = oracle.route(d["logits"].numpy(), k)
     assert np.array_equal(np.sort(ids, axis=1), np.sort(d["chosen"].numpy(), axis=1))
@@ -320,6 +409,29 @@ def _bf16_forward_case(cfg_name, routing, rho=1.0, n_tok=32, block_m=0, sched=L.
 def test_forward_bf16_small_all_rows():
     _bf16_forward_case("bf16_ffn", "uniform", n_tok=10**9,
                        overrides=dict(T=200, H=256, I=256, E=8, k=3))
+
+
+@pytest.mark.parametrize("bm", [64, 256])
+def test_forward_bf16_gathered_rows_all_rows(bm):
+    """gather_rows=1: the up projection reads x's rows by route id (no copy)."""
+    _bf16_forward_case("bf16_ffn", "uniform", n_tok=10**9, block_m=bm, gather_rows=1,
+                       overrides=dict(T=300, H=256, I=256, E=8, k=3))
+
+
+@pytest.mark.parametrize("bm", [64, 128])
+def test_forward_fp8_gathered_rows_all_rows(bm):
+    """gather_rows=1 on the large-batch FP8 path (more than 4096 routes): codes
+    and scales token-major, rows gathered in the GEMM; every output row."""
+    cfg = dict(M=1100, K=1024, N=384, E=32, k=4, softcap=30.0, zipf_bias=1.0)
+    d = inputs.make_fp8_inputs(cfg, seed=5)
+    dev = fp8_device_inputs(d)
+    out, args, _ = run_forward_fp8(dev, d["cfg"], block_m=bm, gather_rows=1)
+    assert L.workspace_size(args) < L.workspace_size(L.forward_args(
+        dtype=L.DTYPE_FP8, M=1100, K=1024, N=384, E=32, top_k=4, w=dev["w_q"],
+        w_scales=dev["w_scales"], gather_rows=0))
+    r = oracle.forward_fp8(d["logits"].numpy(), bits(d["x"]), d["w_q"].numpy(),
+                           d["w_scales"].numpy(), k=4, softcap=30.0, threads=THREADS)
+    assert_close(out, r["out"], f"fp8 gathered rows bm={bm}")
 
 
 @pytest.mark.parametrize("routing", ["balanced", "uniform", "zipf1.2"])
