@@ -292,6 +292,23 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
     tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
     tmem_relinquish();
   }
+  if (p.warm_first > 0 && warp == 0) {
+    // The queue hands CTA c tile c first and tiles c + G, c + 2G ... mostly
+    // next (G CTAs).  When every expert has a single row tile (small batches),
+    // tile t is expert t / (n_tiles * k_splits); its weight rows do not depend
+    // on the routing, so the first warm_first waves' weights are prefetched
+    // into L2 while the router and layout still run (HBM is otherwise idle).
+    const int per_e = p.n_tiles * p.k_splits;
+    for (int w = 0; w < p.warm_first; ++w) {
+      const int t = blockIdx.x + w * gridDim.x;
+      const int e = t / per_e, r = t - e * per_e;
+      const int nt = r / p.k_splits, ks = r - nt * p.k_splits;
+      const int kb0 = ks * p.kb_per_split, kb1 = min(p.KB, kb0 + p.kb_per_split);
+      if (e < p.E)
+        for (int kb = kb0 + lane * p.sk; kb < kb1; kb += 32 * p.sk)
+          tma_prefetch_l2_3d(&tmap_w, 0, e * p.N + nt * kTileN, kb);
+    }
+  }
   // Everything above is independent of the preceding kernel's results.
   pdl_wait();
   for (int i = threadIdx.x; i <= p.E; i += C::kThreads) {  // all copies in flight, one wait

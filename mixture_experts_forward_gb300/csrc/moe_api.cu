@@ -198,6 +198,9 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   const int meta_bytes = gemm_meta_bytes(fp8, a->block_m, p.kb_per_split);
   p.gather = a->gather_rows;
   p.M = a->M;
+  // FP8 weights read once per expert (no row-tile reuse) through the queue:
+  // warm L2 with each CTA's likely first weight tile before the layout is known
+  p.warm_first = (fp8 && !p.w_reuse && a->sched == MOE_SCHED_QUEUE) ? 1 : 0;
   const int rows_bytes = p.gather ? gemm_rows_bytes(fp8, a->block_m) : 0;
   // Several K blocks per stage (more bytes per copy instruction, and 128 *
   // sk contiguous bytes of every weight row per copy): the largest of 4, 2, 1

@@ -142,6 +142,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// L2 prefetch of one 3-D box (no shared memory written, nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // Four rows gathered by row index from a 2-D map whose box is one row high:
 // rows r0..r3 (each the box's inner width starting at column c0) land in
 // shared memory as four consecutive rows, with the map's swizzle.

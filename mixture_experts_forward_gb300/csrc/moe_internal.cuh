@@ -38,6 +38,8 @@ struct GemmParams {
   int w_reuse;                  // experts average more than one row tile: keep weights in L2
   int tail_tiles;               // queue, FP8 scatter, one K split: last tiles split in K halves
   int tail_halfkb;              // K blocks of a split tile's first half (a multiple of sk)
+  int warm_first;               // before the wait for the layout: L2-prefetch the weight tiles
+                                // of this CTA's likely first warm_first tiles (0 = off)
   int gather;                   // A rows gathered from token-major rows (see moe_gemm_args)
   int M;                        // gather: rows of the token-major A (tokens)
   int drop_producer;
