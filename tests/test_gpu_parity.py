@@ -98,8 +98,9 @@ def test_layout_reports_bad_ids():
 
 # ------------------------------------------------------------------ quantise + gather
 @pytest.mark.parametrize("M,K,k", [(16, 256, 2), (128, 2048, 8), (37, 384, 3), (5, 8192, 1),
-                                   (64, 16384, 2), (333, 128, 4)])
+                                   (64, 16384, 2), (333, 128, 4), (4096, 2048, 8), (5000, 1024, 6)])
 def test_quant_gather_bit_exact(M, K, k):
+    """Includes batches large enough for 32 elements per thread (one wave)."""
     g = torch.Generator().manual_seed(M + K)
     x = (torch.randn(M, K, generator=g) * torch.exp(torch.randn(M, 1, generator=g) * 4)).to(torch.bfloat16)
     x[0, :128] = 0.0                                   # an all-zero block
