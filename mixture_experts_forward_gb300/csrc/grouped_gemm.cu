@@ -106,22 +106,23 @@ __host__ __device__ inline int meta_slot_bytes(bool fp8, int bm, int kb_per_spli
 }
 
 // Work items of the queue: with a split tail (p.tail_tiles > 0, one K split)
-// the last tail_tiles output tiles are handed out as two K halves each, so
-// the final wave of work is half as long; the other items are whole tiles.
+// the last tail_tiles output tiles are handed out as tail_parts K parts each
+// (halves or quarters), so the final wave of work is that much shorter; the
+// other items are whole tiles.
 __device__ __forceinline__ int work_items(const GemmParams& p, const int* s_tile_off) {
   const int T = s_tile_off[p.E] * p.n_tiles * p.k_splits;
-  return T + min(p.tail_tiles, T);
+  return T + min(p.tail_tiles, T) * (p.tail_parts - 1);
 }
 
 __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const int* s_tile_off,
                                             const int* s_off, int BM, TileDesc& d) {
-  int half = -1;  // >= 0: K half of a split tail tile
+  int part = -1;  // >= 0: K part of a split tail tile
   if (p.tail_tiles > 0) {
     const int T = s_tile_off[p.E] * p.n_tiles;
     const int F = T - min(p.tail_tiles, T);
     if (t >= F) {
-      half = (t - F) & 1;
-      t = F + ((t - F) >> 1);
+      part = (t - F) % p.tail_parts;
+      t = F + (t - F) / p.tail_parts;
     }
   }
   const int per_m = p.n_tiles * p.k_splits;
@@ -155,9 +156,9 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const in
   const int ks = r - d.n_tile * p.k_splits;
   d.kb0 = ks * p.kb_per_split;
   d.nkb = min(p.kb_per_split, p.KB - d.kb0);
-  if (half >= 0) {  // split point on a stage boundary (tail_halfkb is a multiple of sk)
-    d.kb0 = half * p.tail_halfkb;
-    d.nkb = half ? p.KB - p.tail_halfkb : p.tail_halfkb;
+  if (part >= 0) {  // split points on stage boundaries (tail_partkb is a multiple of sk)
+    d.kb0 = part * p.tail_partkb;
+    d.nkb = part == p.tail_parts - 1 ? p.KB - d.kb0 : p.tail_partkb;
   }
 }
 

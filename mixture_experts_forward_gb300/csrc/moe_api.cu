@@ -214,11 +214,20 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   if (stages < 2) return MOE_ERR_UNSUPPORTED;
   p.num_stages = stages;
   // FP8 scatter through the queue: split the last wave (one tile per CTA) in
-  // K halves, so CTAs finish within half a tile of one another
+  // K parts, so CTAs finish within a part of a tile of one another — quarters
+  // where tiles are narrow (block_m <= 32: a cheap epilogue per part), else halves
   const int ctas = a->num_ctas > 0 ? a->num_ctas : sms;
-  p.tail_halfkb = (p.KB / 2) / p.sk * p.sk;
+  p.tail_parts = 2;
+  for (int parts = a->block_m <= 32 ? 4 : 2; parts >= 2; parts /= 2) {
+    const int partkb = (p.KB / parts) / p.sk * p.sk;
+    if (partkb >= p.sk && p.KB - (parts - 1) * partkb >= p.sk) {
+      p.tail_parts = parts;
+      p.tail_partkb = partkb;
+      break;
+    }
+  }
   if (fp8 && a->epilogue == MOE_EPI_SCATTER && p.k_splits == 1 && a->sched == MOE_SCHED_QUEUE &&
-      p.tail_halfkb >= p.sk && p.KB - p.tail_halfkb >= p.sk)
+      p.tail_partkb > 0)
     p.tail_tiles = ctas;
   CUtensorMap tw, ta;
   if (!make_tmap(&tw, a->w, fp8, static_cast<uint64_t>(a->K),
