@@ -79,10 +79,11 @@ struct Cfg {
   // TMA producer warps (warp 0 plus warps 7..): two measured best (four were
   // no faster on any workload and slower on the BF16 FFN)
   static constexpr int kProducers = 2;
-  // FP8 with block_m >= 64: two epilogue warps per TMEM lane quadrant, each
-  // promoting half of the tile's columns (routed rows), so two warps on every
-  // scheduler share the per-K-block promotion; otherwise one per quadrant
-  static constexpr int kEpiGroups = kFP8 && BM >= 64 ? 2 : 1;
+  // FP8 with block_m >= 64 and BF16 with block_m >= 128: two epilogue warps per
+  // TMEM lane quadrant, each taking half of the tile's columns (routed rows),
+  // so two warps on every scheduler share the per-K-block promotion (FP8) or
+  // the per-tile stores and reductions (BF16); otherwise one per quadrant
+  static constexpr int kEpiGroups = (kFP8 && BM >= 64) || (!kFP8 && BM >= 128) ? 2 : 1;
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kEpiCols = BM / kEpiGroups;  // columns promoted by one epilogue warp
   static constexpr int kWarps = kFirstExtraProducer + kProducers - 1 + 4 * (kEpiGroups - 1);
@@ -804,9 +805,11 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
           break;
         }
         tc_fence_after();
-        for (int c0 = 0; c0 < BM && c0 < d.rows; c0 += 16) {
+        // this warp's columns: [c_lo, c_lo + kEpiCols) (lane_addr includes c_lo)
+        for (int c0 = 0; c0 < C::kEpiCols && c_lo + c0 < d.rows; c0 += 16) {
           float v[16];
           tmem_ld16(lane_addr + buf * C::kAccCols + c0, v);
+          const int s0 = c_lo + c0;  // routed row of v[0]
           if constexpr (C::kSwiglu) {
             float u[16];
             tmem_ld16(lane_addr + buf * C::kAccCols + BM + c0, u);
@@ -816,24 +819,24 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
             const int I = p.N / 2;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              if (c0 + j < d.rows) {
+              if (s0 + j < d.rows) {
                 // silu(g) * u with the fast exponential and division (relative
                 // error ~1e-6, far inside the bf16 rounding of h); for very
                 // negative g the denominator overflows and silu -> 0
                 const float g = v[j];
                 const float h = __fdividef(g, 1.0f + __expf(-g)) * u[j];
-                out[static_cast<size_t>(d.m0 + c0 + j) * I + col] = __float2bfloat16_rn(h);
+                out[static_cast<size_t>(d.m0 + s0 + j) * I + col] = __float2bfloat16_rn(h);
               }
             }
           } else {
             tmem_ld_wait(v);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              if (c0 + j < d.rows) {
-                const size_t r = static_cast<size_t>(d.m0 + c0 + j);
+              if (s0 + j < d.rows) {
+                const size_t r = static_cast<size_t>(d.m0 + s0 + j);
                 if constexpr (kEpi == MOE_EPI_SCATTER)
-                  red_add_f32(static_cast<float*>(p.out) + static_cast<size_t>(tok[c0 + j]) * p.N + col,
-                              wt[c0 + j] * v[j]);
+                  red_add_f32(static_cast<float*>(p.out) + static_cast<size_t>(tok[s0 + j]) * p.N + col,
+                              wt[s0 + j] * v[j]);
                 else if constexpr (kEpi == MOE_EPI_STORE_BF16)
                   static_cast<__nv_bfloat16*>(p.out)[r * p.N + col] = __float2bfloat16_rn(v[j]);
                 else
