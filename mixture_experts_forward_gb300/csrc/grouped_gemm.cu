@@ -83,7 +83,10 @@ struct Cfg {
   // TMEM lane quadrant, each taking half of the tile's columns (routed rows),
   // so two warps on every scheduler share the per-K-block promotion (FP8) or
   // the per-tile stores and reductions (BF16); otherwise one per quadrant
-  static constexpr int kEpiGroups = (kFP8 && BM >= 64) || (!kFP8 && BM >= 128) ? 2 : 1;
+  // (BF16 with block_m 256: four, since its SwiGLU accumulator fills TMEM, so
+  // the tile's epilogue is not overlapped with the next tile's MMAs)
+  static constexpr int kEpiGroups = (!kFP8 && BM >= 256) ? 4
+                                  : (kFP8 && BM >= 64) || (!kFP8 && BM >= 128) ? 2 : 1;
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kEpiCols = BM / kEpiGroups;  // columns promoted by one epilogue warp
   static constexpr int kWarps = kFirstExtraProducer + kProducers - 1 + 4 * (kEpiGroups - 1);
@@ -630,8 +633,9 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
                   "the second epilogue group starts at warp 8");
     const int quad = warp & 3;                     // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;              // weight row within the tile
-    // first column (routed row) of this warp's share of the tile
-    const int c_lo = warp >= 8 ? C::kEpiCols : 0;
+    // first column (routed row) of this warp's share of the tile: groups are
+    // warps 2..5, 8..11, 12..15, 16..19
+    const int c_lo = (warp < 8 ? 0 : (warp - 4) / 4) * C::kEpiCols;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + c_lo;
     int ds = 0, acc_n = 0;
     uint32_t dphase = 0;
