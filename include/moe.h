@@ -229,10 +229,14 @@ moe_status_t moe_forward(const moe_forward_args* args, void* out, void* ws, size
                          void* stream);
 
 /* The same forward for host-resident inputs: `host_logits` (f32 [M,E]) and
- * `host_x` (bf16 [M,K]) are copied into the workspace, the forward runs, and
- * the bf16 result is copied to `host_out`, all enqueued on `stream` (pinned
- * host memory makes the copies asynchronous).  args->logits and args->x are
- * ignored; the weights stay device pointers. */
+ * `host_x` (bf16 [M,K]) go in, the bf16 result goes to `host_out`, all
+ * enqueued on `stream`.  When all three are pinned, device-mapped host
+ * buffers, the inputs total at most 32 MiB, the output at most 32 MiB and
+ * gather_rows is 0, the forward's kernels read the inputs and write the
+ * result in host memory directly (over the host link, no staging copies);
+ * otherwise the inputs are copied into the workspace and the result out of it
+ * (pinned memory makes those copies asynchronous).  args->logits and args->x
+ * are ignored; the weights stay device pointers. */
 moe_status_t moe_forward_host(const moe_forward_args* args, const float* host_logits,
                               const void* host_x, void* host_out, void* ws, size_t ws_bytes,
                               void* stream);

@@ -691,6 +691,21 @@ moe_status_t moe_forward(const moe_forward_args* args, void* out, void* ws, size
                       static_cast<cudaStream_t>(stream));
 }
 
+// Largest input (logits + activations) and output of moe_forward_host that
+// its kernels access in host memory directly.
+constexpr size_t kDirectHostBytes = 32u << 20;
+
+// The device address of a pinned, device-mapped host buffer; nullptr for any
+// other pointer (pageable host memory, device memory, an error).
+const void* device_view(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 moe_status_t moe_forward_host(const moe_forward_args* args, const float* host_logits,
                               const void* host_x, void* host_out, void* ws, size_t ws_bytes,
                               void* stream) {
@@ -705,7 +720,22 @@ moe_status_t moe_forward_host(const moe_forward_args* args, const float* host_lo
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   const size_t M = args->M;
   const size_t out_cols = args->dtype == MOE_DTYPE_FP8_E4M3 ? args->N : args->K;
-  if (cudaMemcpyAsync(w8 + L.st_logits, host_logits, M * args->E * 4, cudaMemcpyHostToDevice,
+  const size_t logits_bytes = M * args->E * 4, x_bytes = M * args->K * 2;
+  const size_t out_bytes = M * out_cols * 2;
+  // Pinned (device-mapped) host buffers of a small forward: its kernels read
+  // the logits and activations and write the result over the host link
+  // themselves (only plain loads and stores touch them), so the step needs no
+  // staging copies and their latency; otherwise copy in and out through the
+  // workspace's staging buffers.
+  if (args->gather_rows == 0 && logits_bytes + x_bytes <= kDirectHostBytes &&
+      out_bytes <= kDirectHostBytes) {
+    const void* dl = device_view(host_logits);
+    const void* dx = device_view(host_x);
+    void* dout = const_cast<void*>(device_view(host_out));
+    if (dl != nullptr && dx != nullptr && dout != nullptr)
+      return forward_impl(args, static_cast<const float*>(dl), dx, dout, ws, ws_bytes, st);
+  }
+  if (cudaMemcpyAsync(w8 + L.st_logits, host_logits, logits_bytes, cudaMemcpyHostToDevice,
                       st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaMemcpyAsync(w8 + L.st_x, host_x, M * args->K * 2, cudaMemcpyHostToDevice, st) !=
