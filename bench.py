@@ -405,8 +405,10 @@ def stored_traffic(src_name: str, kernel: str):
 
 
 def bench_e2e(L, fa, d, kind, dev, args, flush, fl, world):
-    """Same metric through moe_forward_host: pinned host inputs copied in and
-    the bf16 result copied out inside every timed step."""
+    """Same metric through moe_forward_host with pinned host buffers: the
+    inputs move host -> device and the bf16 result device -> host inside every
+    timed step (for small buffers the forward's kernels access the pinned
+    buffers over the host link directly; otherwise staging copies)."""
     stream = torch.cuda.current_stream(dev)
     c = d["cfg"]
     if kind == "fp8":
