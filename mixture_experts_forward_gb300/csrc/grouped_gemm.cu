@@ -63,10 +63,15 @@ struct TileDesc {
   int e, m0, rows, n_tile, kb0, nkb;
 };
 
-template <int BM, bool kFP8, int kEpi>
+// kWide (BF16, not SwiGLU): a tile covers two adjacent 128-row weight tiles
+// (256 output columns) that share its routed-row operand — two MMAs per K
+// block from one stage, as the gated up projection has, so a stage carries
+// twice the tensor work for 1.5 times the bytes.
+template <int BM, bool kFP8, int kEpi, bool kWide = false>
 struct Cfg {
   static constexpr bool kSwiglu = kEpi == MOE_EPI_SWIGLU;
-  static constexpr int kAccCols = kSwiglu ? 2 * BM : BM;
+  static constexpr bool kPair = kSwiglu || kWide;          // two weight tiles per stage
+  static constexpr int kAccCols = kPair ? 2 * BM : BM;
   // FP8: one buffer per K block, up to all 512 columns, so the MMA can run a
   // whole tile or more ahead of the epilogue; BF16: double-buffered tiles.
   static constexpr int kNumAcc = kFP8 ? (512 / BM < 32 ? 512 / BM : 32)
@@ -74,7 +79,7 @@ struct Cfg {
   static constexpr int kTmemNeed = kNumAcc * kAccCols;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
-  static constexpr int kATiles = kSwiglu ? 2 : 1;
+  static constexpr int kATiles = kPair ? 2 : 1;
   static constexpr int kRing = ring_slots(kFP8, BM);
   // TMA producer warps (warp 0 plus warps 7..): two measured best (four were
   // no faster on any workload and slower on the BF16 FFN)
@@ -241,11 +246,14 @@ __device__ __forceinline__ void meta_fill(const GemmParams& p, const TileDesc& d
   }
 }
 
-template <int BM, bool kFP8, int kEpi, bool kGather>
-__global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
+template <int BM, bool kFP8, int kEpi, bool kGather, bool kWide>
+__global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_a, const GemmParams p) {
-  using C = Cfg<BM, kFP8, kEpi>;
+  using C = Cfg<BM, kFP8, kEpi, kWide>;
+  static_assert(!(kWide && (kFP8 || C::kSwiglu || kGather)), "wide tiles: BF16 store / scatter");
+  // weight rows of a tile (two weight tiles when wide)
+  constexpr int kWRows = kWide ? 2 * kTileN : kTileN;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_tfull[C::kNumAcc], bar_tempty[C::kNumAcc];
@@ -452,7 +460,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
       const int* rr = s_rows + ds * BM;   // this tile's route ids (gathered rows)
       if (++ds == C::kRing) { ds = 0; dphase ^= 1u; }
       if (d.nkb < 0) break;
-      const int w_row = d.e * p.N + d.n_tile * kTileN;
+      const int w_row = d.e * p.N + d.n_tile * kWRows;
+      const int w_pair = C::kSwiglu ? p.N / 2 : kTileN;  // row offset of the second weight tile
       for (int i = 0; i < d.nkb; i += SK) {
         if (q % nprod == pw) {
           const uint32_t full = smem_u32(&bar_full[stage]);
@@ -470,13 +479,13 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
             if constexpr (!kGather) {
               // one if / else-if chain: the boxes go out from their lanes as one instruction
               if (lane < C::kATiles)
-                tma_load_3d(sa + lane * SK * kATileBytes, &tmap_w, full, 0, w_row + lane * (p.N / 2),
+                tma_load_3d(sa + lane * SK * kATileBytes, &tmap_w, full, 0, w_row + lane * w_pair,
                             kb, pol_w);
               else if (lane == C::kATiles)
                 tma_load_3d(sa + C::kATiles * SK * kATileBytes, &tmap_a, full, 0, d.m0, kb, pol_a);
             } else {
               if (lane < C::kATiles)
-                tma_load_3d(sa + lane * SK * kATileBytes, &tmap_w, full, 0, w_row + lane * (p.N / 2),
+                tma_load_3d(sa + lane * SK * kATileBytes, &tmap_w, full, 0, w_row + lane * w_pair,
                             kb, pol_w);
               // the routed rows, four per copy (SK * BM / 4 copies over the
               // warp's lanes); a K block past the tile's end reloads its last
@@ -578,7 +587,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
               const uint32_t acc = kFP8 ? (kk > 0) : (i > 0 || kb > 0 || kk > 0);
               const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32);
               umma<kFP8>(d_tmem, smem_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
-              if constexpr (C::kSwiglu)
+              if constexpr (C::kPair)
                 umma<kFP8>(d_tmem + BM, smem_desc_sw128(a_addr + SK * kATileBytes + kk * 32), bdesc,
                            idesc, acc);
             }
@@ -651,7 +660,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
       const float* sc = reinterpret_cast<const float*>(s_meta + ds * meta_bytes);
       const int* tok = reinterpret_cast<const int*>(sc + (kFP8 ? p.kb_per_split * BM : 0));
       const float* wt = reinterpret_cast<const float*>(tok + BM);
-      const int col = d.n_tile * kTileN + row;
+      const int col = d.n_tile * kWRows + row;  // output column (of the first weight tile)
 
       if constexpr (kFP8) {
         constexpr int CW = C::kEpiCols;
@@ -833,18 +842,28 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi>::kThreads, 1)
               }
             }
           } else {
+            // wide tiles: the second weight tile's accumulator is BM columns on,
+            // its output columns 128 on
+            float v2[16];
+            if constexpr (kWide) tmem_ld16(lane_addr + buf * C::kAccCols + BM + c0, v2);
             tmem_ld_wait(v);
+            if constexpr (kWide) tmem_ld_wait(v2);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if (s0 + j < d.rows) {
-                const size_t r = static_cast<size_t>(d.m0 + s0 + j);
-                if constexpr (kEpi == MOE_EPI_SCATTER)
-                  red_add_f32(static_cast<float*>(p.out) + static_cast<size_t>(tok[s0 + j]) * p.N + col,
-                              wt[s0 + j] * v[j]);
-                else if constexpr (kEpi == MOE_EPI_STORE_BF16)
-                  static_cast<__nv_bfloat16*>(p.out)[r * p.N + col] = __float2bfloat16_rn(v[j]);
-                else
-                  static_cast<float*>(p.out)[r * p.N + col] = v[j];
+            for (int h = 0; h < (kWide ? 2 : 1); ++h) {
+              const float* vh = h ? v2 : v;
+              const int colh = col + h * kTileN;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if (s0 + j < d.rows) {
+                  const size_t r = static_cast<size_t>(d.m0 + s0 + j);
+                  if constexpr (kEpi == MOE_EPI_SCATTER)
+                    red_add_f32(static_cast<float*>(p.out) + static_cast<size_t>(tok[s0 + j]) * p.N + colh,
+                                wt[s0 + j] * vh[j]);
+                  else if constexpr (kEpi == MOE_EPI_STORE_BF16)
+                    static_cast<__nv_bfloat16*>(p.out)[r * p.N + colh] = __float2bfloat16_rn(vh[j]);
+                  else
+                    static_cast<float*>(p.out)[r * p.N + colh] = vh[j];
+                }
               }
             }
           }
@@ -894,11 +913,20 @@ struct GemmVariant {
   int threads;
 };
 
-template <int BM, bool kFP8, int kEpi, bool kGather>
+template <int BM, bool kFP8, int kEpi, bool kGather, bool kWide = false>
 GemmVariant variant() {
-  using C = Cfg<BM, kFP8, kEpi>;
-  return GemmVariant{reinterpret_cast<const void*>(&grouped_gemm_kernel<BM, kFP8, kEpi, kGather>),
-                     C::kStageBytes, C::kThreads};
+  using C = Cfg<BM, kFP8, kEpi, kWide>;
+  return GemmVariant{
+      reinterpret_cast<const void*>(&grouped_gemm_kernel<BM, kFP8, kEpi, kGather, kWide>),
+      C::kStageBytes, C::kThreads};
+}
+
+// Wide tiles: BF16 store / scatter epilogues, block_m 128 or 256.
+template <int kEpi>
+bool pick_wide(int bm, GemmVariant& v) {
+  if (bm == 128) { v = variant<128, false, kEpi, false, true>(); return true; }
+  if (bm == 256) { v = variant<256, false, kEpi, false, true>(); return true; }
+  return false;
 }
 
 template <bool kFP8, int kEpi, bool kGather>
@@ -918,7 +946,14 @@ bool pick_bm(int bm, GemmVariant& v) {
 
 // Gathered rows are built for the FP8 GEMM (every epilogue) and the BF16
 // gated up projection (the first GEMM of the BF16 forward).
-bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, GemmVariant& v) {
+bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, bool wide, GemmVariant& v) {
+  if (wide) {
+    if (fp8 || gather) return false;
+    if (epi == MOE_EPI_SCATTER) return pick_wide<MOE_EPI_SCATTER>(bm, v);
+    if (epi == MOE_EPI_STORE) return pick_wide<MOE_EPI_STORE>(bm, v);
+    if (epi == MOE_EPI_STORE_BF16) return pick_wide<MOE_EPI_STORE_BF16>(bm, v);
+    return false;
+  }
   if (fp8) {
     if (epi == MOE_EPI_SCATTER)
       return gather ? pick_bm<true, MOE_EPI_SCATTER, true>(bm, v)
@@ -943,9 +978,13 @@ bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, GemmVariant& v)
 
 bool gemm_gather_supported(bool fp8, int epi) { return fp8 || epi == MOE_EPI_SWIGLU; }
 
-int gemm_stage_bytes(bool fp8, int epi, int bm) {
+bool gemm_wide_supported(bool fp8, int epi, int bm) {
+  return !fp8 && epi != MOE_EPI_SWIGLU && (bm == 128 || bm == 256);
+}
+
+int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide) {
   GemmVariant v;
-  if (!select_gemm_variant(fp8, epi, bm, false, v)) return 0;
+  if (!select_gemm_variant(fp8, epi, bm, false, wide, v)) return 0;
   return v.stage_bytes;
 }
 
@@ -961,7 +1000,7 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
                                 const GemmParams& p, bool fp8, int epi, int bm, int num_ctas,
                                 cudaStream_t stream, bool pdl) {
   GemmVariant v;
-  if (!select_gemm_variant(fp8, epi, bm, p.gather != 0, v)) return cudaErrorInvalidValue;
+  if (!select_gemm_variant(fp8, epi, bm, p.gather != 0, p.wide != 0, v)) return cudaErrorInvalidValue;
   if (p.sk != 1 && p.sk != 2 && p.sk != 4) return cudaErrorInvalidValue;
   const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * p.sk * v.stage_bytes +
                       gemm_meta_bytes(fp8, bm, p.kb_per_split) + gemm_table_bytes(p.E) +

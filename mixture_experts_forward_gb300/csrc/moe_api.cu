@@ -188,12 +188,16 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   p.KB = fp8 ? a->K / 128 : a->K / 64;
   p.k_splits = pick_k_splits(a, sms, p.KB);
   p.kb_per_split = (p.KB + p.k_splits - 1) / p.k_splits;
-  p.n_tiles = (a->epilogue == MOE_EPI_SWIGLU ? a->N / 2 : a->N) / 128;
+  // BF16 store / scatter with 128- or 256-row tiles: two adjacent weight
+  // tiles per tile (a stage then carries two MMAs per K block)
+  p.wide = (gemm_wide_supported(fp8, a->epilogue, a->block_m) && a->gather_rows == 0 &&
+            a->N % 256 == 0) ? 1 : 0;
+  p.n_tiles = (a->epilogue == MOE_EPI_SWIGLU ? a->N / 2 : a->N) / (p.wide ? 256 : 128);
   p.sched = a->sched;
   p.w_reuse = 2LL * a->R >= static_cast<long long>(a->block_m) * a->E ? 1 : 0;
   p.drop_producer = g_drop_producer;
   p.timeout_ns = g_timeout_ns;
-  const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m);
+  const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m, p.wide != 0);
   if (stage_bytes <= 0) return MOE_ERR_UNSUPPORTED;
   const int meta_bytes = gemm_meta_bytes(fp8, a->block_m, p.kb_per_split);
   p.gather = a->gather_rows;
