@@ -124,3 +124,30 @@ def test_workspace_size_and_forward_errors(lib):
     assert lib.moe_workspace_size(ctypes.byref(bf)) == 0        # w2 missing
     bf.w2 = FAKE
     assert lib.moe_workspace_size(ctypes.byref(bf)) > 0
+
+
+@pytest.mark.parametrize("cname,pyclass", [("moe_gemm_args", "GemmArgs"),
+                                           ("moe_forward_args", "ForwardArgs")])
+def test_argument_structs_match_the_binding(tmp_path, cname, pyclass):
+    """The ctypes mirrors of the argument structs have the header's size and
+    field offsets (a C program built against include/moe.h prints them)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cls = getattr(L, pyclass)
+    fields = [f[0] for f in cls._fields_]
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe.h"', "int main(void) {",
+             f'  printf("size %zu\\n", sizeof({cname}));']
+    lines += [f'  printf("{f} %zu\\n", offsetof({cname}, {f}));' for f in fields]
+    lines += ["  return 0;", "}"]
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    assert int(out["size"]) == ctypes.sizeof(cls)
+    for f in fields:
+        assert int(out[f]) == getattr(cls, f).offset, f
