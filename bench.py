@@ -399,15 +399,26 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
             "peak_note": note}
 
 
+def code_sha(path: str) -> str:
+    """Hash of a CUDA source's code: comments and whitespace removed, so that
+    editing a comment does not mark a capture of the same kernel as stale."""
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = " ".join(text.split())
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def stored_traffic(src_name: str, kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else null)."""
+    the current kernel code (else null)."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     j = json.load(open(p))
     src = os.path.join(ROOT, "mixture_experts_forward_gb300", "csrc", src_name)
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = code_sha(src)
     e = j.get(kernel)
     if not e or e.get("source_sha") != sha:
         return None

@@ -14,9 +14,11 @@
 // rows of a tile are the MMA's M side and the routed rows (block_m of them,
 // 16..256) are its N side, so a 4-row expert costs a 128x16 MMA instead of a
 // padded 128-row one and the kernel streams each touched weight block once.
-//   warps 0, 7+ TMA producers (two or four), taking stages in turn; warp 0
-//               also runs the tile queue.  A stage holds sk K blocks and each of its 3-D boxes
-//               (weight and activation tiles, sk K blocks deep) has its own lane
+//   warps 0, 7  TMA producers, taking stages in turn; warp 0 also runs the
+//               tile queue.  A stage holds sk K blocks and each of its 3-D
+//               boxes (weight and activation tiles, sk K blocks deep) has its
+//               own lane.  Gathered rows (kGather): the routed rows come as
+//               tile::gather4 copies of four token rows each instead
 //   warp 1      one thread issues tcgen05.mma into TMEM, commits to mbarriers;
 //               the warp owns the TMEM allocation
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (thread = weight row),
@@ -24,8 +26,13 @@
 //               registers ("promotion"; each K block has its own TMEM buffer;
 //               packed f32x2 multiply-adds), then weighted red.global.add into
 //               the fp32 output, a plain store, or silu(gate)*up to bf16.
-//               FP8 tiles of 64+ routed rows add warps 8..11: two warps per
-//               TMEM lane quadrant, each promoting half of the tile's columns
+//               More epilogue warps per TMEM lane quadrant, each taking a share
+//               of the tile's columns: two (warps 8..11 too) for FP8 tiles of
+//               64+ routed rows and BF16 tiles of 128, four (8..19) for BF16
+//               tiles of 256
+// A stage carries one weight tile, or two (the gate and up rows of the SwiGLU
+// up projection; two adjacent weight tiles of a BF16 "wide" tile) that share
+// the routed-row operand, so two MMAs per K block come from one stage.
 //   warp 6      tile metadata: routed-row tokens, route weights and the FP8
 //               scale products of each tile, staged into a shared ring ahead
 //               of the epilogue (loads issued in dependency order, about
