@@ -235,9 +235,18 @@ def test_gemm_bf16(bm, epi):
     _bf16_gemm_case(R_tokens=200, K=320, N=256, E=8, k=2, bm=bm, epilogue=epi)
 
 
-def test_gemm_bf16_static_schedule():
-    _bf16_gemm_case(R_tokens=300, K=256, N=512, E=3, k=2, bm=64, epilogue=L.EPI_SCATTER,
+@pytest.mark.parametrize("bm", [64, 256])
+def test_gemm_bf16_static_schedule(bm):
+    """Static per-expert partition; block_m 256 with N % 256 == 0 runs wide tiles."""
+    _bf16_gemm_case(R_tokens=300, K=256, N=512, E=3, k=2, bm=bm, epilogue=L.EPI_SCATTER,
                     sched=L.SCHED_STATIC)
+
+
+@pytest.mark.parametrize("bm", [128, 256])
+@pytest.mark.parametrize("epi", [L.EPI_SCATTER, L.EPI_STORE_BF16])
+def test_gemm_bf16_narrow_tiles_when_n_is_odd_multiple_of_128(bm, epi):
+    """N = 384 is not a multiple of 256: one weight tile per tile (no wide tiles)."""
+    _bf16_gemm_case(R_tokens=180, K=192, N=384, E=4, k=2, bm=bm, epilogue=epi)
 
 
 def _gather_gemm_fp8_case(M, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, k_splits=0, seed=0,
