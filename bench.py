@@ -267,7 +267,7 @@ def bench_ours(args, rank, world, local):
     pk = peaks()
 
     roof = dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, flush,
-                           touched, pk)
+                           touched, pk, cfg_name=args.config)
     if kind == "fp8":
         alg_bytes = touched * (N * K + (N // 128) * (K // 128) * 4) + M * E * 4 + M * K * 2 + M * N * 2
         t_roof = max(fl / (2 * pk["bf16"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
@@ -309,7 +309,8 @@ def bench_ours(args, rank, world, local):
         print(json.dumps(res), flush=True)
 
 
-def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, flush, touched, pk):
+def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, flush, touched, pk,
+                    cfg_name=""):
     """Time the grouped GEMM alone (same inputs and tiling as the forward) with
     CUDA events on its stream and report it against its roofline."""
     stream = torch.cuda.current_stream(dev)
@@ -382,7 +383,7 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
     avg_s = statistics.median(g - f for g, f in spans) / n
     t_hbm = alg / (pk["hbm"] * 1e9)
     t_tc = fl / ((2 if kind == "fp8" else 1) * pk["bf16"] * 1e12)
-    traffic = stored_traffic(src, name)
+    traffic = stored_traffic(src, name, cfg_name)
     if t_hbm >= t_tc:
         achieved = alg / avg_s / 1e9
         return {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1),
@@ -410,9 +411,9 @@ def code_sha(path: str) -> str:
     return hashlib.sha256(text.encode()).hexdigest()[:16]
 
 
-def stored_traffic(src_name: str, kernel: str):
+def stored_traffic(src_name: str, kernel: str, config_name: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel code (else null)."""
+    this workload and the current kernel code (else null)."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
@@ -420,7 +421,7 @@ def stored_traffic(src_name: str, kernel: str):
     src = os.path.join(ROOT, "mixture_experts_forward_gb300", "csrc", src_name)
     sha = code_sha(src)
     e = j.get(kernel)
-    if not e or e.get("source_sha") != sha:
+    if not e or e.get("source_sha") != sha or e.get("config") != config_name:
         return None
     return e.get("dram_bytes_per_launch")
 
