@@ -94,6 +94,54 @@ def test_gemm_argument_errors(lib, kw, code):
     assert lib.moe_grouped_gemm(ctypes.byref(g), ctypes.c_void_p(FAKE), 4096, None) == code
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(gather_rows=2), L.MOE_ERR_INVALID_ARG), (dict(gather_rows=-1), L.MOE_ERR_INVALID_ARG),
+    (dict(gather_rows=1, sorted_route_ids=None), L.MOE_ERR_INVALID_ARG),
+    (dict(gather_rows=1, epilogue=L.EPI_STORE, M=0), L.MOE_ERR_INVALID_ARG),
+    (dict(gather_rows=1, epilogue=L.EPI_STORE, M=15), L.MOE_ERR_INVALID_ARG),
+    (dict(gather_rows=1, dtype=L.DTYPE_BF16, a_scales=None, w_scales=None),
+     L.MOE_ERR_UNSUPPORTED),
+    (dict(gather_rows=1, dtype=L.DTYPE_BF16, epilogue=L.EPI_STORE_BF16, a_scales=None,
+          w_scales=None), L.MOE_ERR_UNSUPPORTED),
+])
+def test_gemm_gather_rows_argument_errors(lib, kw, code):
+    """Gathered rows need the route ids and R = M * top_k (slot s reads token
+    row ids[s] // top_k); BF16 gathers only in the gated up projection."""
+    g = _gemm(**kw)
+    assert lib.moe_grouped_gemm(ctypes.byref(g), ctypes.c_void_p(FAKE), 4096, None) == code
+
+
+def _fwd(**kw):
+    a = L.forward_args(**kw)
+    a.w = FAKE
+    a.w_scales = FAKE
+    a.w2 = FAKE
+    return a
+
+
+def test_forward_gather_rows_workspace(lib):
+    """With gathered rows the forward keeps one token-major copy of the
+    activations ([M, K] FP8 codes and [K/128, M] scales) in place of the
+    expert-compact [R, K] one; BF16 reads x directly and keeps no copy.
+    Small FP8 batches (the fused quantise + layout path) ignore the flag."""
+    big = dict(M=4096, K=2048, N=512, E=256, top_k=8)
+    M, K, R = big["M"], big["K"], big["M"] * big["top_k"]
+    plain = L.workspace_size(_fwd(dtype=L.DTYPE_FP8, **big))
+    gath = L.workspace_size(_fwd(dtype=L.DTYPE_FP8, gather_rows=1, **big))
+    saved = (R - M) * (K + (K // 128) * 4)
+    assert abs((plain - gath) - saved) <= 512          # two 256-byte alignments
+    bf = dict(M=4096, K=2048, N=1024, E=64, top_k=8)
+    plain = L.workspace_size(_fwd(dtype=L.DTYPE_BF16, **bf))
+    gath = L.workspace_size(_fwd(dtype=L.DTYPE_BF16, gather_rows=1, **bf))
+    assert abs((plain - gath) - bf["M"] * bf["top_k"] * bf["K"] * 2) <= 256
+    small = dict(M=128, K=2048, N=512, E=256, top_k=8)
+    assert (L.workspace_size(_fwd(dtype=L.DTYPE_FP8, gather_rows=1, **small)) ==
+            L.workspace_size(_fwd(dtype=L.DTYPE_FP8, **small)))
+    for bad in (2, -1):
+        assert lib.moe_workspace_size(ctypes.byref(_fwd(dtype=L.DTYPE_FP8, gather_rows=bad,
+                                                        **big))) == 0
+
+
 def test_gemm_workspace_errors(lib):
     g = _gemm()
     assert lib.moe_grouped_gemm(ctypes.byref(g), None, 4096, None) == L.MOE_ERR_WORKSPACE
