@@ -13,7 +13,10 @@ each step follows:
   section 4 (compact routed rows) and the config-tuning benchmark design
   (gated up projection + down projection);
 * the blog retelling of "Weave" — section 4.3 (histogram, prefix, per-expert
-  tiles).
+  tiles);
+* the FP8 gated FFN (gate+up projection, SiLU, down projection: the closing
+  "Reference: vLLM full MLP" section of the Fused MoE FP8 page and the H200
+  page's config-tuning section 3), with h re-quantised by the 1x128 rule.
 
 Parity status: every function is pinned by a ``-m "not gpu"`` test
 (brute force, closed forms, libm, torch's float8 cast); none is "parity
@@ -77,6 +80,10 @@ def lib():
                                          P, P, P, P, P, P, P, P, P, P]
         L.oracle_dense_fp8.argtypes = [P, P, P, P, P, i, i, i, i, i, P, i, i, P]
         L.oracle_ffn_bf16.argtypes = [P, P, P, P, P, i, i, i, i, i, P, i, i, P]
+        L.oracle_swiglu_f32.argtypes = [f, f]
+        L.oracle_swiglu_f32.restype = f
+        L.oracle_swiglu_quant.argtypes = [P, i, i, P, P]
+        L.oracle_ffn_fp8.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, P, i, i, P]
         _lib = L
     return _lib
 
@@ -262,4 +269,42 @@ def ffn_bf16(x_bf16_bits, ids, weights, w_up_bits, w_dn_bits, tokens=None, threa
     out = np.zeros((n, H), np.float64)
     lib().oracle_ffn_bf16(_p(x), _p(ids), _p(weights), _p(w_up), _p(w_dn), T, H, I, E, k,
                           _p(tok), n, int(threads), _p(out))
+    return out
+
+
+# ----------------------------------------------------------------- FP8 gated FFN
+def swiglu_f32(g: float, u: float) -> float:
+    return lib().oracle_swiglu_f32(g, u)
+
+
+def swiglu_quant(gu: np.ndarray):
+    """gu f32 [R, 2I] (gate columns, then up columns) -> (h_q u8 [R, I],
+    h_scales f32 [I/128, R])."""
+    gu = _c(gu, np.float32)
+    R, I2 = gu.shape
+    I = I2 // 2
+    h_q = np.zeros((R, I), np.uint8)
+    h_s = np.zeros((I // 128, R), np.float32)
+    lib().oracle_swiglu_quant(_p(gu), R, I, _p(h_q), _p(h_s))
+    return h_q, h_s
+
+
+def ffn_fp8(x_bf16_bits, ids, weights, wup_q, wup_s, wdn_q, wdn_s, tokens=None, threads=1):
+    """Token-major FP8 gated FFN; binary64 output rows of ``tokens`` (all when None)."""
+    x = _c(x_bf16_bits, np.uint16)
+    ids = _c(ids, np.int32)
+    weights = _c(weights, np.float32)
+    wup_q = _c(wup_q, np.uint8)
+    wup_s = _c(wup_s, np.float32)
+    wdn_q = _c(wdn_q, np.uint8)
+    wdn_s = _c(wdn_s, np.float32)
+    T, H = x.shape
+    E, I2, _ = wup_q.shape
+    I = I2 // 2
+    k = ids.shape[1]
+    tok = None if tokens is None else _c(tokens, np.int32)
+    n = T if tok is None else len(tok)
+    out = np.zeros((n, H), np.float64)
+    lib().oracle_ffn_fp8(_p(x), _p(ids), _p(weights), _p(wup_q), _p(wup_s), _p(wdn_q), _p(wdn_s),
+                         T, H, I, E, k, _p(tok), n, int(threads), _p(out))
     return out

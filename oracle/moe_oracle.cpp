@@ -203,10 +203,13 @@ int oracle_layout(const int32_t* ids, int M, int E, int k, int block_m,
   return 0;
 }
 
-static void quantize_row(const uint16_t* xrow, int K, uint8_t* q, float* scales) {
+// The 1x128 block rule of "Baseline: 7 kernels" item 4 on a binary32 row:
+// amax = max |v|, s = amax / 448, q = E4M3(v * (1/s)); amax = 0 gives s = 0
+// and all-zero codes.
+static void quantize_f32_row(const float* v, int K, uint8_t* q, float* scales) {
   for (int b = 0; b < K / 128; ++b) {
     float amax = 0.0f;
-    for (int i = 0; i < 128; ++i) amax = std::max(amax, std::fabs(bf16_to_f32(xrow[b * 128 + i])));
+    for (int i = 0; i < 128; ++i) amax = std::max(amax, std::fabs(v[b * 128 + i]));
     if (amax == 0.0f) {
       scales[b] = 0.0f;
       for (int i = 0; i < 128; ++i) q[b * 128 + i] = 0;
@@ -215,8 +218,15 @@ static void quantize_row(const uint16_t* xrow, int K, uint8_t* q, float* scales)
     float s = amax / 448.0f;
     float inv = 1.0f / s;
     scales[b] = s;
-    for (int i = 0; i < 128; ++i) q[b * 128 + i] = oracle_e4m3_encode(bf16_to_f32(xrow[b * 128 + i]) * inv);
+    for (int i = 0; i < 128; ++i) q[b * 128 + i] = oracle_e4m3_encode(v[b * 128 + i] * inv);
   }
+}
+
+// bf16 rows widen to binary32 exactly, then the same rule.
+static void quantize_row(const uint16_t* xrow, int K, uint8_t* q, float* scales) {
+  std::vector<float> v(K);
+  for (int i = 0; i < K; ++i) v[i] = bf16_to_f32(xrow[i]);
+  quantize_f32_row(v.data(), K, q, scales);
 }
 
 void oracle_quant_gather(const uint16_t* x_bf16, int M, int K, int k,
@@ -356,6 +366,70 @@ void oracle_ffn_bf16(const uint16_t* x_bf16, const int32_t* ids, const float* we
         const uint16_t* wd = w_dn + ((size_t)e * H + n) * I;
         double y = 0.0;
         for (int r = 0; r < I; ++r) y += h[r] * double(bf16_to_f32(wd[r]));
+        acc[n] += w * y;
+      }
+    }
+    for (int n = 0; n < H; ++n) out[(size_t)i * H + n] = acc[n];
+  });
+}
+
+float oracle_swiglu_f32(float g, float u) {
+  float e = oracle_exp_spec(-g);   // exp(-g): 0 below -87, +inf above 88
+  float d = 1.0f + e;
+  float sg = g / d;                // silu(g); g / inf = -0 for very negative g
+  return sg * u;
+}
+
+void oracle_swiglu_quant(const float* gu, int R, int I, uint8_t* h_q, float* h_scales) {
+  const int IB = I / 128;
+  std::vector<float> h(I), sc(IB);
+  for (int s = 0; s < R; ++s) {
+    const float* row = gu + (size_t)s * 2 * I;
+    for (int r = 0; r < I; ++r) h[r] = oracle_swiglu_f32(row[r], row[I + r]);
+    quantize_f32_row(h.data(), I, h_q + (size_t)s * I, sc.data());
+    for (int b = 0; b < IB; ++b) h_scales[(size_t)b * R + s] = sc[b];
+  }
+}
+
+void oracle_ffn_fp8(const uint16_t* x_bf16, const int32_t* ids, const float* weights,
+                    const uint8_t* wup_q, const float* wup_s, const uint8_t* wdn_q,
+                    const float* wdn_s, int T, int H, int I, int E, int k,
+                    const int32_t* tokens, int n_tokens, int threads, double* out) {
+  (void)T; (void)E;
+  const int HB = H / 128, IB = I / 128, UB = 2 * I / 128;
+  double dq[256];
+  for (int c = 0; c < 256; ++c) dq[c] = oracle_e4m3_decode(uint8_t(c));
+  parallel_for(n_tokens, threads, [&](int i) {
+    int t = tokens ? tokens[i] : i;
+    std::vector<uint8_t> q(H), qh(I);
+    std::vector<float> sa(HB), sh(IB), gu(2 * I);
+    std::vector<double> acc(H, 0.0);
+    quantize_row(x_bf16 + (size_t)t * H, H, q.data(), sa.data());
+    for (int j = 0; j < k; ++j) {
+      int e = ids[t * k + j];
+      // up projection: gate rows [0, I), up rows [I, 2I); binary64, then
+      // rounded to the binary32 the GEMM accumulates in
+      for (int r = 0; r < 2 * I; ++r) {
+        const uint8_t* w = wup_q + ((size_t)e * 2 * I + r) * H;
+        double y = 0.0;
+        for (int b = 0; b < HB; ++b) {
+          double blk = 0.0;
+          for (int c = b * 128; c < b * 128 + 128; ++c) blk += dq[q[c]] * dq[w[c]];
+          y += double(sa[b]) * double(wup_s[((size_t)e * UB + r / 128) * HB + b]) * blk;
+        }
+        gu[r] = float(y);
+      }
+      // h = silu(gate) * up, re-quantised in 1x128 blocks for the FP8 down projection
+      oracle_swiglu_quant(gu.data(), 1, I, qh.data(), sh.data());
+      double w = weights[t * k + j];
+      for (int n = 0; n < H; ++n) {
+        const uint8_t* wd = wdn_q + ((size_t)e * H + n) * I;
+        double y = 0.0;
+        for (int b = 0; b < IB; ++b) {
+          double blk = 0.0;
+          for (int c = b * 128; c < b * 128 + 128; ++c) blk += dq[qh[c]] * dq[wd[c]];
+          y += double(sh[b]) * double(wdn_s[((size_t)e * HB + n / 128) * IB + b]) * blk;
+        }
         acc[n] += w * y;
       }
     }

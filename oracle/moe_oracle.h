@@ -143,6 +143,39 @@ void oracle_ffn_bf16(const uint16_t* x_bf16, const int32_t* ids, const float* we
                      int T, int H, int I, int E, int k,
                      const int32_t* tokens, int n_tokens, int threads, double* out);
 
+/* --- FP8 gated FFN: the two-layer expert MLP (gate+up projection, SiLU,
+ * down projection) that "Fused MoE FP8" compares against in its closing
+ * section "Reference: vLLM full MLP", in the shape of [P2]'s config-tuning
+ * section 3, with both projections in the FP8 format of [P1] "Baseline"
+ * item 6.  The pages do not say how h enters an FP8 GEMM; the reading taken
+ * is the plainest one the rest supports: h gets the same 1x128 amax/448 rule
+ * as the activations (item 4), decided in binary32, the precision the up
+ * projection accumulates in. --- */
+
+/* silu(g) * u in binary32 operations: e = exp_spec(-g), d = 1 + e,
+ * silu = g / d, result = silu * u. */
+float oracle_swiglu_f32(float g, float u);
+
+/* For every row s of gu (f32 [R, 2I]: gate columns [0,I), up columns
+ * [I,2I)): h[r] = oracle_swiglu_f32(gu[s,r], gu[s,I+r]), then the 1x128 rule
+ * of [P1] item 4 on h: h_q u8 [R, I], h_scales f32 [I/128, R] (block-major,
+ * like a_scales).  I a multiple of 128. */
+void oracle_swiglu_quant(const float* gu, int R, int I, uint8_t* h_q, float* h_scales);
+
+/* Token-major FP8 gated FFN.  x bf16 [T,H] is quantised per token (item 4);
+ * for each of the token's routes j (expert e):
+ *   gu[r] = binary32( sum_b sa[b] wup_s[e,r/128,b] sum_{c in b} dq(q[c]) dq(wup_q[e,r,c]) ),
+ *           r in [0, 2I) (rows [0,I) gate, [I,2I) up; the sum in binary64),
+ *   (qh, sh) = oracle_swiglu_quant(gu),
+ *   y[n] = sum_b sh[b] wdn_s[e,n/128,b] sum_{c in b} dq(qh[c]) dq(wdn_q[e,n,c])  (binary64),
+ * and out[t] = sum_j w[t,j] y_j (binary64, j ascending).
+ * wup_q u8 [E,2I,H], wup_s f32 [E,2I/128,H/128]; wdn_q u8 [E,H,I],
+ * wdn_s f32 [E,H/128,I/128]; H and I multiples of 128. */
+void oracle_ffn_fp8(const uint16_t* x_bf16, const int32_t* ids, const float* weights,
+                    const uint8_t* wup_q, const float* wup_s, const uint8_t* wdn_q,
+                    const float* wdn_s, int T, int H, int I, int E, int k,
+                    const int32_t* tokens, int n_tokens, int threads, double* out);
+
 #ifdef __cplusplus
 }
 #endif
