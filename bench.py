@@ -72,9 +72,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="qwen_small_batch_fp8",
-                    choices=list(inputs.FP8_CONFIGS) + list(inputs.BF16_CONFIGS))
+                    choices=list(inputs.FP8_CONFIGS) + list(inputs.BF16_CONFIGS)
+                    + list(inputs.FFN_FP8_CONFIGS))
     ap.add_argument("--routing", default=None,
-                    help="BF16 routing: balanced | uniform | zipf1.2 | loads "
+                    help="gated-FFN routing: balanced | uniform | zipf1.2 | loads "
                          "(default: loads for imbalance_bf16, else uniform)")
     ap.add_argument("--rho", type=float, default=None,
                     help="max/min expert load for --routing loads (default 40)")
@@ -123,6 +124,13 @@ def workload(cfg_name, args, seed):
         desc = (f"{cfg_name} M={c['M']} K={c['K']} N={c['N']} E={c['E']} top{c['k']} "
                 f"softcap={c['softcap']:g} fp8-e4m3 128x128/1x128 blocks")
         return "fp8", d, desc
+    if cfg_name in inputs.FFN_FP8_CONFIGS:
+        routing = args.routing or "uniform"
+        d = inputs.make_fp8_ffn_inputs(cfg_name, routing=routing, seed=seed)
+        c = d["cfg"]
+        desc = (f"{cfg_name} T={c['T']} H={c['H']} I={c['I']} E={c['E']} top{c['k']} "
+                f"routing={routing} fp8-e4m3 gated FFN (h re-quantised 1x128)")
+        return "fp8ffn", d, desc
     routing = args.routing or ("loads" if cfg_name == "imbalance_bf16" else "uniform")
     rho = args.rho if args.rho is not None else (40.0 if routing == "loads" else 1.0)
     d = inputs.make_bf16_inputs(cfg_name, routing=routing, rho=rho, seed=seed)
@@ -214,6 +222,16 @@ def bench_ours(args, rank, world, local):
                             logits=logits, x=x, w=w, w_scales=ws_, block_m=args.block_m,
                             sched=sched, k_splits=args.k_splits, use_graph=1)
         out_cols = N
+    elif kind == "fp8ffn":
+        logits, x = d["logits"].to(dev), d["x"].to(dev)
+        wu, wus = d["wup_q"].to(dev), d["wup_s"].to(dev)
+        wd, wds = d["wdn_q"].to(dev), d["wdn_s"].to(dev)
+        M, K, N, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
+        fa = L.forward_args(dtype=L.DTYPE_FP8, gated=1, M=M, K=K, N=N, E=E, top_k=k, softcap=0.0,
+                            logits=logits, x=x, w=wu, w_scales=wus, w2=wd, w2_scales=wds,
+                            block_m=args.block_m, sched=sched, k_splits=args.k_splits,
+                            use_graph=1)
+        out_cols = K
     else:
         logits, x = d["logits"].to(dev), d["x"].to(dev)
         w, w2 = d["w_up"].to(dev), d["w_dn"].to(dev)
@@ -257,7 +275,8 @@ def bench_ours(args, rank, world, local):
     fl = flops_per_step(kind, c)
     value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
     ms_per_step = total_ms / args.steps
-    launches_per_step = 4 if kind == "fp8" else 5   # route+layout, quant/gather, GEMM(s), finalize
+    # route+layout, quant/gather, GEMM(s), (FP8 FFN: SwiGLU + re-quantise), finalize
+    launches_per_step = {"fp8": 4, "bf16": 5, "fp8ffn": 6}[kind]
 
     # routing facts of this batch (for bytes and the roofline)
     ids, _ = L.route(logits, k, softcap=c.get("softcap", 0.0))
@@ -270,6 +289,11 @@ def bench_ours(args, rank, world, local):
                            touched, pk, cfg_name=args.config)
     if kind == "fp8":
         alg_bytes = touched * (N * K + (N // 128) * (K // 128) * 4) + M * E * 4 + M * K * 2 + M * N * 2
+        t_roof = max(fl / (2 * pk["bf16"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
+    elif kind == "fp8ffn":
+        # both projections' codes and block scales of every touched expert
+        w_bytes = 3 * N * K + ((2 * N // 128) * (K // 128) + (K // 128) * (N // 128)) * 4
+        alg_bytes = touched * w_bytes + M * E * 4 + M * K * 2 + M * K * 2
         t_roof = max(fl / (2 * pk["bf16"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
     else:
         alg_bytes = touched * (2 * N * K + K * N) * 2 + M * E * 4 + M * K * 2 + M * K * 2
@@ -290,12 +314,12 @@ def bench_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "us_per_forward": round(ms_per_step * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8_e4m3" if kind == "fp8" else "bf16", "data": "synthetic (seeded)",
+        "dtype": "bf16" if kind == "bf16" else "fp8_e4m3", "data": "synthetic (seeded)",
         "config": {"workload": desc, "l2": "flushed between steps (256 MiB write, then 256 MiB read)",
                    "block_m": block_m, "k_splits": k_splits, "sched": args.sched,
                    "touched_experts": touched, "compact_rows": int(M * k),
                    "parallelism": f"replicas x{world} (token data-parallel, no collective)"},
-        "forward_roofline": {"bound": "hbm" if kind == "fp8" and t_roof == alg_bytes / (pk["hbm"] * 1e9) else "tensor",
+        "forward_roofline": {"bound": "hbm" if t_roof == alg_bytes / (pk["hbm"] * 1e9) else "tensor",
                              "alg_bytes": int(alg_bytes), "roofline_us": round(t_roof * 1e6, 3),
                              "frac": round(fwd_roof_frac, 4), "peak_source": pk["src"]},
         "roofline": roof,
@@ -338,6 +362,24 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
         alg = touched * (N * K + (N // 128) * (K // 128) * 4) + R * K + (K // 128) * R * 4 + out_bytes
         fl = 2.0 * R * N * K
         name = "grouped_gemm_kernel<fp8, scatter>" if small else "grouped_gemm_kernel<fp8, store_bf16>"
+        src = "grouped_gemm.cu"
+    elif kind == "fp8ffn":
+        # the forward's largest kernel: the FP8 up projection (gate and up
+        # rows) storing f32 rows for the SwiGLU + re-quantisation step
+        T, H, I, k = c["T"], c["H"], c["I"], c["k"]
+        R = T * k
+        a_q, a_s = L.quant_gather(d["x"].to(dev), k, lay["route_slot"])
+        w, w_s = d["wup_q"].to(dev), d["wup_s"].to(dev)
+        gu = torch.empty(R, 2 * I, dtype=torch.float32, device=dev)
+
+        def launch():
+            L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_STORE, a=a_q, a_scales=a_s, w=w,
+                           w_scales=w_s, offsets=lay["offsets"], tile_offsets=lay["tile_offsets"],
+                           out=gu, ws=ws, block_m=block_m, M=T, top_k=k, sched=sched, k_splits=1)
+        alg = touched * (2 * I * H + (2 * I // 128) * (H // 128) * 4) + R * H + (H // 128) * R * 4 \
+            + R * 2 * I * 4
+        fl = 2.0 * R * (2 * I) * H
+        name = "grouped_gemm_kernel<fp8, store>"
         src = "grouped_gemm.cu"
     else:
         # the forward's largest kernel: the gated up-projection with the SwiGLU
@@ -382,7 +424,8 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
     assert L.get_error(ws) == L.MOE_OK
     avg_s = statistics.median(g - f for g, f in spans) / n
     t_hbm = alg / (pk["hbm"] * 1e9)
-    t_tc = fl / ((2 if kind == "fp8" else 1) * pk["bf16"] * 1e12)
+    fp8 = kind in ("fp8", "fp8ffn")
+    t_tc = fl / ((2 if fp8 else 1) * pk["bf16"] * 1e12)
     traffic = stored_traffic(src, name, cfg_name)
     if t_hbm >= t_tc:
         achieved = alg / avg_s / 1e9
@@ -392,8 +435,8 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
                 "avg_launch_us": round(avg_s * 1e6, 3),
                 "peak_note": f"{pk['src']} copy bandwidth (burst)"}
     achieved = fl / avg_s / 1e12
-    peak = 2 * pk["bf16"] if kind == "fp8" else pk["bf16"]
-    note = f"fp8 = 2 x {pk['src']} bf16 burst" if kind == "fp8" else f"{pk['src']} bf16 burst"
+    peak = 2 * pk["bf16"] if fp8 else pk["bf16"]
+    note = f"fp8 = 2 x {pk['src']} bf16 burst" if fp8 else f"{pk['src']} bf16 burst"
     return {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
             "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
             "flops_per_launch": fl, "avg_launch_us": round(avg_s * 1e6, 3),
@@ -472,8 +515,12 @@ def oracle_step(kind, d, c, tokens, threads):
                            threads=threads)
         return 2.0 * len(tokens) * c["k"] * c["N"] * c["K"]
     ids, w = oracle.route(d["logits"].numpy(), c["k"])
-    oracle.ffn_bf16(inputs.bf16_bits(d["x"]), ids, w, inputs.bf16_bits(d["w_up"]),
-                    inputs.bf16_bits(d["w_dn"]), tokens=tokens, threads=threads)
+    if kind == "fp8ffn":
+        oracle.ffn_fp8(inputs.bf16_bits(d["x"]), ids, w, d["wup_q"].numpy(), d["wup_s"].numpy(),
+                       d["wdn_q"].numpy(), d["wdn_s"].numpy(), tokens=tokens, threads=threads)
+    else:
+        oracle.ffn_bf16(inputs.bf16_bits(d["x"]), ids, w, inputs.bf16_bits(d["w_up"]),
+                        inputs.bf16_bits(d["w_dn"]), tokens=tokens, threads=threads)
     R = len(tokens) * c["k"]
     return 2.0 * R * 2 * c["I"] * c["H"] + 2.0 * R * c["H"] * c["I"]
 

@@ -172,14 +172,32 @@ moe_status_t moe_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_byt
 moe_status_t moe_scatter(const float* rows, const int32_t* route_slot, const float* weights,
                          int M, int N, int top_k, void* out, void* stream);
 
+/* SwiGLU + re-quantisation between the projections of the FP8 gated FFN (the
+ * two-layer expert MLP — gate+up projection, SiLU, down projection — of "Fused
+ * MoE FP8" section "Reference: vLLM full MLP", both projections FP8 as in
+ * "Baseline: 7 kernels" item 6).  For every row s of gu (f32 [R, 2I], the up
+ * projection's output: gate columns [0,I), up columns [I,2I)):
+ *   h[r] = (g / (1 + exp(-g))) * u  with g = gu[s,r], u = gu[s,I+r], in IEEE
+ *          binary32 operations (exp by the router's fixed Cody-Waite sequence),
+ * then the 1x128 rule of item 4 on h: amax = max |h|, s = amax / 448,
+ * h_q = E4M3_rne_satfinite(h * (1/s)) (amax = 0: s = 0, codes 0).
+ * h_q: u8 [R, I]; h_scales: f32 [I/128, R] (block-major, the layout the FP8
+ * grouped GEMM reads as a_scales).  I a multiple of 128, else
+ * MOE_ERR_UNSUPPORTED; gu and h_q 16-byte aligned, h_scales 4-byte aligned, R > 0, else
+ * MOE_ERR_INVALID_ARG.  Device pointers, caller-owned; async on `stream`. */
+moe_status_t moe_swiglu_quant(const float* gu, int R, int I, uint8_t* h_q, float* h_scales,
+                              void* stream);
+
 /* Arguments of the fused forward. */
 typedef struct {
-  moe_dtype_t dtype;      /* FP8_E4M3: one grouped GEMM [E,N,K] with block scales;
+  moe_dtype_t dtype;      /* FP8_E4M3: one grouped GEMM [E,N,K] with block scales (or,
+                             with gated = 1, the FP8 gated FFN);
                              BF16: gated FFN, up [E,2N,K] + SwiGLU, down [E,K,N] */
   int M;                  /* tokens */
   int K;                  /* token feature size (the GEMM's contraction size;
                              for BF16 also the output size) */
-  int N;                  /* FP8: output size; BF16: FFN intermediate size I */
+  int N;                  /* FP8: output size; gated FFN (BF16, or FP8 with gated = 1):
+                             intermediate size I */
   int E, top_k;
   float softcap;          /* 0 = off */
   int renorm;             /* 1 = softmax over the selected top_k (default) */
@@ -200,6 +218,13 @@ typedef struct {
                              no [R, K] copy (FP8 keeps one token-major [M, K] code matrix).
                              0 (default) = write the compact copy, which is faster on
                              GB300 at the benchmark shapes; same results either way */
+  int gated;              /* FP8_E4M3: 1 = gated FFN in FP8 — w = e4m3 w_up [E,2N,K] (gate
+                             rows, then up rows) with w_scales [E,2N/128,K/128]; w2 = e4m3
+                             w_down [E,K,N] with w2_scales [E,K/128,N/128]; h =
+                             silu(gate)*up re-quantised as by moe_swiglu_quant between the
+                             projections; output [M,K].  0 = the single FP8 GEMM.  BF16:
+                             must be 0 or 1 (its forward is always the gated FFN) */
+  const float* w2_scales; /* FP8 with gated = 1: [E,K/128,N/128] */
 } moe_forward_args;
 
 /* Workspace bytes needed by moe_forward / moe_forward_host for these
@@ -209,17 +234,21 @@ size_t moe_workspace_size(const moe_forward_args* args);
 /* The tile rows (block_m) and FP8 K split that moe_forward uses for these
  * arguments, so a caller can reproduce its grouped GEMM with
  * moe_grouped_gemm (k_splits is 1 on the BF16 path and whenever the forward
- * stores bf16 rows instead of scatter-adding). */
+ * stores bf16 rows instead of scatter-adding; for the FP8 gated FFN it is the
+ * down projection's split, the up projection storing with one split). */
 moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k_splits);
 
 /* Fused forward: route -> layout -> quantise+gather (FP8) or gather (BF16)
- * -> grouped GEMM(s) -> weighted scatter -> bf16 output.  While the fp32
+ * -> grouped GEMM(s) -> weighted scatter -> bf16 output.  The FP8 gated FFN
+ * (gated = 1) runs the up projection storing f32 rows [R, 2N], then
+ * moe_swiglu_quant's step into codes [R, N] and scales [N/128, R], then the
+ * FP8 down projection.  While the fp32
  * output accumulator (M x out x 4 bytes) is at most 112 MiB the weighted
  * scatter is fused into the last GEMM's epilogue (fp32 reductions into the
  * accumulator, then one bf16 rounding); above that the GEMM stores each
  * routed row in bf16 and a reduction kernel sums each token's top_k rows
  * with the route weights in fp32 (in route order) before the bf16 rounding.
- * out: bf16 [M, N] (FP8) or [M, K] (BF16).  ws: device workspace of
+ * out: bf16 [M, N] (single FP8 GEMM) or [M, K] (gated FFN).  ws: device workspace of
  * moe_workspace_size() bytes, 256-byte aligned, control block zeroed once.
  * With use_graph = 1 the launch sequence is captured (on a private stream) on
  * first use for this argument set, pointers included, and the graph is

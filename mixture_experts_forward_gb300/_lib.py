@@ -23,7 +23,7 @@ CTRL_BYTES = 256
 EXPORTS = ["moe_status_string", "moe_num_sms", "moe_route", "moe_layout", "moe_quant_gather",
            "moe_grouped_gemm", "moe_scatter", "moe_workspace_size", "moe_forward",
            "moe_forward_host", "moe_get_error", "moe_debug_set_pipeline_fault", "moe_forward_plan",
-           "moe_last_cuda_error", "moe_grouped_gemm_noalloc"]
+           "moe_last_cuda_error", "moe_grouped_gemm_noalloc", "moe_swiglu_quant"]
 
 
 class MoeError(RuntimeError):
@@ -54,7 +54,8 @@ class ForwardArgs(ctypes.Structure):
                 ("logits", ctypes.c_void_p), ("x", ctypes.c_void_p), ("w", ctypes.c_void_p),
                 ("w_scales", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("block_m", ctypes.c_int), ("sched", ctypes.c_int), ("k_splits", ctypes.c_int),
-                ("use_graph", ctypes.c_int), ("gather_rows", ctypes.c_int)]
+                ("use_graph", ctypes.c_int), ("gather_rows", ctypes.c_int),
+                ("gated", ctypes.c_int), ("w2_scales", ctypes.c_void_p)]
 
 
 _lib = None
@@ -79,6 +80,7 @@ def lib():
         L.moe_grouped_gemm.argtypes = [ctypes.POINTER(GemmArgs), P, ctypes.c_size_t, P]
         L.moe_grouped_gemm_noalloc.argtypes = [ctypes.POINTER(GemmArgs), P]
         L.moe_scatter.argtypes = [P, P, P, I, I, I, P, P]
+        L.moe_swiglu_quant.argtypes = [P, I, I, P, P, P]
         L.moe_workspace_size.argtypes = [ctypes.POINTER(ForwardArgs)]
         L.moe_workspace_size.restype = ctypes.c_size_t
         L.moe_forward.argtypes = [ctypes.POINTER(ForwardArgs), P, P, ctypes.c_size_t, P]
@@ -207,17 +209,33 @@ def scatter(rows: torch.Tensor, route_slot: torch.Tensor, weights: torch.Tensor,
     return out
 
 
+def swiglu_quant(gu: torch.Tensor, stream=None):
+    """moe_swiglu_quant: gu f32 [R, 2I] (gate columns, then up columns) ->
+    (h_q u8 [R, I], h_scales f32 [I/128, R])."""
+    R, I2 = gu.shape
+    I = I2 // 2
+    h_q = torch.empty(R, I, dtype=torch.uint8, device=gu.device)
+    h_s = torch.empty(I // 128, R, dtype=torch.float32, device=gu.device)
+    _check(lib().moe_swiglu_quant(_ptr(gu), R, I, _ptr(h_q), _ptr(h_s), _stream(stream)),
+           "moe_swiglu_quant")
+    return h_q, h_s
+
+
 # ------------------------------------------------------------------ forward
 def forward_args(*, dtype, M, K, N, E, top_k, softcap=0.0, renorm=1, logits=None, x=None, w=None,
                  w_scales=None, w2=None, block_m=0, sched=SCHED_QUEUE, k_splits=0,
-                 use_graph=1, gather_rows=0) -> ForwardArgs:
+                 use_graph=1, gather_rows=0, gated=0, w2_scales=None) -> ForwardArgs:
+    """Arguments of moe_forward.  gated=1 with dtype FP8: the FP8 gated FFN
+    (w = w_up codes [E,2N,K] + w_scales, w2 = w_down codes [E,K,N] + w2_scales)."""
     return ForwardArgs(dtype=dtype, M=M, K=K, N=N, E=E, top_k=top_k, softcap=float(softcap),
                        renorm=int(renorm), logits=None if logits is None else logits.data_ptr(),
                        x=None if x is None else x.data_ptr(),
                        w=None if w is None else w.data_ptr(),
                        w_scales=None if w_scales is None else w_scales.data_ptr(),
                        w2=None if w2 is None else w2.data_ptr(), block_m=block_m, sched=sched,
-                       k_splits=k_splits, use_graph=use_graph, gather_rows=gather_rows)
+                       k_splits=k_splits, use_graph=use_graph, gather_rows=gather_rows,
+                       gated=gated,
+                       w2_scales=None if w2_scales is None else w2_scales.data_ptr())
 
 
 def workspace_size(args: ForwardArgs) -> int:

@@ -252,12 +252,24 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
 // Workspace layout of the forward.
 struct WsLayout {
   size_t ctrl, ids, weights, counts, offsets, tile_off, sorted, slot, a, a_scales, acc, h;
+  size_t hq, hs;  // FP8 gated FFN: h codes [R, N] and scales [N/128, R] (h: f32 gu [R, 2N])
   size_t local_rank, cta_hist, cta_base;
   size_t st_logits, st_x, st_out;
   size_t total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// The FP8 gated FFN (two FP8 projections with h re-quantised between them).
+bool fp8_ffn(const moe_forward_args* f) {
+  return f->dtype == MOE_DTYPE_FP8_E4M3 && f->gated == 1;
+}
+
+// Columns of the forward's output: N for the single FP8 GEMM, K (the token
+// feature size) for the gated FFNs.
+long long out_cols(const moe_forward_args* f) {
+  return (f->dtype == MOE_DTYPE_FP8_E4M3 && f->gated != 1) ? f->N : f->K;
+}
 
 bool forward_shape_ok(const moe_forward_args* f) {
   return f != nullptr && f->M > 0 && f->K > 0 && f->N > 0 && f->E > 0 && f->top_k > 0;
@@ -270,8 +282,7 @@ bool forward_shape_ok(const moe_forward_args* f) {
 // in bf16 instead and one kernel reduces every token's rows (streaming).
 constexpr long long kAccOnChipBytes = 112ll << 20;
 bool rows_path(const moe_forward_args* f) {
-  const long long out_cols = f->dtype == MOE_DTYPE_FP8_E4M3 ? f->N : f->K;
-  return static_cast<long long>(f->M) * out_cols * 4 > kAccOnChipBytes;
+  return static_cast<long long>(f->M) * out_cols(f) * 4 > kAccOnChipBytes;
 }
 
 // The forward's large-batch path with gather_rows set gathers the routed rows
@@ -310,17 +321,25 @@ WsLayout ws_layout(const moe_forward_args* f) {
   const size_t a_rows = gather ? M : R;
   L.a = (gather && !fp8) ? 0 : take(fp8 ? a_rows * K : a_rows * K * 2);
   L.a_scales = fp8 ? take((K / 128) * a_rows * 4) : 0;
-  const size_t out_cols = fp8 ? N : K;
+  const size_t cols = static_cast<size_t>(out_cols(f));
   // fp32 accumulator [M, out] for the scatter-add, or bf16 expert-compact rows
   // [R, out] reduced afterwards (see rows_path)
   if (rows_path(f))
-    L.acc = take(R * out_cols * 2);
+    L.acc = take(R * cols * 2);
   else
-    L.acc = take(M * out_cols * 4);
-  L.h = fp8 ? 0 : take(R * N * 2);
+    L.acc = take(M * cols * 4);
+  // gated FFN intermediates: BF16 h [R, N]; FP8 the up projection's f32 rows
+  // [R, 2N], then h's codes [R, N] and block scales [N/128, R]
+  if (!fp8) {
+    L.h = take(R * N * 2);
+  } else if (fp8_ffn(f)) {
+    L.h = take(R * 2 * N * 4);
+    L.hq = take(R * N);
+    L.hs = take((N / 128) * R * 4);
+  }
   L.st_logits = take(M * E * 4);
   L.st_x = take(M * K * 2);
-  L.st_out = take(M * out_cols * 2);
+  L.st_out = take(M * cols * 2);
   L.total = off;
   return L;
 }
@@ -335,10 +354,12 @@ moe_status_t check_forward(const moe_forward_args* f) {
   if (f->K % 128 != 0 || f->N % 128 != 0 || f->K > 16384) return MOE_ERR_UNSUPPORTED;
   if (!(f->softcap >= 0.0f)) return MOE_ERR_INVALID_ARG;
   if (f->gather_rows != 0 && f->gather_rows != 1) return MOE_ERR_INVALID_ARG;
+  if (f->gated != 0 && f->gated != 1) return MOE_ERR_INVALID_ARG;
   if (f->block_m != 0 && (f->block_m < 16 || f->block_m > 256 || (f->block_m & (f->block_m - 1))))
     return MOE_ERR_UNSUPPORTED;
   if (f->dtype == MOE_DTYPE_FP8_E4M3) {
     if (f->w_scales == nullptr) return MOE_ERR_INVALID_ARG;
+    if (f->gated == 1 && (f->w2 == nullptr || f->w2_scales == nullptr)) return MOE_ERR_INVALID_ARG;
     if (f->block_m > 128) return MOE_ERR_UNSUPPORTED;
   } else {
     if (f->w2 == nullptr) return MOE_ERR_INVALID_ARG;
@@ -393,21 +414,21 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   if (fp8) {
     uint8_t* a_q = ws + L.a;
     float* a_s = reinterpret_cast<float*>(ws + L.a_scales);
+    const bool ffn = fp8_ffn(f);
+    const int cols = static_cast<int>(out_cols(f));   // zeroed accumulator width
     if (small)
-      e = launch_quant_layout(x, M, K, k, E, bm, ids, a_q, a_s, acc, N, counts, offsets, sorted,
-                              slot, tile_off, ctrl, stream, pdl);
+      e = launch_quant_layout(x, M, K, k, E, bm, ids, a_q, a_s, acc, cols, counts, offsets,
+                              sorted, slot, tile_off, ctrl, stream, pdl);
     else
-      e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, rows ? nullptr : acc, N, pl, stream,
+      e = launch_quant_gather(x, M, K, k, slot, a_q, a_s, rows ? nullptr : acc, cols, pl, stream,
                               pdl, gather);
     if (e != cudaSuccess) return cuda_status(e);
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));
     g.dtype = MOE_DTYPE_FP8_E4M3;
-    g.epilogue = rows ? MOE_EPI_STORE_BF16 : MOE_EPI_SCATTER;
     g.sched = f->sched;
     g.block_m = bm;
     g.E = E;
-    g.N = N;
     g.K = K;
     g.R = R;
     g.M = M;
@@ -420,18 +441,42 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     g.tile_offsets = tile_off;
     g.sorted_route_ids = sorted;
     g.route_weights = wts;
+    g.gather_rows = gather ? 1 : 0;
+    moe_status_t s;
+    if (ffn) {
+      // up projection (gate and up rows) -> f32 rows; SwiGLU + 1x128
+      // re-quantisation; the down projection then reads h like activations
+      float* gu = reinterpret_cast<float*>(ws + L.h);
+      uint8_t* h_q = ws + L.hq;
+      float* h_s = reinterpret_cast<float*>(ws + L.hs);
+      g.epilogue = MOE_EPI_STORE;
+      g.N = 2 * N;
+      g.out = gu;
+      g.k_splits = 1;
+      s = run_gemm(&g, ctrl, false, stream, pdl);
+      if (s != MOE_OK) return s;
+      s = cuda_status(launch_swiglu_quant(gu, R, N, h_q, h_s, device_sms(), stream, pdl));
+      if (s != MOE_OK) return s;
+      g.gather_rows = 0;
+      g.N = K;
+      g.K = N;
+      g.a = h_q;
+      g.a_scales = h_s;
+      g.w = f->w2;
+      g.w_scales = f->w2_scales;
+    } else {
+      g.N = N;
+    }
+    g.epilogue = rows ? MOE_EPI_STORE_BF16 : MOE_EPI_SCATTER;
     g.out = acc;
     g.k_splits = rows ? 1 : f->k_splits;
-    g.gather_rows = gather ? 1 : 0;
-    moe_status_t s = run_gemm(&g, ctrl, false, stream, pdl);
+    s = run_gemm(&g, ctrl, ffn, stream, pdl);
     if (s != MOE_OK) return s;
     if (rows)
-      s = cuda_status(launch_reduce_rows(acc, slot, wts, M, N, k, out, device_sms(), stream, pdl));
-    else
-      s = cuda_status(launch_finalize(acc, out, static_cast<size_t>(M) * N, device_sms(), stream,
-                                      pdl));
-    if (s != MOE_OK) return s;
-    return MOE_OK;
+      return cuda_status(launch_reduce_rows(acc, slot, wts, M, cols, k, out, device_sms(), stream,
+                                            pdl));
+    return cuda_status(launch_finalize(acc, out, static_cast<size_t>(M) * cols, device_sms(),
+                                       stream, pdl));
   }
   // BF16 gated FFN: (route + rank above) -> gather, placing the routes -> up (SwiGLU)
   // -> down (scatter-add, or bf16 rows) -> finalize (or weighted row reduction)
@@ -639,6 +684,17 @@ moe_status_t moe_quant_gather(const void* x, int M, int K, int top_k, const int3
                                          static_cast<cudaStream_t>(stream), false));
 }
 
+moe_status_t moe_swiglu_quant(const float* gu, int R, int I, uint8_t* h_q, float* h_scales,
+                              void* stream) {
+  if (gu == nullptr || h_q == nullptr || h_scales == nullptr) return MOE_ERR_INVALID_ARG;
+  if (R <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  if (I % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(gu) || !aligned16(h_q) || (reinterpret_cast<uintptr_t>(h_scales) & 3u) != 0)
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_swiglu_quant(gu, R, I, h_q, h_scales, device_sms(),
+                                         static_cast<cudaStream_t>(stream), false));
+}
+
 moe_status_t moe_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_bytes, void* stream) {
   moe_status_t s = check_gemm(args);
   if (s != MOE_OK) return s;
@@ -670,20 +726,22 @@ moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k
   const int R = args->M * args->top_k;
   *block_m = args->block_m > 0 ? args->block_m : auto_block_m(fp8, R, args->E);
   *k_splits = 1;
-  // the scatter-add GEMM may split K; the bf16-rows form uses one split
+  // the scatter-add GEMM (the gated FFN's down projection) may split K; the
+  // bf16-rows form uses one split
   if (fp8 && !rows_path(args)) {
+    const bool ffn = fp8_ffn(args);
     moe_gemm_args g;
     std::memset(&g, 0, sizeof(g));
     g.dtype = MOE_DTYPE_FP8_E4M3;
     g.epilogue = MOE_EPI_SCATTER;
     g.block_m = *block_m;
     g.E = args->E;
-    g.N = args->N;
-    g.K = args->K;
+    g.N = ffn ? args->K : args->N;
+    g.K = ffn ? args->N : args->K;
     g.R = R;
     g.k_splits = args->k_splits;
     const int sms = device_sms();
-    *k_splits = pick_k_splits(&g, sms > 0 ? sms : 148, args->K / 128);
+    *k_splits = pick_k_splits(&g, sms > 0 ? sms : 148, g.K / 128);
   }
   return MOE_OK;
 }
@@ -723,9 +781,9 @@ moe_status_t moe_forward_host(const moe_forward_args* args, const float* host_lo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   const size_t M = args->M;
-  const size_t out_cols = args->dtype == MOE_DTYPE_FP8_E4M3 ? args->N : args->K;
+  const size_t cols = static_cast<size_t>(out_cols(args));
   const size_t logits_bytes = M * args->E * 4, x_bytes = M * args->K * 2;
-  const size_t out_bytes = M * out_cols * 2;
+  const size_t out_bytes = M * cols * 2;
   // Pinned (device-mapped) host buffers of a small forward: its kernels read
   // the logits and activations and write the result over the host link
   // themselves (only plain loads and stores touch them), so the step needs no
@@ -749,7 +807,7 @@ moe_status_t moe_forward_host(const moe_forward_args* args, const float* host_lo
                    w8 + L.st_out, ws, ws_bytes, st);
   if (s != MOE_OK) return s;
   return cuda_status(
-      cudaMemcpyAsync(host_out, w8 + L.st_out, M * out_cols * 2, cudaMemcpyDeviceToHost, st));
+      cudaMemcpyAsync(host_out, w8 + L.st_out, out_bytes, cudaMemcpyDeviceToHost, st));
 }
 
 moe_status_t moe_get_error(void* ws, moe_status_t* status, void* stream) {

@@ -16,6 +16,21 @@ inline cudaError_t prefer_max_shared(F* kernel) {
                               cudaSharedmemCarveoutMaxShared);
 }
 
+// Launch configuration of a plain kernel, as a programmatic dependent of the
+// previous launch on `stream` when `pdl` is set (attr: one slot, caller-owned).
+inline cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t stream, bool pdl,
+                                   cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 // Parameters of one grouped-GEMM launch (beyond the two TMA descriptors).
 struct GemmParams {
   const float* a_scales;        // FP8: [KB, R]
@@ -83,6 +98,10 @@ cudaError_t launch_quant_layout(const void* x, int M, int K, int k, int E, int b
                                 int zero_cols, int32_t* counts, int32_t* offsets,
                                 int32_t* sorted_route_ids, int32_t* route_slot,
                                 int32_t* tile_offsets, Ctrl* ctrl, cudaStream_t stream, bool pdl);
+// SwiGLU of the FP8 gated FFN's up projection (gu f32 [R, 2I], gate columns
+// first) re-quantised by the 1x128 rule: h_q u8 [R, I], h_scales f32 [I/128, R].
+cudaError_t launch_swiglu_quant(const float* gu, int R, int I, uint8_t* h_q, float* h_scales,
+                                int num_sms, cudaStream_t stream, bool pdl);
 cudaError_t launch_finalize(const float* acc, void* out, size_t n, int num_sms,
                             cudaStream_t stream, bool pdl);
 // token_major: write each token's codes once ([M, K], scales [K/128, M]) and

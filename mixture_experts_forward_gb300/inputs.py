@@ -22,6 +22,9 @@ source pages' workloads; no dataset is involved):
 * ``imbalance_bf16`` — T=16384, H=4096, I=1024, E=8, top-2 (the Mixtral-like
   layer of the Weave retelling, section 1.2) with expert loads whose
   max/min ratio is rho in {1, 4, 16, 40}.
+* ``ffn_fp8`` — the ``bf16_ffn`` shape and routing with FP8 expert weights
+  (gate+up [E,2I,H] and down [E,H,I], each prepared like the FP8 workloads'
+  weights: std 1/sqrt(fan_in), 128x128 blocks, amax/448 scales).
 
 Routing structure for the BF16 cases is realised through the logits: the
 chosen experts get +20 on top of N(0,1) noise and softcap is off, so top-k
@@ -39,6 +42,10 @@ FP8_CONFIGS = {
     "qwen_small_batch_fp8": dict(M=128, K=2048, N=512, E=256, k=8, softcap=30.0, zipf_bias=0.0),
     "skewed_large_batch_fp8": dict(M=4096, K=2048, N=512, E=256, k=8, softcap=30.0,
                                    zipf_bias=2.5),
+}
+
+FFN_FP8_CONFIGS = {
+    "ffn_fp8": dict(T=8192, H=3072, I=1536, E=16, k=8),
 }
 
 BF16_CONFIGS = {
@@ -79,7 +86,13 @@ def make_fp8_inputs(name_or_cfg, seed: int = 0, **overrides):
         rank = torch.arange(1, E + 1, dtype=torch.float64)
         logits = (logits + (cfg["zipf_bias"] * torch.log(1.0 / rank)).to(torch.float32)).contiguous()
     x = torch.randn(M, K, generator=g, dtype=torch.float32).to(torch.bfloat16)
-    std = 1.0 / math.sqrt(K)
+    codes, scales = _normal_weights_e4m3(E, N, K, 1.0 / math.sqrt(K), g)
+    return dict(cfg=cfg, logits=logits, x=x, w_q=codes, w_scales=scales)
+
+
+def _normal_weights_e4m3(E: int, N: int, K: int, std: float, g: torch.Generator):
+    """N(0, std) weights [E, N, K] drawn expert-chunk by expert-chunk, then
+    prepared by quantize_weights_e4m3."""
     codes = torch.empty(E, N, K, dtype=torch.uint8)
     scales = torch.empty(E, N // 128, K // 128, dtype=torch.float32)
     chunk = max(1, (1 << 26) // (N * K))       # bound the float32 temporaries
@@ -87,7 +100,7 @@ def make_fp8_inputs(name_or_cfg, seed: int = 0, **overrides):
         e1 = min(E, e0 + chunk)
         w = torch.randn(e1 - e0, N, K, generator=g, dtype=torch.float32) * std
         codes[e0:e1], scales[e0:e1] = quantize_weights_e4m3(w)
-    return dict(cfg=cfg, logits=logits, x=x, w_q=codes, w_scales=scales)
+    return codes, scales
 
 
 def _chosen_to_logits(chosen: torch.Tensor, E: int, g: torch.Generator) -> torch.Tensor:
@@ -144,6 +157,25 @@ def make_bf16_inputs(name_or_cfg, routing: str = "uniform", seed: int = 0, rho: 
     w_dn = (torch.randn(E, H, I, generator=g, dtype=torch.float32) / math.sqrt(I)).to(torch.bfloat16)
     cfg.update(routing=routing, rho=rho, softcap=0.0)
     return dict(cfg=cfg, logits=logits, x=x, w_up=w_up, w_dn=w_dn, chosen=chosen)
+
+
+def make_fp8_ffn_inputs(name_or_cfg, routing: str = "uniform", seed: int = 0, **overrides):
+    """Inputs of one FP8 gated-FFN workload as CPU tensors: logits f32 [T,E],
+    x bf16 [T,H], wup_q uint8 [E,2I,H] (rows [0,I) gate, [I,2I) up) with
+    wup_s f32 [E,2I/128,H/128], wdn_q uint8 [E,H,I] with wdn_s f32
+    [E,H/128,I/128]."""
+    cfg = dict(FFN_FP8_CONFIGS[name_or_cfg]) if isinstance(name_or_cfg, str) else dict(name_or_cfg)
+    cfg.update(overrides)
+    T, H, I, E, k = cfg["T"], cfg["H"], cfg["I"], cfg["E"], cfg["k"]
+    g = _gen(seed)
+    chosen = routing_choice(T, E, k, routing, g)
+    logits = _chosen_to_logits(chosen, E, g)
+    x = torch.randn(T, H, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    wup_q, wup_s = _normal_weights_e4m3(E, 2 * I, H, 1.0 / math.sqrt(H), g)
+    wdn_q, wdn_s = _normal_weights_e4m3(E, H, I, 1.0 / math.sqrt(I), g)
+    cfg.update(routing=routing, softcap=0.0)
+    return dict(cfg=cfg, logits=logits, x=x, wup_q=wup_q, wup_s=wup_s, wdn_q=wdn_q, wdn_s=wdn_s,
+                chosen=chosen)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

@@ -142,6 +142,47 @@ def test_forward_gather_rows_workspace(lib):
                                                         **big))) == 0
 
 
+def test_swiglu_quant_argument_errors(lib):
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    assert lib.moe_swiglu_quant(None, 4, 128, f, f, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_swiglu_quant(f, 4, 128, None, f, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_swiglu_quant(f, 0, 128, f, f, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_swiglu_quant(f, 4, 200, f, f, None) == L.MOE_ERR_UNSUPPORTED
+    assert lib.moe_swiglu_quant(P(FAKE + 4), 4, 128, f, f, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_swiglu_quant(f, 4, 128, P(FAKE + 8), f, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_swiglu_quant(f, 4, 128, f, P(FAKE + 2), None) == L.MOE_ERR_INVALID_ARG
+
+
+def test_forward_fp8_gated_checks_and_workspace(lib):
+    """The FP8 gated FFN needs both projections' codes and scales; its
+    workspace holds the up projection's f32 rows [R, 2N], h's codes [R, N]
+    and scales, and an accumulator as wide as the token features K."""
+    shape = dict(M=8192, K=3072, N=1536, E=16, top_k=8)
+    R = shape["M"] * shape["top_k"]
+    a = L.forward_args(dtype=L.DTYPE_FP8, gated=1, **shape)
+    a.w = FAKE
+    a.w_scales = FAKE
+    assert lib.moe_workspace_size(ctypes.byref(a)) == 0          # w2 missing
+    a.w2 = FAKE
+    assert lib.moe_workspace_size(ctypes.byref(a)) == 0          # w2_scales missing
+    a.w2_scales = FAKE
+    n = L.workspace_size(a)
+    K, N, M = shape["K"], shape["N"], shape["M"]
+    assert n >= R * 2 * N * 4 + R * N + (N // 128) * R * 4 + R * K + M * K * 4
+    single = L.forward_args(dtype=L.DTYPE_FP8, **shape)
+    single.w = FAKE
+    single.w_scales = FAKE
+    assert L.workspace_size(single) < n - R * 2 * N * 4
+    for bad in (2, -1):
+        a.gated = bad
+        assert lib.moe_workspace_size(ctypes.byref(a)) == 0
+    bf = L.forward_args(dtype=L.DTYPE_BF16, gated=1, M=64, K=256, N=256, E=4, top_k=2)
+    bf.w = FAKE
+    bf.w2 = FAKE
+    assert lib.moe_workspace_size(ctypes.byref(bf)) > 0         # BF16 is always gated
+
+
 def test_gemm_workspace_errors(lib):
     g = _gemm()
     assert lib.moe_grouped_gemm(ctypes.byref(g), None, 4096, None) == L.MOE_ERR_WORKSPACE
