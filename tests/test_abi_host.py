@@ -116,6 +116,7 @@ def _fwd(**kw):
     a.w = FAKE
     a.w_scales = FAKE
     a.w2 = FAKE
+    a.w2_scales = FAKE
     return a
 
 
@@ -181,6 +182,22 @@ def test_forward_fp8_gated_checks_and_workspace(lib):
     bf.w = FAKE
     bf.w2 = FAKE
     assert lib.moe_workspace_size(ctypes.byref(bf)) > 0         # BF16 is always gated
+
+
+def test_forward_plan_of_the_gated_fp8_ffn(lib):
+    """The plan's K split is that of the scatter-add GEMM: for the FP8 gated
+    FFN the down projection, whose contraction is the intermediate size N
+    (here 8 K blocks, and 20 tiles of 256 outputs: split in 2), not the single
+    FP8 GEMM's K (2 K blocks: no split)."""
+    def plan(**kw):
+        a = _fwd(dtype=L.DTYPE_FP8, M=16, K=256, N=1024, E=8, top_k=2, **kw)
+        return L.forward_plan(a)
+    assert plan(gated=1) == (16, 2)
+    assert plan() == (16, 1)
+    assert plan(gated=1, k_splits=3) == (16, 3)
+    assert plan(k_splits=3) == (16, 2)                     # capped at the 2 K blocks
+    big = _fwd(dtype=L.DTYPE_FP8, gated=1, M=16384, K=2048, N=256, E=8, top_k=2)
+    assert L.forward_plan(big)[1] == 1                     # bf16-rows form: one split
 
 
 def test_gemm_workspace_errors(lib):
