@@ -9,6 +9,12 @@ Metric: TFLOPS on compact routed rows (2*R*N*K per forward, R = M*top_k);
 µs per forward and the fraction of the roofline are reported beside it.
 
   python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+                  [--config qwen_small_batch_fp8 | tiny_fp8 | skewed_large_batch_fp8 |
+                            bf16_ffn | imbalance_bf16 | ffn_fp8]
+
+The gated-FFN workloads (bf16_ffn, imbalance_bf16, ffn_fp8) count the FLOPs of
+both projections, 2*R*2I*H + 2*R*H*I; ffn_fp8 is the FP8 gated FFN (h
+re-quantised in 1x128 blocks between the projections).
 
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (token data-parallel, no collective on the data path); rank 0 prints the
