@@ -91,6 +91,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--measure-fp8-peak", action="store_true",
+                    help="measure the dense FP8 (e4m3) tensor peak with torch._scaled_mm "
+                         "(cuBLASLt) on 8192^3, print one JSON line and exit")
     return ap.parse_args()
 
 
@@ -154,44 +157,81 @@ def flops_per_step(kind, c):
 
 
 def peaks():
+    """Roofline denominators: HBM and bf16 from MEASURED_PEAKS.json (else the
+    fallback figures); FP8 from the committed measurement of the vendor FP8
+    GEMM (profiles/fp8_dense_peak.json, written from `--measure-fp8-peak`),
+    else twice the bf16 burst."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         j = json.load(open(p))
-        return dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j["bf16_tflops_sustained"],
-                    src="measured")
-    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+        pk = dict(hbm=j["hbm_gbs"], bf16=j["bf16_tflops"], bf16_sus=j["bf16_tflops_sustained"],
+                  src="measured")
+    else:
+        pk = dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+    pk["fp8_nominal"] = 2 * pk["bf16"]
+    f = os.path.join(ROOT, "profiles", "fp8_dense_peak.json")
+    if os.path.exists(f):
+        pk["fp8"] = json.load(open(f))["fp8_e4m3_tflops"]
+        pk["fp8_src"] = "measured cuBLASLt e4m3 8192^3 burst"
+    else:
+        pk["fp8"] = pk["fp8_nominal"]
+        pk["fp8_src"] = f"2 x {pk['src']} bf16 burst"
+    return pk
 
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples around a timed region: one
+    query when it starts, a 50 ms polling loop while it runs, and one query
+    right after the last step has been enqueued (while the GPU still works
+    through the queue), so even a region of a few milliseconds has a record."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.path = None
+        self.lines = []
+
+    def _cmd(self):
+        return ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                "--format=csv,noheader,nounits"]
+
+    def sample_now(self):
+        try:
+            r = subprocess.run(self._cmd(), capture_output=True, text=True, timeout=10)
+            self.lines += r.stdout.splitlines()
+        except (FileNotFoundError, OSError, subprocess.TimeoutExpired):
+            pass
 
     def start(self):
-        self.path = tempfile.mktemp(suffix=".csv")
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        self.sample_now()
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            self.proc = subprocess.Popen(self._cmd() + ["-lms", "50"], stdout=fd,
+                                         stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
+        os.close(fd)
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.path is not None:
+            with open(self.path) as f:
+                self.lines += f.read().splitlines()
+            os.unlink(self.path)
+            self.path = None
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in self.lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -203,7 +243,6 @@ class ClockSampler:
             for nm, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
-        os.unlink(self.path)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
@@ -270,6 +309,7 @@ def bench_ours(args, rank, world, local):
         starts[i].record(stream)
         L.forward(fa, out, ws)
         ends[i].record(stream)
+    sampler.sample_now()                 # while the GPU still drains the queued steps
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
@@ -295,12 +335,12 @@ def bench_ours(args, rank, world, local):
                            touched, pk, cfg_name=args.config)
     if kind == "fp8":
         alg_bytes = touched * (N * K + (N // 128) * (K // 128) * 4) + M * E * 4 + M * K * 2 + M * N * 2
-        t_roof = max(fl / (2 * pk["bf16"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
+        t_roof = max(fl / (pk["fp8"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
     elif kind == "fp8ffn":
         # both projections' codes and block scales of every touched expert
         w_bytes = 3 * N * K + ((2 * N // 128) * (K // 128) + (K // 128) * (N // 128)) * 4
         alg_bytes = touched * w_bytes + M * E * 4 + M * K * 2 + M * K * 2
-        t_roof = max(fl / (2 * pk["bf16"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
+        t_roof = max(fl / (pk["fp8"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
     else:
         alg_bytes = touched * (2 * N * K + K * N) * 2 + M * E * 4 + M * K * 2 + M * K * 2
         t_roof = max(fl / (pk["bf16"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
@@ -327,7 +367,8 @@ def bench_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world} (token data-parallel, no collective)"},
         "forward_roofline": {"bound": "hbm" if t_roof == alg_bytes / (pk["hbm"] * 1e9) else "tensor",
                              "alg_bytes": int(alg_bytes), "roofline_us": round(t_roof * 1e6, 3),
-                             "frac": round(fwd_roof_frac, 4), "peak_source": pk["src"]},
+                             "frac": round(fwd_roof_frac, 4), "peak_source": pk["src"],
+                             "fp8_peak_source": pk["fp8_src"] if kind != "bf16" else None},
         "roofline": roof,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -431,7 +472,7 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
     avg_s = statistics.median(g - f for g, f in spans) / n
     t_hbm = alg / (pk["hbm"] * 1e9)
     fp8 = kind in ("fp8", "fp8ffn")
-    t_tc = fl / ((2 if fp8 else 1) * pk["bf16"] * 1e12)
+    t_tc = fl / ((pk["fp8"] if fp8 else pk["bf16"]) * 1e12)
     traffic = stored_traffic(src, name, cfg_name)
     if t_hbm >= t_tc:
         achieved = alg / avg_s / 1e9
@@ -441,12 +482,15 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
                 "avg_launch_us": round(avg_s * 1e6, 3),
                 "peak_note": f"{pk['src']} copy bandwidth (burst)"}
     achieved = fl / avg_s / 1e12
-    peak = 2 * pk["bf16"] if fp8 else pk["bf16"]
-    note = f"fp8 = 2 x {pk['src']} bf16 burst" if fp8 else f"{pk['src']} bf16 burst"
-    return {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
-            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-            "flops_per_launch": fl, "avg_launch_us": round(avg_s * 1e6, 3),
-            "peak_note": note}
+    peak = pk["fp8"] if fp8 else pk["bf16"]
+    note = pk["fp8_src"] if fp8 else f"{pk['src']} bf16 burst"
+    res = {"kernel": name, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+           "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+           "flops_per_launch": fl, "avg_launch_us": round(avg_s * 1e6, 3),
+           "peak_note": note}
+    if fp8:
+        res["frac_of_nominal_2x_bf16"] = round(achieved / pk["fp8_nominal"], 4)
+    return res
 
 
 def code_sha(path: str) -> str:
@@ -585,8 +629,63 @@ def bench_reference(args, rank, world):
     print(json.dumps(res), flush=True)
 
 
+def measure_fp8_peak():
+    """Dense E4M3 x E4M3 -> bf16 GEMM throughput of the vendor library on this
+    GPU, the FP8 counterpart of the driver's bf16 measurement: 8192^3
+    (2 * 8192^3 FLOPs), best of 10 single launches (burst) and the mean over
+    back-to-back launches for about 4 s (sustained), CUDA events on the
+    launching stream, with the clocks sampled meanwhile."""
+    n = 8192
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(0)
+    a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn).t()  # column-major
+    one = torch.ones((), device=dev)
+
+    def mm():
+        return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    fl = 2.0 * n ** 3
+    stream = torch.cuda.current_stream()
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        mm()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e-3)
+    sampler = ClockSampler(0)
+    sampler.start()
+    reps, total = 0, 0.0
+    while total < 4.0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(100):
+            mm()
+        e1.record(stream)
+        sampler.sample_now()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1) * 1e-3
+        reps += 100
+    clocks = sampler.stop()
+    print(json.dumps({"fp8_e4m3_tflops": round(fl / best / 1e12, 1),
+                      "fp8_e4m3_tflops_sustained": round(fl * reps / total / 1e12, 1),
+                      "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, unit tensor scales, 8192^3: "
+                             "best of 10 (burst); 100-launch batches back to back for ~4 s "
+                             "(sustained); CUDA events",
+                      "torch": torch.__version__, "gpu": torch.cuda.get_device_name(0),
+                      "clocks": clocks}), flush=True)
+
+
 def main():
     args = parse()
+    if args.measure_fp8_peak:
+        measure_fp8_peak()
+        return
     rank, world, local = dist_setup(args.gpus)
     try:
         if args.impl == "reference":

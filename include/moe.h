@@ -238,6 +238,44 @@ size_t moe_workspace_size(const moe_forward_args* args);
  * down projection's split, the up projection storing with one split). */
 moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k_splits);
 
+/* Offset of a buffer that the forward does not keep for these arguments. */
+#define MOE_WS_NONE ((size_t)-1)
+
+/* Where moe_forward keeps its intermediates inside the workspace: byte
+ * offsets from the workspace's start.  Once a forward has completed on its
+ * stream these buffers hold the results of its own steps, each in exactly
+ * the form the standalone entry points define (the next forward on the same
+ * workspace overwrites them):
+ *   ids, weights      s32 / f32 [M, top_k]: moe_route ("Fused MoE FP8",
+ *                     section "Baseline: 7 kernels", item 1);
+ *   counts [E], offsets [E+1], tile_offsets [E+1] (tiles of block_m rows),
+ *   sorted_route_ids [R], route_slot [R]: moe_layout (items 2-3, section
+ *                     "Fusion 3"), R = M * top_k;
+ *   a, a_scales       FP8: E4M3 codes u8 [a_rows, K] and scales f32
+ *                     [K/128, a_rows] of moe_quant_gather (items 4-5): the
+ *                     expert-compact rows (a_rows = R, row = slot) or, with
+ *                     gather_rows on the large-batch path, each token once
+ *                     (a_rows = M, row = token).  BF16: the expert-compact
+ *                     bf16 rows [R, K] (row = slot, a copy of x's row
+ *                     sorted_route_ids[slot] / top_k), a_scales MOE_WS_NONE;
+ *                     a = MOE_WS_NONE when the BF16 up projection gathers
+ *                     its rows itself;
+ *   h_q, h_scales     FP8 gated FFN only: h's E4M3 codes u8 [R, N] and scales
+ *                     f32 [N/128, R] (the moe_swiglu_quant step), else
+ *                     MOE_WS_NONE;
+ *   block_m           the forward's tile rows (as moe_forward_plan).
+ * Host-only query; nothing is enqueued.  MOE_ERR_INVALID_ARG /
+ * MOE_ERR_UNSUPPORTED as moe_workspace_size's arguments, or map == NULL. */
+typedef struct {
+  size_t ids, weights, counts, offsets, tile_offsets, sorted_route_ids, route_slot;
+  size_t a, a_scales;
+  size_t h_q, h_scales;
+  int a_rows;
+  int block_m;
+} moe_workspace_map;
+
+moe_status_t moe_forward_workspace_map(const moe_forward_args* args, moe_workspace_map* map);
+
 /* Fused forward: route -> layout -> quantise+gather (FP8) or gather (BF16)
  * -> grouped GEMM(s) -> weighted scatter -> bf16 output.  The FP8 gated FFN
  * (gated = 1) runs the up projection storing f32 rows [R, 2N], then
@@ -253,7 +291,9 @@ moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k
  * With use_graph = 1 the launch sequence is captured (on a private stream) on
  * first use for this argument set, pointers included, and the graph is
  * replayed on `stream`; when `stream` is already capturing, the kernels are
- * launched directly into the caller's capture. */
+ * launched directly into the caller's capture.  Cached graphs belong to the
+ * device's current context: do not use a forward with use_graph = 1 on a
+ * device after cudaDeviceReset. */
 moe_status_t moe_forward(const moe_forward_args* args, void* out, void* ws, size_t ws_bytes,
                          void* stream);
 
@@ -294,7 +334,9 @@ moe_status_t moe_get_error(void* ws, moe_status_t* status, void* stream);
  *
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is kept for the life of the
+ *   process: do not call this entry point on a device after cudaDeviceReset
+ *   (the reset recreates the array elsewhere).
  * - Each call clears the scratch (cudaMemsetAsync on `stream`) before its
  *   kernel, since the array keeps the previous call's contents.
  * - All calls in the process share the one array per device: calls whose

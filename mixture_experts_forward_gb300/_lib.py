@@ -23,7 +23,9 @@ CTRL_BYTES = 256
 EXPORTS = ["moe_status_string", "moe_num_sms", "moe_route", "moe_layout", "moe_quant_gather",
            "moe_grouped_gemm", "moe_scatter", "moe_workspace_size", "moe_forward",
            "moe_forward_host", "moe_get_error", "moe_debug_set_pipeline_fault", "moe_forward_plan",
-           "moe_last_cuda_error", "moe_grouped_gemm_noalloc", "moe_swiglu_quant"]
+           "moe_last_cuda_error", "moe_grouped_gemm_noalloc", "moe_swiglu_quant",
+           "moe_forward_workspace_map"]
+WS_NONE = (1 << 64) - 1   # MOE_WS_NONE
 
 
 class MoeError(RuntimeError):
@@ -58,6 +60,13 @@ class ForwardArgs(ctypes.Structure):
                 ("gated", ctypes.c_int), ("w2_scales", ctypes.c_void_p)]
 
 
+class WorkspaceMap(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("ids", "weights", "counts", "offsets", "tile_offsets", "sorted_route_ids",
+                 "route_slot", "a", "a_scales", "h_q", "h_scales")] + \
+               [("a_rows", ctypes.c_int), ("block_m", ctypes.c_int)]
+
+
 _lib = None
 
 
@@ -87,6 +96,8 @@ def lib():
         L.moe_forward_host.argtypes = [ctypes.POINTER(ForwardArgs), P, P, P, P, ctypes.c_size_t, P]
         L.moe_forward_plan.argtypes = [ctypes.POINTER(ForwardArgs), ctypes.POINTER(I),
                                        ctypes.POINTER(I)]
+        L.moe_forward_workspace_map.argtypes = [ctypes.POINTER(ForwardArgs),
+                                                ctypes.POINTER(WorkspaceMap)]
         L.moe_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
         L.moe_debug_set_pipeline_fault.argtypes = [I, ctypes.c_uint64]
         for name in EXPORTS:
@@ -251,6 +262,30 @@ def forward_plan(args: ForwardArgs):
     _check(lib().moe_forward_plan(ctypes.byref(args), ctypes.byref(bm), ctypes.byref(ks)),
            "moe_forward_plan")
     return bm.value, ks.value
+
+
+def workspace_map(args: ForwardArgs) -> dict:
+    """moe_forward_workspace_map: byte offsets of the forward's intermediates
+    in its workspace (None for a buffer the forward does not keep), plus
+    a_rows and block_m."""
+    m = WorkspaceMap()
+    _check(lib().moe_forward_workspace_map(ctypes.byref(args), ctypes.byref(m)),
+           "moe_forward_workspace_map")
+    out = {}
+    for name, _ in WorkspaceMap._fields_:
+        v = getattr(m, name)
+        out[name] = None if (name not in ("a_rows", "block_m") and v == WS_NONE) else v
+    return out
+
+
+def ws_view(ws: torch.Tensor, offset: int, dtype: torch.dtype, shape) -> torch.Tensor:
+    """The workspace bytes at ``offset`` viewed as a tensor of dtype/shape
+    (no copy)."""
+    n = 1
+    for s in shape:
+        n *= int(s)
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    return ws[offset:offset + nbytes].view(dtype).view(*shape)
 
 
 def forward(args: ForwardArgs, out: torch.Tensor, ws: torch.Tensor, stream=None):

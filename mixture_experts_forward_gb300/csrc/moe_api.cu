@@ -746,6 +746,30 @@ moe_status_t moe_forward_plan(const moe_forward_args* args, int* block_m, int* k
   return MOE_OK;
 }
 
+moe_status_t moe_forward_workspace_map(const moe_forward_args* args, moe_workspace_map* map) {
+  moe_status_t s = check_forward(args);
+  if (s != MOE_OK) return s;
+  if (map == nullptr) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(args);
+  const bool fp8 = args->dtype == MOE_DTYPE_FP8_E4M3;
+  const bool gather = forward_gathers(args);
+  const int R = args->M * args->top_k;
+  map->ids = L.ids;
+  map->weights = L.weights;
+  map->counts = L.counts;
+  map->offsets = L.offsets;
+  map->tile_offsets = L.tile_off;
+  map->sorted_route_ids = L.sorted;
+  map->route_slot = L.slot;
+  map->a = (gather && !fp8) ? MOE_WS_NONE : L.a;
+  map->a_scales = fp8 ? L.a_scales : MOE_WS_NONE;
+  map->h_q = fp8_ffn(args) ? L.hq : MOE_WS_NONE;
+  map->h_scales = fp8_ffn(args) ? L.hs : MOE_WS_NONE;
+  map->a_rows = gather ? args->M : R;
+  map->block_m = args->block_m > 0 ? args->block_m : auto_block_m(fp8, R, args->E);
+  return MOE_OK;
+}
+
 moe_status_t moe_forward(const moe_forward_args* args, void* out, void* ws, size_t ws_bytes,
                          void* stream) {
   if (args == nullptr) return MOE_ERR_INVALID_ARG;

@@ -69,12 +69,16 @@ __global__ void __launch_bounds__(1024) quant_gather_kernel(
       if ((c & 7) == 0) a_scales[static_cast<size_t>(c >> 3) * M + t] = s;
     }
     pdl_wait();
-    if (valid && c < k) route_slot_of(t * k + c, t, route_slot, route_slot, pl, R);
+    // a token has G threads and top_k routes (top_k may exceed G): strided
+    if (valid)
+      for (int j = c; j < k; j += G) route_slot_of(t * k + j, t, route_slot, route_slot, pl, R);
     return;
   }
   pdl_wait();
 
-  if (valid && c < k) s_slot[lt * k + c] = route_slot_of(t * k + c, t, route_slot, route_slot, pl, R);
+  if (valid)
+    for (int j = c; j < k; j += G)
+      s_slot[lt * k + j] = route_slot_of(t * k + j, t, route_slot, route_slot, pl, R);
   __syncthreads();
   if (!valid) return;
 

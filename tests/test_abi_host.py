@@ -200,6 +200,68 @@ def test_forward_plan_of_the_gated_fp8_ffn(lib):
     assert L.forward_plan(big)[1] == 1                     # bf16-rows form: one split
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(block_m=24), L.MOE_ERR_UNSUPPORTED), (dict(K=200), L.MOE_ERR_UNSUPPORTED),
+    (dict(E=2000), L.MOE_ERR_UNSUPPORTED), (dict(epilogue=L.EPI_SWIGLU), L.MOE_ERR_UNSUPPORTED),
+    (dict(a=None), L.MOE_ERR_INVALID_ARG), (dict(a_scales=None), L.MOE_ERR_INVALID_ARG),
+    (dict(R=33), L.MOE_ERR_INVALID_ARG), (dict(sorted_route_ids=None), L.MOE_ERR_INVALID_ARG),
+    (dict(epilogue=L.EPI_STORE, k_splits=2), L.MOE_ERR_UNSUPPORTED),
+    (dict(dtype=7), L.MOE_ERR_INVALID_ARG), (dict(out=FAKE + 8), L.MOE_ERR_INVALID_ARG),
+    (dict(gather_rows=2), L.MOE_ERR_INVALID_ARG),
+    (dict(gather_rows=1, dtype=L.DTYPE_BF16, a_scales=None, w_scales=None),
+     L.MOE_ERR_UNSUPPORTED),
+])
+def test_gemm_noalloc_argument_errors_match(lib, kw, code):
+    """The allocation-free GEMM rejects bad arguments exactly as the
+    workspace entry point does, before touching its scratch or the GPU."""
+    g = _gemm(**kw)
+    assert lib.moe_grouped_gemm(ctypes.byref(g), ctypes.c_void_p(FAKE), 4096, None) == code
+    assert lib.moe_grouped_gemm_noalloc(ctypes.byref(g), None) == code
+    assert lib.moe_grouped_gemm_noalloc(None, None) == L.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [
+    dict(dtype=L.DTYPE_FP8, M=128, K=2048, N=512, E=256, top_k=8),           # fused quant+layout
+    dict(dtype=L.DTYPE_FP8, M=4096, K=2048, N=512, E=256, top_k=8),          # route+rank path
+    dict(dtype=L.DTYPE_FP8, M=4096, K=2048, N=512, E=256, top_k=8, gather_rows=1),
+    dict(dtype=L.DTYPE_FP8, gated=1, M=8192, K=3072, N=1536, E=16, top_k=8),
+    dict(dtype=L.DTYPE_BF16, M=8192, K=3072, N=1536, E=16, top_k=8),
+    dict(dtype=L.DTYPE_BF16, M=8192, K=3072, N=1536, E=16, top_k=8, gather_rows=1),
+])
+def test_forward_workspace_map(lib, kw):
+    """Every intermediate the map names lies inside the workspace, 256-byte
+    aligned, without overlapping another; a_rows and block_m follow the
+    forward's plan and gathered rows."""
+    a = _fwd(**kw)
+    n = L.workspace_size(a)
+    m = L.workspace_map(a)
+    M, K, N, E, k = kw["M"], kw["K"], kw["N"], kw["E"], kw["top_k"]
+    R = M * k
+    fp8 = kw["dtype"] == L.DTYPE_FP8
+    gather = kw.get("gather_rows", 0) == 1 and not (fp8 and R <= 4096)
+    assert m["block_m"] == L.forward_plan(a)[0]
+    assert m["a_rows"] == (M if gather else R)
+    sizes = dict(ids=R * 4, weights=R * 4, counts=E * 4, offsets=(E + 1) * 4,
+                 tile_offsets=(E + 1) * 4, sorted_route_ids=R * 4, route_slot=R * 4)
+    if m["a"] is not None:
+        sizes["a"] = m["a_rows"] * K * (1 if fp8 else 2)
+    if m["a_scales"] is not None:
+        sizes["a_scales"] = (K // 128) * m["a_rows"] * 4
+    if m["h_q"] is not None:
+        sizes["h_q"] = R * N
+        sizes["h_scales"] = (N // 128) * R * 4
+    assert (m["a"] is None) == (not fp8 and gather)
+    assert (m["a_scales"] is None) == (not fp8)
+    assert (m["h_q"] is None) == (kw.get("gated", 0) != 1 or not fp8)
+    spans = sorted((m[name], m[name] + sz) for name, sz in sizes.items())
+    assert spans[0][0] >= L.CTRL_BYTES
+    for (b0, e0), (b1, _) in zip(spans, spans[1:]):
+        assert e0 <= b1
+    assert spans[-1][1] <= n
+    assert all(b % 256 == 0 for b, _ in spans)
+    assert lib.moe_forward_workspace_map(ctypes.byref(a), None) == L.MOE_ERR_INVALID_ARG
+
+
 def test_gemm_workspace_errors(lib):
     g = _gemm()
     assert lib.moe_grouped_gemm(ctypes.byref(g), None, 4096, None) == L.MOE_ERR_WORKSPACE
@@ -233,7 +295,8 @@ def test_workspace_size_and_forward_errors(lib):
 
 
 @pytest.mark.parametrize("cname,pyclass", [("moe_gemm_args", "GemmArgs"),
-                                           ("moe_forward_args", "ForwardArgs")])
+                                           ("moe_forward_args", "ForwardArgs"),
+                                           ("moe_workspace_map", "WorkspaceMap")])
 def test_argument_structs_match_the_binding(tmp_path, cname, pyclass):
     """The ctypes mirrors of the argument structs have the header's size and
     field offsets (a C program built against include/moe.h prints them)."""
