@@ -52,7 +52,11 @@ typedef enum { MOE_DTYPE_FP8_E4M3 = 0, MOE_DTYPE_BF16 = 1 } moe_dtype_t;
 typedef enum {
   MOE_EPI_SCATTER = 0,  /* out f32 [M,N] += route_weight * row   (weighted scatter-add) */
   MOE_EPI_STORE = 1,    /* out f32 [R,N]  = row                   (expert-compact rows) */
-  MOE_EPI_SWIGLU = 2,   /* out bf16 [R,N/2] = silu(gate) * up; weight rows [0,N/2) gate, [N/2,N) up */
+  MOE_EPI_SWIGLU = 2,   /* h = silu(gate) * up; weight rows [0,N/2) gate, [N/2,N) up.
+                           BF16: out bf16 [R,N/2] = h.  FP8: h in binary32 as moe_swiglu_quant
+                           computes it from the fp32 accumulators, re-quantised by the 1x128
+                           rule: out u8 [R,N/2] E4M3 codes, out_scales f32 [N/256,R]
+                           (N % 256 == 0) */
   MOE_EPI_STORE_BF16 = 3 /* out bf16 [R,N] = bf16(row)            (expert-compact rows; the
                             forward's large-batch path reduces them with the route weights
                             afterwards instead of scatter-adding into an fp32 accumulator) */
@@ -147,8 +151,10 @@ typedef struct {
                                  (FP8 a_scales token-major [K/128, M]); sorted_route_ids, M
                                  and top_k are then required for every epilogue, and an
                                  empty slot (id < 0) reads row 0 (its result is dropped).
-                                 Built for FP8 (every epilogue) and the BF16 SWIGLU
-                                 epilogue; other BF16 epilogues: MOE_ERR_UNSUPPORTED */
+                                 Built for FP8 (STORE, STORE_BF16, SCATTER) and the BF16
+                                 SWIGLU epilogue; others: MOE_ERR_UNSUPPORTED */
+  float* out_scales;          /* FP8 SWIGLU only: f32 [N/256, R] block scales of h (see
+                                 moe_epilogue_t); ignored otherwise */
 } moe_gemm_args;
 
 /* Grouped GEMM — "Fused MoE FP8" section "Baseline: 7 kernels" item 6, with
@@ -217,12 +223,14 @@ typedef struct {
                              of reading an expert-compact copy; the workspace then holds
                              no [R, K] copy (FP8 keeps one token-major [M, K] code matrix).
                              0 (default) = write the compact copy, which is faster on
-                             GB300 at the benchmark shapes; same results either way */
+                             GB300 at the benchmark shapes; same results either way.
+                             Ignored by the FP8 gated FFN (its fused SwiGLU up
+                             projection reads the compact copy) */
   int gated;              /* FP8_E4M3: 1 = gated FFN in FP8 — w = e4m3 w_up [E,2N,K] (gate
                              rows, then up rows) with w_scales [E,2N/128,K/128]; w2 = e4m3
                              w_down [E,K,N] with w2_scales [E,K/128,N/128]; h =
-                             silu(gate)*up re-quantised as by moe_swiglu_quant between the
-                             projections; output [M,K].  0 = the single FP8 GEMM.  BF16:
+                             silu(gate)*up re-quantised by the 1x128 rule in the up
+                             projection's epilogue (MOE_EPI_SWIGLU, FP8); output [M,K].  0 = the single FP8 GEMM.  BF16:
                              must be 0 or 1 (its forward is always the gated FFN) */
   const float* w2_scales; /* FP8 with gated = 1: [E,K/128,N/128] */
 } moe_forward_args;
@@ -278,9 +286,9 @@ moe_status_t moe_forward_workspace_map(const moe_forward_args* args, moe_workspa
 
 /* Fused forward: route -> layout -> quantise+gather (FP8) or gather (BF16)
  * -> grouped GEMM(s) -> weighted scatter -> bf16 output.  The FP8 gated FFN
- * (gated = 1) runs the up projection storing f32 rows [R, 2N], then
- * moe_swiglu_quant's step into codes [R, N] and scales [N/128, R], then the
- * FP8 down projection.  While the fp32
+ * (gated = 1) runs the up projection with the FP8 SWIGLU epilogue (gate and up
+ * tiles of the same 128 h columns; h re-quantised in the epilogue into codes
+ * [R, N] and scales [N/128, R]), then the FP8 down projection.  While the fp32
  * output accumulator (M x out x 4 bytes) is at most 112 MiB the weighted
  * scatter is fused into the last GEMM's epilogue (fp32 reductions into the
  * accumulator, then one bf16 rounding); above that the GEMM stores each

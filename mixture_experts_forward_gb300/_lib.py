@@ -46,7 +46,7 @@ class GemmArgs(ctypes.Structure):
                 ("offsets", ctypes.c_void_p), ("tile_offsets", ctypes.c_void_p),
                 ("sorted_route_ids", ctypes.c_void_p), ("route_weights", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("k_splits", ctypes.c_int), ("num_ctas", ctypes.c_int),
-                ("gather_rows", ctypes.c_int)]
+                ("gather_rows", ctypes.c_int), ("out_scales", ctypes.c_void_p)]
 
 
 class ForwardArgs(ctypes.Structure):
@@ -173,9 +173,10 @@ def quant_gather(x: torch.Tensor, k: int, route_slot: torch.Tensor, zero_acc=Non
 def grouped_gemm(*, dtype, epilogue, a, w, offsets, tile_offsets, out, ws, block_m,
                  a_scales=None, w_scales=None, sorted_route_ids=None, route_weights=None,
                  M=0, top_k=0, sched=SCHED_QUEUE, k_splits=0, num_ctas=0, gather_rows=0,
-                 stream=None):
+                 out_scales=None, stream=None):
     """moe_grouped_gemm.  gather_rows=1: `a` (and FP8 a_scales) are token-major
-    and compact slot s reads row sorted_route_ids[s] // top_k."""
+    and compact slot s reads row sorted_route_ids[s] // top_k.  FP8 SWIGLU:
+    out = u8 [R, N/2] codes of h, out_scales = f32 [N/256, R]."""
     E, N, K = w.shape
     R = sorted_route_ids.numel() if gather_rows else a.shape[0]
     g = GemmArgs(dtype=dtype, epilogue=epilogue, sched=sched, block_m=block_m, E=E, N=N, K=K,
@@ -186,7 +187,8 @@ def grouped_gemm(*, dtype, epilogue, a, w, offsets, tile_offsets, out, ws, block
                  sorted_route_ids=None if sorted_route_ids is None else sorted_route_ids.data_ptr(),
                  route_weights=None if route_weights is None else route_weights.data_ptr(),
                  out=out.data_ptr(), k_splits=k_splits, num_ctas=num_ctas,
-                 gather_rows=gather_rows)
+                 gather_rows=gather_rows,
+                 out_scales=None if out_scales is None else out_scales.data_ptr())
     _check(lib().moe_grouped_gemm(ctypes.byref(g), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_grouped_gemm")
     return out
@@ -194,7 +196,8 @@ def grouped_gemm(*, dtype, epilogue, a, w, offsets, tile_offsets, out, ws, block
 
 def grouped_gemm_noalloc(*, dtype, epilogue, a, w, offsets, tile_offsets, out, block_m,
                          a_scales=None, w_scales=None, sorted_route_ids=None, route_weights=None,
-                         M=0, top_k=0, sched=SCHED_QUEUE, k_splits=0, num_ctas=0, stream=None):
+                         M=0, top_k=0, sched=SCHED_QUEUE, k_splits=0, num_ctas=0,
+                         out_scales=None, stream=None):
     """moe_grouped_gemm_noalloc: the same GEMM with the library's own static
     scratch instead of a workspace (for callers that cannot allocate)."""
     E, N, K = w.shape
@@ -205,7 +208,8 @@ def grouped_gemm_noalloc(*, dtype, epilogue, a, w, offsets, tile_offsets, out, b
                  offsets=offsets.data_ptr(), tile_offsets=tile_offsets.data_ptr(),
                  sorted_route_ids=None if sorted_route_ids is None else sorted_route_ids.data_ptr(),
                  route_weights=None if route_weights is None else route_weights.data_ptr(),
-                 out=out.data_ptr(), k_splits=k_splits, num_ctas=num_ctas)
+                 out=out.data_ptr(), k_splits=k_splits, num_ctas=num_ctas,
+                 out_scales=None if out_scales is None else out_scales.data_ptr())
     _check(lib().moe_grouped_gemm_noalloc(ctypes.byref(g), _stream(stream)),
            "moe_grouped_gemm_noalloc")
     return out

@@ -43,7 +43,9 @@
 // MMAs, frees its TMEM and returns.
 #include <cuda_bf16.h>
 
+#include "ieee_math.cuh"
 #include "moe_internal.cuh"
+#include "quant_common.cuh"
 
 namespace moe {
 
@@ -70,18 +72,25 @@ struct TileDesc {
   int e, m0, rows, n_tile, kb0, nkb;
 };
 
-// kWide (BF16, not SwiGLU): a tile covers two adjacent 128-row weight tiles
-// (256 output columns) that share its routed-row operand — two MMAs per K
-// block from one stage, as the gated up projection has, so a stage carries
-// twice the tensor work for 1.5 times the bytes.
+// kWide (not SwiGLU): a tile covers two adjacent 128-row weight tiles (256
+// output columns) that share its routed-row operand — two MMAs per K block
+// from one stage, as the gated up projection has, so a stage carries twice
+// the tensor work for 1.5 times the bytes.
+//
+// FP8 pair tiles (FP8 with two weight tiles per stage: kWide, or the gated up
+// projection's gate + up tiles) keep one K block's two partial products per
+// TMEM buffer (2 * BM columns), promote them into two register accumulators
+// per epilogue thread, and run one TMA producer warp so that four epilogue
+// warps per TMEM lane quadrant fit the register file at 128 routed rows.
 template <int BM, bool kFP8, int kEpi, bool kWide = false>
 struct Cfg {
   static constexpr bool kSwiglu = kEpi == MOE_EPI_SWIGLU;
   static constexpr bool kPair = kSwiglu || kWide;          // two weight tiles per stage
+  static constexpr bool kFP8Pair = kFP8 && kPair;
   static constexpr int kAccCols = kPair ? 2 * BM : BM;
   // FP8: one buffer per K block, up to all 512 columns, so the MMA can run a
   // whole tile or more ahead of the epilogue; BF16: double-buffered tiles.
-  static constexpr int kNumAcc = kFP8 ? (512 / BM < 32 ? 512 / BM : 32)
+  static constexpr int kNumAcc = kFP8 ? (512 / kAccCols < 32 ? 512 / kAccCols : 32)
                                       : (512 / kAccCols >= 2 ? 2 : 1);
   static constexpr int kTmemNeed = kNumAcc * kAccCols;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
@@ -89,19 +98,23 @@ struct Cfg {
   static constexpr int kATiles = kPair ? 2 : 1;
   static constexpr int kRing = ring_slots(kFP8, BM);
   // TMA producer warps (warp 0 plus warps 7..): two measured best (four were
-  // no faster on any workload and slower on the BF16 FFN)
-  static constexpr int kProducers = 2;
+  // no faster on any workload and slower on the BF16 FFN); FP8 pair tiles: one
+  static constexpr int kProducers = kFP8Pair ? 1 : 2;
   // FP8 with block_m >= 64 and BF16 with block_m >= 128: two epilogue warps per
   // TMEM lane quadrant, each taking half of the tile's columns (routed rows),
   // so two warps on every scheduler share the per-K-block promotion (FP8) or
   // the per-tile stores and reductions (BF16); otherwise one per quadrant
   // (BF16 with block_m 256: four, since its SwiGLU accumulator fills TMEM, so
-  // the tile's epilogue is not overlapped with the next tile's MMAs)
-  static constexpr int kEpiGroups = (!kFP8 && BM >= 256) ? 4
+  // the tile's epilogue is not overlapped with the next tile's MMAs).  FP8
+  // pair tiles: one warp per quadrant for every 32 routed rows.
+  static constexpr int kEpiGroups = kFP8Pair ? (BM >= 32 ? BM / 32 : 1)
+                                  : (!kFP8 && BM >= 256) ? 4
                                   : (kFP8 && BM >= 64) || (!kFP8 && BM >= 128) ? 2 : 1;
   static constexpr int kEpiWarps = 4 * kEpiGroups;
   static constexpr int kEpiCols = BM / kEpiGroups;  // columns promoted by one epilogue warp
-  static constexpr int kWarps = kFirstExtraProducer + kProducers - 1 + 4 * (kEpiGroups - 1);
+  // first warp of the second epilogue group (after the extra producers)
+  static constexpr int kGroup1Warp = kFirstExtraProducer + kProducers - 1;
+  static constexpr int kWarps = kGroup1Warp + 4 * (kEpiGroups - 1);
   static constexpr int kThreads = 32 * kWarps;
   // bytes of one K block of a stage; a stage holds p.sk K blocks laid out as
   // [kATiles][sk] weight tiles, then [sk] activation tiles
@@ -114,12 +127,25 @@ struct Cfg {
   static_assert(kTmemNeed <= 512, "TMEM");
 };
 
-// Bytes of one metadata slot: [kb_per_split][BM] FP8 scale products, then
-// BM token ids and BM route weights.
-__host__ __device__ inline int meta_slot_bytes(bool fp8, int bm, int kb_per_split) {
-  const int n = (fp8 ? kb_per_split * bm : 0) + 2 * bm;
+// Bytes of one metadata slot.  FP8 single tiles: [kb_per_split][BM] scale
+// products a_scale * w_scale; FP8 pair tiles: [kb_per_split][BM] activation
+// scales, then the two weight tiles' scales [2][kb_per_split].  Then BM token
+// ids and BM route weights.
+// Floats of the pair tiles' weight-scale vectors, padded so the token ids
+// that follow stay 16-byte aligned (they are read as 4-int vectors).
+__host__ __device__ inline int pair_sw_floats(int kb_per_split) {
+  return (2 * kb_per_split + 3) & ~3;
+}
+
+__host__ __device__ inline int meta_slot_bytes(bool fp8, int bm, int kb_per_split,
+                                               bool pair = false) {
+  const int n = (fp8 ? kb_per_split * bm + (pair ? pair_sw_floats(kb_per_split) : 0) : 0) + 2 * bm;
   return (n * 4 + 15) & ~15;
 }
+
+// Shared memory of the FP8 SwiGLU epilogue's block amax exchange: per epilogue
+// group, two tile buffers of [4 quadrants][32 routed rows] floats.
+__host__ __device__ constexpr int swiglu_red_bytes(int groups) { return groups * 2 * 4 * 32 * 4; }
 
 // Work items of the queue: with a split tail (p.tail_tiles > 0, one K split)
 // the last tail_tiles output tiles are handed out as tail_parts K parts each
@@ -187,7 +213,10 @@ __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const in
 // ring slot (rr) and the activation scales are token-major ([KB, M]);
 // otherwise the ids are loaded from sorted_route_ids and the scales are
 // compact ([KB, R]), their addresses independent of the ids.
-template <int BM, bool kFP8, int kEpi, bool kGather>
+// FP8 pair tiles (kPair): sc holds the activation scales alone and the two
+// weight tiles' scales follow as sw[2][kb_per_split] (the epilogue forms the
+// products), so the slot stays the size of a single tile's.
+template <int BM, bool kFP8, int kEpi, bool kGather, bool kPair = false, bool kWide = false>
 __device__ __forceinline__ void meta_fill(const GemmParams& p, const TileDesc& d, int lane,
                                           const int* rr, float* sc, int* tok, float* wt) {
   constexpr int kRows = (BM + 31) / 32;  // rows of the tile per lane
@@ -201,8 +230,20 @@ __device__ __forceinline__ void meta_fill(const GemmParams& p, const TileDesc& d
     else
       rid[j] = (kEpi == MOE_EPI_SCATTER && s < d.rows) ? __ldg(p.sorted_route_ids + d.m0 + s) : -1;
   }
+  if constexpr (kFP8 && kPair) {
+    // the two weight tiles' 128-row blocks: adjacent (wide) or gate and up
+    const int nb0 = kWide ? 2 * d.n_tile : d.n_tile;
+    const int nb1 = kWide ? 2 * d.n_tile + 1 : d.n_tile + NB / 2;
+    float* sw = sc + p.kb_per_split * BM;
+    for (int kb = lane; kb < d.nkb; kb += 32) {
+      sw[kb] = __ldg(p.w_scales + (static_cast<size_t>(d.e) * NB + nb0) * p.KB + d.kb0 + kb);
+      sw[p.kb_per_split + kb] =
+          __ldg(p.w_scales + (static_cast<size_t>(d.e) * NB + nb1) * p.KB + d.kb0 + kb);
+    }
+  }
   if constexpr (kFP8) {
     // scale products for up to 16 K blocks at a time, all loads in flight together
+    // (pair tiles: the activation scales alone, vb = 1)
     const float* wsc = p.w_scales + (static_cast<size_t>(d.e) * NB + d.n_tile) * p.KB + d.kb0;
     const size_t a_ld = kGather ? static_cast<size_t>(p.M) : static_cast<size_t>(p.R);
     const float* asc = p.a_scales + static_cast<size_t>(d.kb0) * a_ld + (kGather ? 0 : d.m0);
@@ -219,7 +260,10 @@ __device__ __forceinline__ void meta_fill(const GemmParams& p, const TileDesc& d
       float vb[16];
 #pragma unroll
       for (int kb = 0; kb < 16; ++kb) {
-        vb[kb] = kb0 + kb < d.nkb ? __ldg(wsc + kb0 + kb) : 0.0f;
+        if constexpr (kPair)
+          vb[kb] = 1.0f;
+        else
+          vb[kb] = kb0 + kb < d.nkb ? __ldg(wsc + kb0 + kb) : 0.0f;
 #pragma unroll
         for (int j = 0; j < kRows; ++j) {
           const int s = lane + 32 * j;
@@ -258,7 +302,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_a, const GemmParams p) {
   using C = Cfg<BM, kFP8, kEpi, kWide>;
-  static_assert(!(kWide && (kFP8 || C::kSwiglu || kGather)), "wide tiles: BF16 store / scatter");
+  static_assert(!(kWide && (C::kSwiglu || kGather)), "wide tiles: store / scatter, compact rows");
+  static_assert(!(C::kFP8Pair && kGather), "FP8 pair tiles read compact rows");
   // weight rows of a tile (two weight tiles when wide)
   constexpr int kWRows = kWide ? 2 * kTileN : kTileN;
   extern __shared__ uint8_t smem_raw[];
@@ -266,6 +311,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
   __shared__ __align__(8) uint64_t bar_tfull[C::kNumAcc], bar_tempty[C::kNumAcc];
   __shared__ __align__(8) uint64_t bar_dfull[kMaxRing], bar_dempty[kMaxRing], bar_mfull[kMaxRing];
   __shared__ __align__(8) uint64_t bar_drain;
+  // FP8 SwiGLU: per epilogue group, the four quadrant warps' block-amax exchange
+  __shared__ __align__(8) uint64_t bar_red[4];
   __shared__ TileDesc s_desc[kMaxRing];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
@@ -276,14 +323,20 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
   const int NST = p.num_stages;
   const int SK = p.sk;                                  // K blocks per stage
   const int stage_bytes = SK * C::kStageBytes;
-  const int meta_bytes = meta_slot_bytes(kFP8, BM, p.kb_per_split);
+  const int meta_bytes = meta_slot_bytes(kFP8, BM, p.kb_per_split, C::kFP8Pair);
+  // first int of a metadata slot's token ids (after the FP8 scales)
+  const int tok_off =
+      kFP8 ? p.kb_per_split * BM + (C::kFP8Pair ? pair_sw_floats(p.kb_per_split) : 0) : 0;
   uint8_t* s_meta = smem_gen + NST * stage_bytes;       // C::kRing slots of meta_bytes
   // tile offsets and row offsets of the experts ([E + 1] each) after the ring
   int* s_tile_off = reinterpret_cast<int*>(s_meta + C::kRing * meta_bytes);
   int* s_off = s_tile_off + (p.E + 1);
   // gathered-rows mode: route id of every routed row of each ring slot's tile
-  // ([kRing][BM], -1 past the tile's rows), after the tables
+  // ([kRing][BM], -1 past the tile's rows), after the tables; the FP8 SwiGLU
+  // epilogue's block-amax exchange sits in the same place (neither mode has
+  // the other)
   int* s_rows = s_tile_off + ((2 * (p.E + 1) + 3) & ~3);
+  float* s_red = reinterpret_cast<float*>(s_rows);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -301,6 +354,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
       mbar_init(smem_u32(&bar_mfull[i]), 1);
     }
     mbar_init(smem_u32(&bar_drain), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bar_red[i]), 4);
     s_abort = 0;
     mbar_fence_init();
   }
@@ -326,7 +380,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
       const int kb0 = ks * p.kb_per_split, kb1 = min(p.KB, kb0 + p.kb_per_split);
       if (e < p.E)
         for (int kb = kb0 + lane * p.sk; kb < kb1; kb += 32 * p.sk)
-          tma_prefetch_l2_3d(&tmap_w, 0, e * p.N + nt * kTileN, kb);
+          tma_prefetch_l2_3d(&tmap_w, 0, e * p.N + nt * (kWide ? 2 * kTileN : kTileN), kb);
     }
   }
   // Everything above is independent of the preceding kernel's results.
@@ -634,9 +688,10 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
       const TileDesc d = s_desc[ds];
       if (d.nkb >= 0) {
         float* sc = reinterpret_cast<float*>(s_meta + ds * meta_bytes);
-        int* tok = reinterpret_cast<int*>(sc + (kFP8 ? p.kb_per_split * BM : 0));
+        int* tok = reinterpret_cast<int*>(sc + tok_off);
         float* wt = reinterpret_cast<float*>(tok + BM);
-        meta_fill<BM, kFP8, kEpi, kGather>(p, d, lane, s_rows + ds * BM, sc, tok, wt);
+        meta_fill<BM, kFP8, kEpi, kGather, C::kPair, kWide>(p, d, lane, s_rows + ds * BM, sc, tok,
+                                                            wt);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bar_mfull[ds]));
@@ -645,15 +700,16 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    static_assert(C::kEpiGroups == 1 || kFirstExtraProducer + C::kProducers - 1 == 8,
-                  "the second epilogue group starts at warp 8");
     const int quad = warp & 3;                     // TMEM lane quadrant of this warp
     const int row = quad * 32 + lane;              // weight row within the tile
-    // first column (routed row) of this warp's share of the tile: groups are
-    // warps 2..5, 8..11, 12..15, 16..19
-    const int c_lo = (warp < 8 ? 0 : (warp - 4) / 4) * C::kEpiCols;
+    // epilogue group of this warp (four consecutive warps, one per quadrant):
+    // warps 2..5, then from kGroup1Warp (7 or 8) on, four at a time
+    const int grp = warp < C::kGroup1Warp ? 0 : 1 + (warp - C::kGroup1Warp) / 4;
+    // first column (routed row) of this warp's share of the tile
+    const int c_lo = grp * C::kEpiCols;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + c_lo;
     int ds = 0, acc_n = 0;
+    int ntile = 0;   // tiles finished by this warp (FP8 pair tiles)
     uint32_t dphase = 0;
     bool ok = true;
     for (;;) {
@@ -665,11 +721,174 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
       const TileDesc d = s_desc[ds];
       if (d.nkb < 0) break;
       const float* sc = reinterpret_cast<const float*>(s_meta + ds * meta_bytes);
-      const int* tok = reinterpret_cast<const int*>(sc + (kFP8 ? p.kb_per_split * BM : 0));
+      const int* tok = reinterpret_cast<const int*>(sc + tok_off);
       const float* wt = reinterpret_cast<const float*>(tok + BM);
       const int col = d.n_tile * kWRows + row;  // output column (of the first weight tile)
 
-      if constexpr (kFP8) {
+      if constexpr (C::kFP8Pair) {
+        // Two weight tiles per K block (adjacent tiles, or gate and up): each
+        // thread promotes its weight row of both for its CW routed rows, in
+        // chunks of 8 columns per tile (the accumulators fill the register
+        // budget of 16 epilogue warps).
+        constexpr int CW = C::kEpiCols;
+        static_assert(CW == 16 || CW == 32, "pair-tile columns per warp");
+        float acc_a[CW], acc_b[CW];
+#pragma unroll
+        for (int j = 0; j < CW; ++j) {
+          acc_a[j] = 0.0f;
+          acc_b[j] = 0.0f;
+        }
+        const float* sw = sc + p.kb_per_split * BM;   // weight scales [2][kb_per_split]
+        for (int i = 0; i < d.nkb && ok; ++i) {
+          const int a = acc_n;
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&bar_tfull[a % C::kNumAcc]),
+                                    static_cast<uint32_t>(a / C::kNumAcc) & 1u, &s_abort, tmo))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t base = lane_addr + (a % C::kNumAcc) * C::kAccCols;
+          const float swa = sw[i], swb = sw[p.kb_per_split + i];
+          const float* sav = sc + i * BM + c_lo;     // activation scales of this warp's rows
+          // 8 columns of one tile at a time: [tile][chunk] in order, each load
+          // waited for before its multiply-adds
+#pragma unroll
+          for (int u = 0; u < 2 * (CW / 8); ++u) {
+            const int t = u & 1, c0 = (u >> 1) * 8;
+            float v[8];
+            tmem_ld8(base + t * BM + c0, v);
+            tmem_ld_wait(v);
+            if (u == 2 * (CW / 8) - 1) {             // the K block is in registers: release it
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[a % C::kNumAcc]));
+            }
+            float* acc = t ? acc_b : acc_a;
+            const float wsc = t ? swb : swa;
+#pragma unroll
+            for (int q = 0; q < 8; q += 4) {
+              const float4 s4 = *reinterpret_cast<const float4*>(sav + c0 + q);
+              float f0, f1, f2, f3;                  // a_scale * w_scale, rounded once
+              mul2(f0, f1, s4.x, s4.y, wsc, wsc);
+              mul2(f2, f3, s4.z, s4.w, wsc, wsc);
+              fma2(acc[c0 + q], acc[c0 + q + 1], v[q], v[q + 1], f0, f1);
+              fma2(acc[c0 + q + 2], acc[c0 + q + 3], v[q + 2], v[q + 3], f2, f3);
+            }
+          }
+          ++acc_n;
+        }
+        if (!ok) break;
+        if constexpr (C::kSwiglu) {
+          // h = silu(gate) * up = (g / (1 + exp(-g))) * u in binary32 for this
+          // thread's h column n_tile * 128 + row and routed rows c_lo + j (exp
+          // by the router's fixed sequence; the quotient by the approximate
+          // division, within 2 ulp, whose lack of a slow path keeps the 64
+          // accumulators in registers); then the 1x128 rule over the tile's
+          // 128 h columns, which are the 128 TMEM lanes of the group's four
+          // quadrant warps
+          const int I = p.N / 2;
+          float* h = acc_a;                          // h overwrites the gate accumulator
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            const float e = exp_ieee(-acc_a[j]);     // +inf for g < -88: h = -0
+            h[j] = __fmul_rn(__fdividef(acc_a[j], __fadd_rn(1.0f, e)), acc_b[j]);
+          }
+          // reduce-scatter of the maxima over the warp: lane l ends with the
+          // maximum over its quadrant's 32 h columns of routed row c_lo + l % CW
+          // (the first step, over lane bit 4, reads |h| directly)
+          float m[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if constexpr (CW == 16) {
+              m[j] = fmaxf(fabsf(h[j]), __shfl_xor_sync(0xffffffffu, fabsf(h[j]), 16));
+            } else {
+              const bool hi = (lane & 16) != 0;
+              const float send = fabsf(hi ? h[j] : h[j + 16]);
+              const float keep = fabsf(hi ? h[j + 16] : h[j]);
+              m[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+            }
+          }
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1) {
+            const bool hi = (lane & o) != 0;
+#pragma unroll
+            for (int j = 0; j < o; ++j) {
+              const float send = hi ? m[j] : m[j + o];
+              const float keep = hi ? m[j + o] : m[j];
+              m[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+            }
+          }
+          // ... then over the four quadrant warps (double-buffered by tile)
+          float* red = s_red + (grp * 2 + (ntile & 1)) * 128;   // [4 quadrants][32]
+          if (lane < CW) red[quad * 32 + lane] = m[0];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_red[grp]));
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_red[grp]),
+                                                 static_cast<uint32_t>(ntile) & 1u, &s_abort,
+                                                 tmo))) {
+            ok = false;
+            break;
+          }
+          const int cl = lane % CW;
+          const float amax = fmaxf(fmaxf(red[cl], red[32 + cl]), fmaxf(red[64 + cl], red[96 + cl]));
+          float scale = 0.0f, inv = 0.0f;
+          if (amax > 0.0f) {
+            scale = __fdiv_rn(amax, 448.0f);
+            inv = __fdiv_rn(1.0f, scale);
+          }
+          // block scales [I/128, R] (the quadrant-0 warp writes its group's rows)
+          if (quad == 0 && lane < CW && c_lo + lane < d.rows)
+            p.out_scales[static_cast<size_t>(d.n_tile) * p.R + d.m0 + c_lo + lane] = scale;
+          // codes [R, I]: routed row c_lo + j, h column n_tile * 128 + row
+          uint8_t* hq = static_cast<uint8_t*>(p.out) + static_cast<size_t>(d.m0 + c_lo) * I + col;
+#pragma unroll
+          for (int j = 0; j < CW; j += 2) {
+            const float i0 = __shfl_sync(0xffffffffu, inv, j);
+            const float i1 = __shfl_sync(0xffffffffu, inv, j + 1);
+            const uint16_t q2 = cvt_e4m3x2(__fmul_rn(h[j], i0), __fmul_rn(h[j + 1], i1));
+            // a block whose amax is 0 has all-zero codes
+            if (c_lo + j < d.rows) hq[static_cast<size_t>(j) * I] = i0 > 0.0f ? (q2 & 0xff) : 0;
+            if (c_lo + j + 1 < d.rows)
+              hq[static_cast<size_t>(j + 1) * I] = i1 > 0.0f ? (q2 >> 8) : 0;
+          }
+        } else if constexpr (kEpi == MOE_EPI_SCATTER) {
+          // both weight tiles' outputs of each routed row (columns col and col + 128)
+          float* out = static_cast<float*>(p.out) + col;
+#pragma unroll
+          for (int s0 = 0; s0 < CW; s0 += 4) {
+            if (c_lo + s0 < d.rows) {
+              const int4 t4 = *reinterpret_cast<const int4*>(tok + c_lo + s0);
+              const float4 w4 = *reinterpret_cast<const float4*>(wt + c_lo + s0);
+              const int tk[4] = {t4.x, t4.y, t4.z, t4.w};
+              const float ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                if (c_lo + s0 + j < d.rows) {
+                  float* o = out + static_cast<size_t>(tk[j]) * p.N;
+                  red_add_f32(o, ww[j] * acc_a[s0 + j]);
+                  red_add_f32(o + kTileN, ww[j] * acc_b[s0 + j]);
+                }
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < CW; ++j) {
+            if (c_lo + j < d.rows) {
+              const size_t o = static_cast<size_t>(d.m0 + c_lo + j) * p.N + col;
+              if constexpr (kEpi == MOE_EPI_STORE_BF16) {
+                static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(acc_a[j]);
+                static_cast<__nv_bfloat16*>(p.out)[o + kTileN] = __float2bfloat16_rn(acc_b[j]);
+              } else {
+                static_cast<float*>(p.out)[o] = acc_a[j];
+                static_cast<float*>(p.out)[o + kTileN] = acc_b[j];
+              }
+            }
+          }
+        }
+        ++ntile;
+      } else if constexpr (kFP8) {
         constexpr int CW = C::kEpiCols;
         float acc[CW];
 #pragma unroll
@@ -928,9 +1147,13 @@ GemmVariant variant() {
       C::kStageBytes, C::kThreads};
 }
 
-// Wide tiles: BF16 store / scatter epilogues, block_m 128 or 256.
+// Wide tiles: store / scatter epilogues; BF16 at block_m 128 or 256, FP8 at 128.
 template <int kEpi>
-bool pick_wide(int bm, GemmVariant& v) {
+bool pick_wide(bool fp8, int bm, GemmVariant& v) {
+  if (fp8) {
+    if (bm == 128) { v = variant<128, true, kEpi, false, true>(); return true; }
+    return false;
+  }
   if (bm == 128) { v = variant<128, false, kEpi, false, true>(); return true; }
   if (bm == 256) { v = variant<256, false, kEpi, false, true>(); return true; }
   return false;
@@ -955,11 +1178,22 @@ bool pick_bm(int bm, GemmVariant& v) {
 // gated up projection (the first GEMM of the BF16 forward).
 bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, bool wide, GemmVariant& v) {
   if (wide) {
-    if (fp8 || gather) return false;
-    if (epi == MOE_EPI_SCATTER) return pick_wide<MOE_EPI_SCATTER>(bm, v);
-    if (epi == MOE_EPI_STORE) return pick_wide<MOE_EPI_STORE>(bm, v);
-    if (epi == MOE_EPI_STORE_BF16) return pick_wide<MOE_EPI_STORE_BF16>(bm, v);
+    if (gather) return false;
+    if (epi == MOE_EPI_SCATTER) return pick_wide<MOE_EPI_SCATTER>(fp8, bm, v);
+    if (epi == MOE_EPI_STORE) return pick_wide<MOE_EPI_STORE>(fp8, bm, v);
+    if (epi == MOE_EPI_STORE_BF16) return pick_wide<MOE_EPI_STORE_BF16>(fp8, bm, v);
     return false;
+  }
+  if (fp8 && epi == MOE_EPI_SWIGLU) {
+    // gate + up pair tiles with the SwiGLU + 1x128 re-quantisation epilogue
+    if (gather) return false;
+    switch (bm) {
+      case 16: v = variant<16, true, MOE_EPI_SWIGLU, false>(); return true;
+      case 32: v = variant<32, true, MOE_EPI_SWIGLU, false>(); return true;
+      case 64: v = variant<64, true, MOE_EPI_SWIGLU, false>(); return true;
+      case 128: v = variant<128, true, MOE_EPI_SWIGLU, false>(); return true;
+      default: return false;
+    }
   }
   if (fp8) {
     if (epi == MOE_EPI_SCATTER)
@@ -986,7 +1220,7 @@ bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, bool wide, Gemm
 bool gemm_gather_supported(bool fp8, int epi) { return fp8 || epi == MOE_EPI_SWIGLU; }
 
 bool gemm_wide_supported(bool fp8, int epi, int bm) {
-  return !fp8 && epi != MOE_EPI_SWIGLU && (bm == 128 || bm == 256);
+  return epi != MOE_EPI_SWIGLU && (fp8 ? bm == 128 : (bm == 128 || bm == 256));
 }
 
 int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide) {
@@ -999,8 +1233,14 @@ int gemm_table_bytes(int E) { return (2 * (E + 1) * 4 + 15) & ~15; }
 
 int gemm_rows_bytes(bool fp8, int bm) { return ring_slots(fp8, bm) * bm * 4; }
 
-int gemm_meta_bytes(bool fp8, int bm, int kb_per_split) {
-  return ring_slots(fp8, bm) * meta_slot_bytes(fp8, bm, kb_per_split);
+int gemm_meta_bytes(bool fp8, int bm, int kb_per_split, bool pair) {
+  return ring_slots(fp8, bm) * meta_slot_bytes(fp8, bm, kb_per_split, pair);
+}
+
+int gemm_extra_bytes(bool fp8, int epi, int bm, bool gather) {
+  if (gather) return gemm_rows_bytes(fp8, bm);
+  if (fp8 && epi == MOE_EPI_SWIGLU) return swiglu_red_bytes(bm >= 32 ? bm / 32 : 1);
+  return 0;
 }
 
 cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_a,
@@ -1009,9 +1249,10 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
   GemmVariant v;
   if (!select_gemm_variant(fp8, epi, bm, p.gather != 0, p.wide != 0, v)) return cudaErrorInvalidValue;
   if (p.sk != 1 && p.sk != 2 && p.sk != 4) return cudaErrorInvalidValue;
+  const bool pair = fp8 && (p.wide != 0 || epi == MOE_EPI_SWIGLU);
   const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * p.sk * v.stage_bytes +
-                      gemm_meta_bytes(fp8, bm, p.kb_per_split) + gemm_table_bytes(p.E) +
-                      (p.gather ? gemm_rows_bytes(fp8, bm) : 0);
+                      gemm_meta_bytes(fp8, bm, p.kb_per_split, pair) + gemm_table_bytes(p.E) +
+                      gemm_extra_bytes(fp8, epi, bm, p.gather != 0);
   cudaError_t err = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err == cudaSuccess)

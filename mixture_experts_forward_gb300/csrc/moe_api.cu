@@ -130,8 +130,13 @@ moe_status_t check_gemm(const moe_gemm_args* a) {
   if (a->N % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (fp8) {
     if (a->K % 128 != 0 || a->block_m > 128) return MOE_ERR_UNSUPPORTED;
-    if (a->epilogue == MOE_EPI_SWIGLU) return MOE_ERR_UNSUPPORTED;
     if (a->a_scales == nullptr || a->w_scales == nullptr) return MOE_ERR_INVALID_ARG;
+    if (a->epilogue == MOE_EPI_SWIGLU) {
+      // gate + up tiles of 128 h columns each; codes and block scales out
+      if (a->N % 256 != 0 || a->gather_rows != 0) return MOE_ERR_UNSUPPORTED;
+      if (a->out_scales == nullptr || (reinterpret_cast<uintptr_t>(a->out_scales) & 3u) != 0)
+        return MOE_ERR_INVALID_ARG;
+    }
   } else {
     if (a->K % 64 != 0) return MOE_ERR_UNSUPPORTED;
     if (a->epilogue == MOE_EPI_SWIGLU && a->N % 256 != 0) return MOE_ERR_UNSUPPORTED;
@@ -177,6 +182,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   p.sorted_route_ids = a->sorted_route_ids;
   p.route_weights = a->route_weights;
   p.out = a->out;
+  p.out_scales = a->out_scales;
   p.ctrl = ctrl;
   p.queue_ctr = second ? &ctrl->queue2 : &ctrl->queue;
   p.done_ctr = second ? &ctrl->done2 : &ctrl->done;
@@ -199,13 +205,14 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   p.timeout_ns = g_timeout_ns;
   const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m, p.wide != 0);
   if (stage_bytes <= 0) return MOE_ERR_UNSUPPORTED;
-  const int meta_bytes = gemm_meta_bytes(fp8, a->block_m, p.kb_per_split);
+  const bool pair = fp8 && (p.wide != 0 || a->epilogue == MOE_EPI_SWIGLU);
+  const int meta_bytes = gemm_meta_bytes(fp8, a->block_m, p.kb_per_split, pair);
   p.gather = a->gather_rows;
   p.M = a->M;
   // FP8 weights read once per expert (no row-tile reuse) through the queue:
   // warm L2 with each CTA's likely first weight tile before the layout is known
   p.warm_first = (fp8 && !p.w_reuse && a->sched == MOE_SCHED_QUEUE) ? 1 : 0;
-  const int rows_bytes = p.gather ? gemm_rows_bytes(fp8, a->block_m) : 0;
+  const int rows_bytes = gemm_extra_bytes(fp8, a->epilogue, a->block_m, p.gather != 0);
   // Several K blocks per stage (more bytes per copy instruction, and 128 *
   // sk contiguous bytes of every weight row per copy): the largest of 4, 2, 1
   // that divides a split and still leaves at least three stages.
@@ -289,7 +296,9 @@ bool rows_path(const moe_forward_args* f) {
 // inside the first grouped GEMM.
 bool forward_gathers(const moe_forward_args* f) {
   const bool fp8 = f->dtype == MOE_DTYPE_FP8_E4M3;
-  return f->gather_rows == 1 && !(fp8 && quant_layout_fits(f->M, f->K, f->top_k, f->E));
+  // the FP8 gated FFN's fused SwiGLU up projection reads compact rows only
+  return f->gather_rows == 1 && !(fp8 && quant_layout_fits(f->M, f->K, f->top_k, f->E)) &&
+         !fp8_ffn(f);
 }
 
 WsLayout ws_layout(const moe_forward_args* f) {
@@ -328,12 +337,11 @@ WsLayout ws_layout(const moe_forward_args* f) {
     L.acc = take(R * cols * 2);
   else
     L.acc = take(M * cols * 4);
-  // gated FFN intermediates: BF16 h [R, N]; FP8 the up projection's f32 rows
-  // [R, 2N], then h's codes [R, N] and block scales [N/128, R]
+  // gated FFN intermediates: BF16 h [R, N]; FP8 h's codes [R, N] and block
+  // scales [N/128, R], written by the up projection's epilogue
   if (!fp8) {
     L.h = take(R * N * 2);
   } else if (fp8_ffn(f)) {
-    L.h = take(R * 2 * N * 4);
     L.hq = take(R * N);
     L.hs = take((N / 128) * R * 4);
   }
@@ -444,19 +452,19 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     g.gather_rows = gather ? 1 : 0;
     moe_status_t s;
     if (ffn) {
-      // up projection (gate and up rows) -> f32 rows; SwiGLU + 1x128
-      // re-quantisation; the down projection then reads h like activations
-      float* gu = reinterpret_cast<float*>(ws + L.h);
+      // up projection (gate and up tiles) with the SwiGLU + 1x128
+      // re-quantisation in its epilogue: h's codes and block scales, which the
+      // down projection then reads like activations
       uint8_t* h_q = ws + L.hq;
       float* h_s = reinterpret_cast<float*>(ws + L.hs);
-      g.epilogue = MOE_EPI_STORE;
+      g.epilogue = MOE_EPI_SWIGLU;
       g.N = 2 * N;
-      g.out = gu;
+      g.out = h_q;
+      g.out_scales = h_s;
       g.k_splits = 1;
       s = run_gemm(&g, ctrl, false, stream, pdl);
       if (s != MOE_OK) return s;
-      s = cuda_status(launch_swiglu_quant(gu, R, N, h_q, h_s, device_sms(), stream, pdl));
-      if (s != MOE_OK) return s;
+      g.out_scales = nullptr;
       g.gather_rows = 0;
       g.N = K;
       g.K = N;

@@ -40,6 +40,7 @@ struct GemmParams {
   const int32_t* sorted_route_ids;
   const float* route_weights;
   void* out;
+  float* out_scales;            // FP8 SwiGLU: h block scales [N/256, R]
   Ctrl* ctrl;
   unsigned* queue_ctr;          // tile-queue counter (zero at launch; reset by the last CTA)
   unsigned* done_ctr;
@@ -129,8 +130,11 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
 int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide = false);
 // BF16 store / scatter tiles of two adjacent weight tiles (256 output columns)
 bool gemm_wide_supported(bool fp8, int epi, int bm);
-int gemm_meta_bytes(bool fp8, int bm, int kb_per_split);
+int gemm_meta_bytes(bool fp8, int bm, int kb_per_split, bool pair = false);
 int gemm_rows_bytes(bool fp8, int bm);   // the route-id ring of the gathered-rows mode
+// shared memory after the tables: the gathered-rows ring, or the FP8 SwiGLU
+// epilogue's block-amax exchange
+int gemm_extra_bytes(bool fp8, int epi, int bm, bool gather);
 bool gemm_gather_supported(bool fp8, int epi);
 int gemm_table_bytes(int E);
 

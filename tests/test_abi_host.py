@@ -80,7 +80,11 @@ def _gemm(**kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(block_m=24), L.MOE_ERR_UNSUPPORTED), (dict(block_m=256), L.MOE_ERR_UNSUPPORTED),
     (dict(K=200), L.MOE_ERR_UNSUPPORTED), (dict(N=200), L.MOE_ERR_UNSUPPORTED),
-    (dict(E=2000), L.MOE_ERR_UNSUPPORTED), (dict(epilogue=L.EPI_SWIGLU), L.MOE_ERR_UNSUPPORTED),
+    (dict(E=2000), L.MOE_ERR_UNSUPPORTED),
+    (dict(epilogue=L.EPI_SWIGLU, out_scales=None), L.MOE_ERR_INVALID_ARG),
+    (dict(epilogue=L.EPI_SWIGLU, out_scales=FAKE + 2), L.MOE_ERR_INVALID_ARG),
+    (dict(epilogue=L.EPI_SWIGLU, N=384, out_scales=FAKE), L.MOE_ERR_UNSUPPORTED),
+    (dict(epilogue=L.EPI_SWIGLU, out_scales=FAKE, gather_rows=1), L.MOE_ERR_UNSUPPORTED),
     (dict(a=None), L.MOE_ERR_INVALID_ARG), (dict(a_scales=None), L.MOE_ERR_INVALID_ARG),
     (dict(R=33), L.MOE_ERR_INVALID_ARG), (dict(sorted_route_ids=None), L.MOE_ERR_INVALID_ARG),
     (dict(epilogue=L.EPI_STORE, k_splits=2), L.MOE_ERR_UNSUPPORTED),
@@ -157,8 +161,9 @@ def test_swiglu_quant_argument_errors(lib):
 
 def test_forward_fp8_gated_checks_and_workspace(lib):
     """The FP8 gated FFN needs both projections' codes and scales; its
-    workspace holds the up projection's f32 rows [R, 2N], h's codes [R, N]
-    and scales, and an accumulator as wide as the token features K."""
+    workspace holds h's codes [R, N] and scales (written by the up
+    projection's fused SwiGLU epilogue: no f32 [R, 2N] rows), and an
+    accumulator as wide as the token features K."""
     shape = dict(M=8192, K=3072, N=1536, E=16, top_k=8)
     R = shape["M"] * shape["top_k"]
     a = L.forward_args(dtype=L.DTYPE_FP8, gated=1, **shape)
@@ -170,11 +175,12 @@ def test_forward_fp8_gated_checks_and_workspace(lib):
     a.w2_scales = FAKE
     n = L.workspace_size(a)
     K, N, M = shape["K"], shape["N"], shape["M"]
-    assert n >= R * 2 * N * 4 + R * N + (N // 128) * R * 4 + R * K + M * K * 4
+    assert n >= R * N + (N // 128) * R * 4 + R * K + M * K * 4
+    assert n < R * N + (N // 128) * R * 4 + R * K + M * K * 4 + R * 2 * N * 4
     single = L.forward_args(dtype=L.DTYPE_FP8, **shape)
     single.w = FAKE
     single.w_scales = FAKE
-    assert L.workspace_size(single) < n - R * 2 * N * 4
+    assert L.workspace_size(single) < n
     for bad in (2, -1):
         a.gated = bad
         assert lib.moe_workspace_size(ctypes.byref(a)) == 0
@@ -202,7 +208,7 @@ def test_forward_plan_of_the_gated_fp8_ffn(lib):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(block_m=24), L.MOE_ERR_UNSUPPORTED), (dict(K=200), L.MOE_ERR_UNSUPPORTED),
-    (dict(E=2000), L.MOE_ERR_UNSUPPORTED), (dict(epilogue=L.EPI_SWIGLU), L.MOE_ERR_UNSUPPORTED),
+    (dict(E=2000), L.MOE_ERR_UNSUPPORTED), (dict(epilogue=L.EPI_SWIGLU), L.MOE_ERR_INVALID_ARG),
     (dict(a=None), L.MOE_ERR_INVALID_ARG), (dict(a_scales=None), L.MOE_ERR_INVALID_ARG),
     (dict(R=33), L.MOE_ERR_INVALID_ARG), (dict(sorted_route_ids=None), L.MOE_ERR_INVALID_ARG),
     (dict(epilogue=L.EPI_STORE, k_splits=2), L.MOE_ERR_UNSUPPORTED),

@@ -186,6 +186,74 @@ def test_gemm_fp8_few_ctas_many_tiles():
     _fp8_gemm_case(M=512, K=2048, N=512, E=4, k=2, bm=64, epilogue=L.EPI_SCATTER, num_ctas=8)
 
 
+@pytest.mark.parametrize("epi,sched,ks,ctas", [
+    (L.EPI_SCATTER, L.SCHED_QUEUE, 1, 0), (L.EPI_SCATTER, L.SCHED_STATIC, 1, 0),
+    (L.EPI_SCATTER, L.SCHED_QUEUE, 2, 0), (L.EPI_SCATTER, L.SCHED_QUEUE, 0, 8),
+    (L.EPI_STORE, L.SCHED_QUEUE, 0, 0), (L.EPI_STORE_BF16, L.SCHED_QUEUE, 0, 5)])
+def test_gemm_fp8_wide_tiles(epi, sched, ks, ctas):
+    """128 routed rows against two adjacent 128-row weight tiles per tile (N a
+    multiple of 256): one TMEM buffer per K block holds both tiles' partial
+    products, four epilogue warps per lane quadrant promote them; ragged
+    expert tiles, K splits, few CTAs looping over many tiles."""
+    _fp8_gemm_case(M=700, K=1024, N=512, E=8, k=3, bm=128, epilogue=epi, sched=sched,
+                   k_splits=ks, skew=1.5, num_ctas=ctas)
+
+
+def _e4m3_order(c: np.ndarray) -> np.ndarray:
+    """Signed position of an E4M3 code on the number line; 0x00 and 0x80 both 0."""
+    c = c.astype(np.int32)
+    mag = c & 0x7F
+    return np.where(c & 0x80, -mag, mag)
+
+
+def _fp8_swiglu_case(M, K, I, E, k, bm, sched=L.SCHED_QUEUE, num_ctas=0, skew=1.0, seed=0):
+    """The FP8 SWIGLU epilogue (gate rows [0, I), up rows [I, 2I) of [E, 2I, K])
+    against the oracle's pipeline: binary64 up projection of the same codes
+    rounded to binary32, then its SwiGLU + 1x128 rule.  The device accumulates
+    in fp32 in another order, so an h on an E4M3 rounding boundary may take the
+    neighbouring code: codes equal or one step apart (at most 0.2 %), block
+    scales within 3e-5 relative, dequantised h within the output tolerance."""
+    d = inputs.make_fp8_inputs(dict(M=M, K=K, N=2 * I, E=E, k=k, softcap=0.0, zipf_bias=skew),
+                               seed=seed)
+    rid, _ = oracle.route(d["logits"].numpy(), k)
+    lay = oracle.layout(rid, E, block_m=bm)
+    a_q, a_s = oracle.quant_gather(bits(d["x"]), k, lay["route_slot"])
+    gu = oracle.grouped_gemm_fp8(a_q, a_s, d["w_q"].numpy(), d["w_scales"].numpy(),
+                                 lay["offsets"], threads=THREADS).astype(np.float32)
+    hq_ref, hs_ref = oracle.swiglu_quant(gu)
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    R = M * k
+    h_q = torch.full((R, I), 0x7F, dtype=torch.uint8, device="cuda")
+    h_s = torch.full((I // 128, R), -1.0, device="cuda")
+    ws = L.new_workspace(L.CTRL_BYTES)
+    L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_SWIGLU, a=cu(a_q), a_scales=cu(a_s),
+                   w=d["w_q"].cuda(), w_scales=d["w_scales"].cuda(), offsets=cu(lay["offsets"]),
+                   tile_offsets=cu(lay["tile_offsets"]), out=h_q, out_scales=h_s, ws=ws,
+                   block_m=bm, sched=sched, num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    assert L.get_error(ws) == L.MOE_OK
+    hq, hs = np_(h_q), np_(h_s)
+    assert np.all(np.abs(hs - hs_ref) <= 3e-5 * np.abs(hs_ref)), "h block scales"
+    step = np.abs(_e4m3_order(hq) - _e4m3_order(hq_ref))
+    assert step.max() <= 1, f"h codes off by {step.max()} steps"
+    assert (step > 0).mean() <= 2e-3, f"{(step > 0).mean():.2e} of h codes on the other side"
+    dq = oracle.e4m3_decode_table()
+    h_got = dq[hq].astype(np.float64) * np.repeat(hs.T, 128, axis=1)
+    h_ref = dq[hq_ref].astype(np.float64) * np.repeat(hs_ref.T, 128, axis=1)
+    assert_close(torch.from_numpy(h_got), h_ref, f"fp8 swiglu bm={bm}")
+
+
+@pytest.mark.parametrize("bm", [16, 32, 64, 128])
+def test_gemm_fp8_swiglu_epilogue(bm):
+    _fp8_swiglu_case(M=300, K=512, I=384, E=16, k=4, bm=bm)
+
+
+@pytest.mark.parametrize("sched,ctas", [(L.SCHED_STATIC, 0), (L.SCHED_QUEUE, 6)])
+def test_gemm_fp8_swiglu_schedules(sched, ctas):
+    """Static partition, and six CTAs looping over many 128-row tiles."""
+    _fp8_swiglu_case(M=900, K=1024, I=256, E=6, k=2, bm=128, sched=sched, num_ctas=ctas, skew=2.0)
+
+
 def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, seed=0):
     g = torch.Generator().manual_seed(seed)
     M = R_tokens
