@@ -321,8 +321,9 @@ def bench_ours(args, rank, world, local):
     fl = flops_per_step(kind, c)
     value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
     ms_per_step = total_ms / args.steps
-    # route+layout, quant/gather, GEMM(s), (FP8 FFN: SwiGLU + re-quantise), finalize
-    launches_per_step = {"fp8": 4, "bf16": 5, "fp8ffn": 6}[kind]
+    # route+layout, quant/gather, GEMM(s) (the FP8 FFN's up projection carries
+    # the SwiGLU + re-quantisation), finalize
+    launches_per_step = {"fp8": 4, "bf16": 5, "fp8ffn": 5}[kind]
 
     # routing facts of this batch (for bytes and the roofline)
     ids, _ = L.route(logits, k, softcap=c.get("softcap", 0.0))
@@ -412,21 +413,23 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
         src = "grouped_gemm.cu"
     elif kind == "fp8ffn":
         # the forward's largest kernel: the FP8 up projection (gate and up
-        # rows) storing f32 rows for the SwiGLU + re-quantisation step
+        # tiles) with the fused SwiGLU + 1x128 re-quantisation epilogue
         T, H, I, k = c["T"], c["H"], c["I"], c["k"]
         R = T * k
         a_q, a_s = L.quant_gather(d["x"].to(dev), k, lay["route_slot"])
         w, w_s = d["wup_q"].to(dev), d["wup_s"].to(dev)
-        gu = torch.empty(R, 2 * I, dtype=torch.float32, device=dev)
+        h_q = torch.empty(R, I, dtype=torch.uint8, device=dev)
+        h_s = torch.empty(I // 128, R, dtype=torch.float32, device=dev)
 
         def launch():
-            L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_STORE, a=a_q, a_scales=a_s, w=w,
+            L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_SWIGLU, a=a_q, a_scales=a_s, w=w,
                            w_scales=w_s, offsets=lay["offsets"], tile_offsets=lay["tile_offsets"],
-                           out=gu, ws=ws, block_m=block_m, M=T, top_k=k, sched=sched, k_splits=1)
+                           out=h_q, out_scales=h_s, ws=ws, block_m=block_m, M=T, top_k=k,
+                           sched=sched, k_splits=1)
         alg = touched * (2 * I * H + (2 * I // 128) * (H // 128) * 4) + R * H + (H // 128) * R * 4 \
-            + R * 2 * I * 4
+            + R * I + (I // 128) * R * 4
         fl = 2.0 * R * (2 * I) * H
-        name = "grouped_gemm_kernel<fp8, store>"
+        name = "grouped_gemm_kernel<fp8, swiglu>"
         src = "grouped_gemm.cu"
     else:
         # the forward's largest kernel: the gated up-projection with the SwiGLU

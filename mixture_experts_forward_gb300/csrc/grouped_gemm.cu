@@ -87,6 +87,15 @@ struct Cfg {
   static constexpr bool kSwiglu = kEpi == MOE_EPI_SWIGLU;
   static constexpr bool kPair = kSwiglu || kWide;          // two weight tiles per stage
   static constexpr bool kFP8Pair = kFP8 && kPair;
+  // FP8 pair tiles of 128 routed rows that store their results run
+  // token-major: the routed rows are the MMA's M side (TMEM lanes) and both
+  // weight tiles, contiguous in the stage, its N = 256 side, so each
+  // instruction carries twice the work, each epilogue thread owns one routed
+  // row (one scale per weight tile and K block) and its outputs leave as
+  // 16-byte vectors.  The scatter keeps weight rows on the lanes: a warp's
+  // reduction then covers 32 consecutive columns of one token (4 sectors)
+  // instead of 16 bytes of 32 tokens (32 sectors), which measured faster.
+  static constexpr bool kTok = kFP8Pair && BM == 128 && kEpi != MOE_EPI_SCATTER;
   static constexpr int kAccCols = kPair ? 2 * BM : BM;
   // FP8: one buffer per K block, up to all 512 columns, so the MMA can run a
   // whole tile or more ahead of the epilogue; BF16: double-buffered tiles.
@@ -643,14 +652,24 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
             const uint32_t a_addr = sbase + kb * kATileBytes;
             const uint32_t b_addr = sbase + C::kATiles * SK * kATileBytes + kb * (BM * kRowBytes);
             const uint32_t d_tmem = tmem_base + buf * C::kAccCols;
+            if constexpr (C::kTok) {
+              // M = the 128 routed rows, N = both weight tiles (256 rows,
+              // contiguous because a stage holds one K block)
+              constexpr uint32_t idesc_t = make_idesc(0u, 128u, 256u);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t acc = kFP8 ? (kk > 0) : (i > 0 || kb > 0 || kk > 0);
-              const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32);
-              umma<kFP8>(d_tmem, smem_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
-              if constexpr (C::kPair)
-                umma<kFP8>(d_tmem + BM, smem_desc_sw128(a_addr + SK * kATileBytes + kk * 32), bdesc,
-                           idesc, acc);
+              for (int kk = 0; kk < 4; ++kk)
+                umma<true>(d_tmem, smem_desc_sw128(b_addr + kk * 32),
+                           smem_desc_sw128(a_addr + kk * 32), idesc_t, kk > 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t acc = kFP8 ? (kk > 0) : (i > 0 || kb > 0 || kk > 0);
+                const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32);
+                umma<kFP8>(d_tmem, smem_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
+                if constexpr (C::kPair)
+                  umma<kFP8>(d_tmem + BM, smem_desc_sw128(a_addr + SK * kATileBytes + kk * 32),
+                             bdesc, idesc, acc);
+              }
             }
             if constexpr (kFP8) {
               umma_commit(smem_u32(&bar_tfull[buf]));
@@ -725,7 +744,126 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
       const float* wt = reinterpret_cast<const float*>(tok + BM);
       const int col = d.n_tile * kWRows + row;  // output column (of the first weight tile)
 
-      if constexpr (C::kFP8Pair) {
+      if constexpr (C::kTok) {
+        // Token-major pair tile: TMEM lane = routed row s of the tile, 256
+        // accumulator columns = the two weight tiles' rows.  This warp's 64
+        // columns: store / scatter [64 grp, +64) of tile grp / 2; SwiGLU the
+        // gate columns [32 grp, +32) and the matching up columns [128 + 32 grp,
+        // +32), i.e. h columns n_tile * 128 + 32 grp + j.
+        const int s = row;
+        const uint32_t lrow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+        const float* sw = sc + p.kb_per_split * BM;    // weight scales [2][kb_per_split]
+        float acc[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+        for (int i = 0; i < d.nkb && ok; ++i) {
+          const int a = acc_n;
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&bar_tfull[a % C::kNumAcc]),
+                                    static_cast<uint32_t>(a / C::kNumAcc) & 1u, &s_abort, tmo))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t base = lrow + (a % C::kNumAcc) * C::kAccCols;
+          const float sa = sc[i * BM + s];             // this row's activation scale
+          const float fa = __fmul_rn(sa, sw[i]);       // a_scale * w_scale, rounded once
+          const float fb = __fmul_rn(sa, sw[p.kb_per_split + i]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c0 = C::kSwiglu ? (u < 2 ? 32 * grp + 16 * u : 128 + 32 * grp + 16 * (u - 2))
+                                      : 64 * grp + 16 * u;
+            const float f = C::kSwiglu ? (u < 2 ? fa : fb) : (grp < 2 ? fa : fb);
+            float v[16];
+            tmem_ld16(base + c0, v);
+            tmem_ld_wait(v);
+            if (u == 3) {                              // the K block is in registers: release it
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[a % C::kNumAcc]));
+            }
+#pragma unroll
+            for (int j = 0; j < 16; j += 2)
+              fma2(acc[16 * u + j], acc[16 * u + j + 1], v[j], v[j + 1], f, f);
+          }
+          ++acc_n;
+        }
+        if (!ok) break;
+        const bool live = s < d.rows;
+        if constexpr (C::kSwiglu) {
+          // h = silu(gate) * up in binary32 (exp by the router's sequence, the
+          // quotient by the approximate division, within 2 ulp), into acc[0, 32)
+          const int I = p.N / 2;
+          float mx = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float e = exp_ieee(-acc[j]);         // +inf for g < -88: h = -0
+            acc[j] = __fmul_rn(__fdividef(acc[j], __fadd_rn(1.0f, e)), acc[32 + j]);
+            mx = fmaxf(mx, fabsf(acc[j]));
+          }
+          // the row's 1x128 block = its 32 h columns in each of the quadrant's
+          // four group warps: one exchange through shared memory (double-
+          // buffered by tile) under a bounded mbarrier wait
+          float* red = s_red + ((ntile & 1) * 4 + quad) * 128;   // [4 groups][32 lanes]
+          red[grp * 32 + lane] = mx;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bar_red[quad]));
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_red[quad]),
+                                                 static_cast<uint32_t>(ntile) & 1u, &s_abort,
+                                                 tmo))) {
+            ok = false;
+            break;
+          }
+          const float amax =
+              fmaxf(fmaxf(red[lane], red[32 + lane]), fmaxf(red[64 + lane], red[96 + lane]));
+          uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          float scale = 0.0f;
+          if (amax > 0.0f) {
+            scale = __fdiv_rn(amax, 448.0f);
+            const float inv = __fdiv_rn(1.0f, scale);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t c01 = cvt_e4m3x2(__fmul_rn(acc[4 * q], inv), __fmul_rn(acc[4 * q + 1], inv));
+              const uint32_t c23 =
+                  cvt_e4m3x2(__fmul_rn(acc[4 * q + 2], inv), __fmul_rn(acc[4 * q + 3], inv));
+              w[q] = c01 | (c23 << 16);
+            }
+          }
+          if (live) {
+            if (grp == 0) p.out_scales[static_cast<size_t>(d.n_tile) * p.R + d.m0 + s] = scale;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
+                                                  static_cast<size_t>(d.m0 + s) * I +
+                                                  d.n_tile * kTileN + 32 * grp);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+        } else if (live) {
+          const int c_out = d.n_tile * 2 * kTileN + 64 * grp;   // first output column
+          if constexpr (kEpi == MOE_EPI_SCATTER) {
+            const float wv = wt[s];
+            float* o = static_cast<float*>(p.out) + static_cast<size_t>(tok[s]) * p.N + c_out;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4)
+              red_add_v4_f32(o + j, wv * acc[j], wv * acc[j + 1], wv * acc[j + 2], wv * acc[j + 3]);
+          } else if constexpr (kEpi == MOE_EPI_STORE_BF16) {
+            uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                static_cast<size_t>(d.m0 + s) * p.N + c_out);
+#pragma unroll
+            for (int j = 0; j < 64; j += 8) {
+              __nv_bfloat162 b[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) b[q] = __floats2bfloat162_rn(acc[j + 2 * q], acc[j + 2 * q + 1]);
+              o[j / 8] = *reinterpret_cast<const uint4*>(b);
+            }
+          } else {
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) +
+                                                  static_cast<size_t>(d.m0 + s) * p.N + c_out);
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) o[j / 4] = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+          }
+        }
+        ++ntile;
+      } else if constexpr (C::kFP8Pair) {
         // Two weight tiles per K block (adjacent tiles, or gate and up): each
         // thread promotes its weight row of both for its CW routed rows, in
         // chunks of 8 columns per tile (the accumulators fill the register

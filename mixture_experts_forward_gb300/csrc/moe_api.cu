@@ -220,6 +220,10 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   p.sk = 1;
   for (int sk = 4; sk >= 2; sk /= 2)
     if (p.kb_per_split % sk == 0 && avail / (sk * stage_bytes) >= 3) { p.sk = sk; break; }
+  // FP8 pair tiles of 128 routed rows that store their results feed both
+  // weight tiles to one MMA as a single 256-row operand, so a stage holds one
+  // K block (the tiles adjacent)
+  if (pair && a->block_m == 128 && a->epilogue != MOE_EPI_SCATTER) p.sk = 1;
   int stages = avail / (p.sk * stage_bytes);
   if (stages > 16) stages = 16;
   if (stages < 2) return MOE_ERR_UNSUPPORTED;

@@ -311,6 +311,13 @@ __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v));
 }
 
+// Four consecutive fp32 reductions in one 16-byte vector operation (p 16-byte aligned).
+__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // (d0, d1) = (a0·b0 + d0, a1·b1 + d1): one packed fp32 multiply-add
 // (fma.rn.f32x2), each half rounded exactly as a scalar fmaf.
 __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
