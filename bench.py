@@ -516,7 +516,7 @@ def stored_traffic(src_name: str, kernel: str, config_name: str):
     j = json.load(open(p))
     src = os.path.join(ROOT, "mixture_experts_forward_gb300", "csrc", src_name)
     sha = code_sha(src)
-    e = j.get(kernel)
+    e = j.get(f"{kernel}@{config_name}")
     if not e or e.get("source_sha") != sha or e.get("config") != config_name:
         return None
     return e.get("dram_bytes_per_launch")
