@@ -43,7 +43,6 @@
 // MMAs, frees its TMEM and returns.
 #include <cuda_bf16.h>
 
-#include "ieee_math.cuh"
 #include "moe_internal.cuh"
 #include "quant_common.cuh"
 
@@ -791,13 +790,15 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
         if (!ok) break;
         const bool live = s < d.rows;
         if constexpr (C::kSwiglu) {
-          // h = silu(gate) * up in binary32 (exp by the router's sequence, the
-          // quotient by the approximate division, within 2 ulp), into acc[0, 32)
+          // h = silu(gate) * up in binary32 with the fast exponential and
+          // division (each within a few ulp; the tile end is on the MMA's
+          // critical path, since TMEM holds only two K blocks of the next
+          // tile), into acc[0, 32)
           const int I = p.N / 2;
           float mx = 0.0f;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float e = exp_ieee(-acc[j]);         // +inf for g < -88: h = -0
+            const float e = __expf(-acc[j]);           // +inf for very negative g: h = -0
             acc[j] = __fmul_rn(__fdividef(acc[j], __fadd_rn(1.0f, e)), acc[32 + j]);
             mx = fmaxf(mx, fabsf(acc[j]));
           }
@@ -919,17 +920,16 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
         if (!ok) break;
         if constexpr (C::kSwiglu) {
           // h = silu(gate) * up = (g / (1 + exp(-g))) * u in binary32 for this
-          // thread's h column n_tile * 128 + row and routed rows c_lo + j (exp
-          // by the router's fixed sequence; the quotient by the approximate
-          // division, within 2 ulp, whose lack of a slow path keeps the 64
-          // accumulators in registers); then the 1x128 rule over the tile's
-          // 128 h columns, which are the 128 TMEM lanes of the group's four
-          // quadrant warps
+          // thread's h column n_tile * 128 + row and routed rows c_lo + j (the
+          // fast exponential and division, each within a few ulp; the IEEE
+          // division's slow path would push the 64 accumulators out of
+          // registers); then the 1x128 rule over the tile's 128 h columns,
+          // which are the 128 TMEM lanes of the group's four quadrant warps
           const int I = p.N / 2;
           float* h = acc_a;                          // h overwrites the gate accumulator
 #pragma unroll
           for (int j = 0; j < CW; ++j) {
-            const float e = exp_ieee(-acc_a[j]);     // +inf for g < -88: h = -0
+            const float e = __expf(-acc_a[j]);       // +inf for very negative g: h = -0
             h[j] = __fmul_rn(__fdividef(acc_a[j], __fadd_rn(1.0f, e)), acc_b[j]);
           }
           // reduce-scatter of the maxima over the warp: lane l ends with the
