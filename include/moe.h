@@ -78,6 +78,14 @@ const char* moe_status_string(moe_status_t s);
 /* Number of streaming multiprocessors of the current device (0 on error). */
 int moe_num_sms(void);
 
+/* Clusters of two CTAs that can be resident at once on the current device
+ * for the FP8 scatter GEMM at block_m 128 with N a multiple of 256, whose
+ * 256-row weight tiles are each computed by a CTA pair (tcgen05 MMAs with
+ * M = 256 spanning both SMs).  0: that form is unavailable (or on error) and
+ * those GEMMs run the single-CTA form.  The grid of such a GEMM is the even
+ * number of CTAs min(num_ctas or the SM count, 2 x this). */
+int moe_gemm_cta_pairs(void);
+
 /* Name and text of the CUDA error behind the calling thread's most recent
  * MOE_ERR_CUDA ("" if none); a static per-thread buffer. */
 const char* moe_last_cuda_error(void);
@@ -128,7 +136,7 @@ moe_status_t moe_quant_gather(const void* x, int M, int K, int top_k,
 typedef struct {
   moe_dtype_t dtype;          /* FP8_E4M3 (blockwise scales) or BF16 */
   moe_epilogue_t epilogue;    /* SCATTER, STORE, SWIGLU or STORE_BF16 */
-  moe_sched_t sched;          /* QUEUE or STATIC */
+  moe_sched_t sched;          /* QUEUE or STATIC (CTA pairs: a fixed round-robin order) */
   int block_m;                /* routed rows per tile: 16..256, multiple of 16
                                  (FP8: at most 128) */
   int E, N, K;                /* weights are [E, N, K] */
@@ -144,7 +152,12 @@ typedef struct {
   const float* route_weights; /* SCATTER: [M*top_k] */
   void* out;                  /* see moe_epilogue_t */
   int k_splits;               /* FP8 SCATTER: K split into this many tiles (0 = auto) */
-  int num_ctas;               /* persistent CTAs (0 = one per SM) */
+  int num_ctas;               /* persistent CTAs (0 = one per SM).  FP8 SCATTER with
+                                 block_m 128, N a multiple of 256 and gather_rows 0 runs
+                                 clusters of two CTAs (moe_gemm_cta_pairs), each pair
+                                 walking every (G/2)-th 256-row tile in a fixed order: the
+                                 grid G is then num_ctas rounded down to even and capped
+                                 at twice the resident pairs (num_ctas 1: single CTAs) */
   int gather_rows;            /* 0: `a` holds the expert-compact rows [R, K] (FP8 a_scales
                                  [K/128, R]).  1: `a` is token-major [M, K] and the kernel
                                  gathers compact slot s from row sorted_route_ids[s] / top_k

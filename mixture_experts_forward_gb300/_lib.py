@@ -24,7 +24,7 @@ EXPORTS = ["moe_status_string", "moe_num_sms", "moe_route", "moe_layout", "moe_q
            "moe_grouped_gemm", "moe_scatter", "moe_workspace_size", "moe_forward",
            "moe_forward_host", "moe_get_error", "moe_debug_set_pipeline_fault", "moe_forward_plan",
            "moe_last_cuda_error", "moe_grouped_gemm_noalloc", "moe_swiglu_quant",
-           "moe_forward_workspace_map"]
+           "moe_forward_workspace_map", "moe_gemm_cta_pairs"]
 WS_NONE = (1 << 64) - 1   # MOE_WS_NONE
 
 
@@ -82,6 +82,7 @@ def lib():
         L.moe_status_string.argtypes = [I]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_num_sms.restype = I
+        L.moe_gemm_cta_pairs.restype = I
         L.moe_last_cuda_error.restype = ctypes.c_char_p
         L.moe_route.argtypes = [P, I, I, I, F, I, P, P, P]
         L.moe_layout.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P]
@@ -102,7 +103,7 @@ def lib():
         L.moe_debug_set_pipeline_fault.argtypes = [I, ctypes.c_uint64]
         for name in EXPORTS:
             if name not in ("moe_status_string", "moe_num_sms", "moe_workspace_size",
-                            "moe_last_cuda_error"):
+                            "moe_last_cuda_error", "moe_gemm_cta_pairs"):
                 getattr(L, name).restype = I
         _lib = L
     return _lib
@@ -319,3 +320,8 @@ def debug_set_pipeline_fault(drop_producer: bool, timeout_ns: int = 0):
 
 def num_sms() -> int:
     return lib().moe_num_sms()
+
+
+def gemm_cta_pairs() -> int:
+    """CTA pairs resident at once for the FP8 scatter GEMM at block_m 128 (0: not used)."""
+    return lib().moe_gemm_cta_pairs()

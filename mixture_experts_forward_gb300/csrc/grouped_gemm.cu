@@ -81,7 +81,17 @@ struct TileDesc {
 // TMEM buffer (2 * BM columns), promote them into two register accumulators
 // per epilogue thread, and run one TMA producer warp so that four epilogue
 // warps per TMEM lane quadrant fit the register file at 128 routed rows.
-template <int BM, bool kFP8, int kEpi, bool kWide = false>
+//
+// CTA pairs (kCta2; FP8 scatter at 128 routed rows): a cluster of two CTAs on
+// two SMs computes one tile of 256 weight rows x 128 routed rows with
+// tcgen05.mma.cta_group::2 (M = 256).  Each CTA stages its own 128 weight rows
+// and half of the routed rows (64) and holds its weight rows' 128 x 128
+// accumulator in its own TMEM, so a K block's buffer is 128 columns (four in
+// TMEM) and a stage 24 KB per K block: twice the K blocks in flight per SM of
+// the single-CTA pair tile, for the same tensor work per SM.  The even CTA
+// issues every MMA; its mbarriers count both CTAs' copies and both CTAs'
+// epilogue releases.
+template <int BM, bool kFP8, int kEpi, bool kWide = false, bool kCta2 = false>
 struct Cfg {
   static constexpr bool kSwiglu = kEpi == MOE_EPI_SWIGLU;
   static constexpr bool kPair = kSwiglu || kWide;          // two weight tiles per stage
@@ -107,7 +117,7 @@ struct Cfg {
   static constexpr int kRing = ring_slots(kFP8, BM);
   // TMA producer warps (warp 0 plus warps 7..): two measured best (four were
   // no faster on any workload and slower on the BF16 FFN); FP8 pair tiles: one
-  static constexpr int kProducers = kFP8Pair ? 1 : 2;
+  static constexpr int kProducers = (kFP8Pair || kCta2) ? 1 : 2;
   // FP8 with block_m >= 64 and BF16 with block_m >= 128: two epilogue warps per
   // TMEM lane quadrant, each taking half of the tile's columns (routed rows),
   // so two warps on every scheduler share the per-K-block promotion (FP8) or
@@ -116,6 +126,7 @@ struct Cfg {
   // the tile's epilogue is not overlapped with the next tile's MMAs).  FP8
   // pair tiles: one warp per quadrant for every 32 routed rows.
   static constexpr int kEpiGroups = kFP8Pair ? (BM >= 32 ? BM / 32 : 1)
+                                  : kCta2 ? 4
                                   : (!kFP8 && BM >= 256) ? 4
                                   : (kFP8 && BM >= 64) || (!kFP8 && BM >= 128) ? 2 : 1;
   static constexpr int kEpiWarps = 4 * kEpiGroups;
@@ -126,13 +137,16 @@ struct Cfg {
   static constexpr int kThreads = 32 * kWarps;
   // bytes of one K block of a stage; a stage holds p.sk K blocks laid out as
   // [kATiles][sk] weight tiles, then [sk] activation tiles
-  static constexpr int kStageBytes = kATiles * kATileBytes + BM * kRowBytes;
+  // routed rows of a stage (CTA pairs: this CTA's half)
+  static constexpr int kBRows = kCta2 ? BM / 2 : BM;
+  static constexpr int kStageBytes = kATiles * kATileBytes + kBRows * kRowBytes;
   // FP8 epilogue: K blocks whose partials are loaded before one wait (<= 64 columns)
   static constexpr int kKbGroup = BM <= 64 ? 64 / BM : 1;
   static constexpr int kLdCols = BM <= 64 ? BM : 64;   // columns per load wave
   static_assert(BM % 16 == 0 && BM >= 16 && BM <= 256, "block_m");
   static_assert(!kFP8 || BM <= 128, "FP8 block_m <= 128");
   static_assert(kTmemNeed <= 512, "TMEM");
+  static_assert(!kCta2 || (kFP8 && BM == 128 && !kPair && kEpi == MOE_EPI_SCATTER), "CTA pairs");
 };
 
 // Bytes of one metadata slot.  FP8 single tiles: [kb_per_split][BM] scale
@@ -305,15 +319,16 @@ __device__ __forceinline__ void meta_fill(const GemmParams& p, const TileDesc& d
   }
 }
 
-template <int BM, bool kFP8, int kEpi, bool kGather, bool kWide>
-__global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
+template <int BM, bool kFP8, int kEpi, bool kGather, bool kWide, bool kCta2>
+__global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_a, const GemmParams p) {
-  using C = Cfg<BM, kFP8, kEpi, kWide>;
+  using C = Cfg<BM, kFP8, kEpi, kWide, kCta2>;
+  static_assert(!(kCta2 && kGather), "CTA pairs read compact rows");
   static_assert(!(kWide && (C::kSwiglu || kGather)), "wide tiles: store / scatter, compact rows");
   static_assert(!(C::kFP8Pair && kGather), "FP8 pair tiles read compact rows");
-  // weight rows of a tile (two weight tiles when wide)
-  constexpr int kWRows = kWide ? 2 * kTileN : kTileN;
+  // weight rows of a tile (two weight tiles when wide or split over a CTA pair)
+  constexpr int kWRows = (kWide || kCta2) ? 2 * kTileN : kTileN;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_tfull[C::kNumAcc], bar_tempty[C::kNumAcc];
@@ -326,6 +341,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA pairs: 0 for the CTA that issues the MMAs, 1 for its peer
+  const uint32_t rank = kCta2 ? cluster_ctarank() : 0u;
   const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* smem_gen = smem_raw + (smem_base - smem_u32(smem_raw));
   const int NST = p.num_stages;
@@ -353,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
     }
     for (int i = 0; i < C::kNumAcc; ++i) {
       mbar_init(smem_u32(&bar_tfull[i]), 1);
-      mbar_init(smem_u32(&bar_tempty[i]), C::kEpiWarps);
+      mbar_init(smem_u32(&bar_tempty[i]), kCta2 ? 2 * C::kEpiWarps : C::kEpiWarps);
     }
     for (int i = 0; i < C::kRing; ++i) {
       mbar_init(smem_u32(&bar_dfull[i]), 1);
@@ -371,10 +388,16 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
     tma_prefetch_desc(&tmap_a);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
-    tmem_relinquish();
+    if constexpr (kCta2) {
+      // one warp of each CTA of the pair: the same columns in both TMEMs
+      tmem_alloc_pair(smem_u32(&s_tmem), C::kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&s_tmem), C::kTmemCols);
+      tmem_relinquish();
+    }
   }
-  if (p.warm_first > 0 && warp == 0) {
+  if (!kCta2 && p.warm_first > 0 && warp == 0) {
     // The queue hands CTA c tile c first and tiles c + G, c + 2G ... mostly
     // next (G CTAs).  When every expert has a single row tile (small batches),
     // tile t is expert t / (n_tiles * k_splits); its weight rows do not depend
@@ -400,6 +423,9 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
   cp_async_wait_all();
   tc_fence_before();
   __syncthreads();
+  // CTA pairs: both CTAs' mbarriers are initialised (and their TMEM
+  // allocated) before either CTA signals the other's
+  if constexpr (kCta2) cluster_sync();
   tc_fence_after();
   // The dependent kernel (the forward's finalize) may become resident now;
   // its griddepcontrol.wait still waits for this grid to complete.
@@ -444,6 +470,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
     // tile's first stage has been issued, so the atomic's round trip overlaps
     // that tile's loads instead of delaying them
     int queued = p.sched == MOE_SCHED_QUEUE ? c : -1;
+    // CTA pairs: both CTAs walk the same list, tiles c/2, c/2 + G/2, ...
+    int rr_i = 0;
     bool claim = false;             // lane 0 of warp 0: the next tile is still to be claimed
     // Gathered rows: warp 0 loads each tile's route ids (kRpl per lane) and
     // puts them in the tile's ring slot with its descriptor.  The queue's next
@@ -464,7 +492,11 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
         } else {
           int t = -1;
           if (lane == 0) {
-            if (p.sched == MOE_SCHED_QUEUE) {
+            if (kCta2) {
+              const int t2 = (c >> 1) + rr_i * (G >> 1);
+              ++rr_i;
+              t = t2 < total_tiles ? t2 : -1;
+            } else if (p.sched == MOE_SCHED_QUEUE) {
               t = queued < total_tiles ? queued : -1;
               claim = t >= 0;
             } else {
@@ -529,14 +561,16 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
       const int* rr = s_rows + ds * BM;   // this tile's route ids (gathered rows)
       if (++ds == C::kRing) { ds = 0; dphase ^= 1u; }
       if (d.nkb < 0) break;
-      const int w_row = d.e * p.N + d.n_tile * kWRows;
+      const int w_row = d.e * p.N + d.n_tile * kWRows + (kCta2 ? static_cast<int>(rank) * kTileN : 0);
       const int w_pair = C::kSwiglu ? p.N / 2 : kTileN;  // row offset of the second weight tile
       for (int i = 0; i < d.nkb; i += SK) {
         if (q % nprod == pw) {
           const uint32_t full = smem_u32(&bar_full[stage]);
           if (lane == 0) {
             got = mbar_wait(smem_u32(&bar_empty[stage]), phase ^ 1u, &s_abort, tmo);
-            if (got && !p.drop_producer) mbar_arrive_expect_tx(full, stage_bytes);
+            // CTA pairs: the even CTA's barrier counts both CTAs' bytes
+            if (got && !p.drop_producer && rank == 0)
+              mbar_arrive_expect_tx(full, kCta2 ? 2 * stage_bytes : stage_bytes);
           }
           if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
           q_own = q;
@@ -545,7 +579,16 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
             // box spans SK K blocks (a box running past K reads the fill value)
             const uint32_t sa = smem_base + stage * stage_bytes;
             const int kb = d.kb0 + i;
-            if constexpr (!kGather) {
+            if constexpr (kCta2) {
+              // this CTA's weight rows and its half of the routed rows, both
+              // counted on the even CTA's barrier
+              const uint32_t full0 = mapa_shared(full, 0);
+              if (lane == 0)
+                tma_load_3d_pair(sa, &tmap_w, full0, 0, w_row, kb, pol_w);
+              else if (lane == 1)
+                tma_load_3d_pair(sa + SK * kATileBytes, &tmap_a, full0, 0,
+                                 d.m0 + static_cast<int>(rank) * C::kBRows, kb, pol_a);
+            } else if constexpr (!kGather) {
               // one if / else-if chain: the boxes go out from their lanes as one instruction
               if (lane < C::kATiles)
                 tma_load_3d(sa + lane * SK * kATileBytes, &tmap_w, full, 0, w_row + lane * w_pair,
@@ -611,14 +654,32 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
       // loads it issued into the ring's last pass (global stages after
       // q - NST, whose slots are not refilled) have landed, so no copy is
       // still writing shared memory when the CTA exits.
+      // CTA pairs: a copy counts on the even CTA's barrier, so each CTA waits
+      // instead until the MMAs that read the stage have completed
       if (!p.drop_producer) {
         for (int qq = q_own; qq >= 0 && qq > q - NST; qq -= nprod)
-          mbar_wait_drain(smem_u32(&bar_full[qq % NST]), static_cast<uint32_t>(qq / NST) & 1u, tmo);
+          mbar_wait_drain(smem_u32(kCta2 ? &bar_empty[qq % NST] : &bar_full[qq % NST]),
+                          static_cast<uint32_t>(qq / NST) & 1u, tmo);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (kCta2 && rank != 0 && lane == 0) {
+      // the peer of a CTA pair issues nothing: it only retires the descriptors
+      int ds = 0;
+      uint32_t dphase = 0;
+      for (;;) {
+        if (!mbar_wait(smem_u32(&bar_dfull[ds]), dphase, &s_abort, tmo)) {
+          set_error(p.ctrl, MOE_ERR_TIMEOUT, 2);
+          s_abort = 1;
+          break;
+        }
+        const int nkb = s_desc[ds].nkb;
+        mbar_arrive(smem_u32(&bar_dempty[ds]));
+        if (++ds == C::kRing) { ds = 0; dphase ^= 1u; }
+        if (nkb < 0) break;
+      }
+    } else if (lane == 0) {
       constexpr uint32_t idesc = make_idesc(kFP8 ? 0u : 1u, 128u, static_cast<uint32_t>(BM));
       int stage = 0, ds = 0, acc_n = 0;
       uint32_t phase = 0, dphase = 0;
@@ -649,37 +710,48 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
               tc_fence_after();
             }
             const uint32_t a_addr = sbase + kb * kATileBytes;
-            const uint32_t b_addr = sbase + C::kATiles * SK * kATileBytes + kb * (BM * kRowBytes);
+            const uint32_t b_addr =
+                sbase + C::kATiles * SK * kATileBytes + kb * (C::kBRows * kRowBytes);
             const uint32_t d_tmem = tmem_base + buf * C::kAccCols;
-            if constexpr (C::kTok) {
+            // descriptor low words of this K block's operands (a K step adds 2)
+            const uint32_t alo = smem_desc_lo(a_addr), blo = smem_desc_lo(b_addr);
+            if constexpr (kCta2) {
+              // M = 256 weight rows (128 per CTA), N = 128 routed rows (64 per CTA)
+              constexpr uint32_t idesc_p = make_idesc(0u, 256u, 128u);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_lo<true, true>(d_tmem, alo + 2 * kk, blo + 2 * kk, idesc_p, kk > 0 ? 1u : 0u);
+            } else if constexpr (C::kTok) {
               // M = the 128 routed rows, N = both weight tiles (256 rows,
               // contiguous because a stage holds one K block)
               constexpr uint32_t idesc_t = make_idesc(0u, 128u, 256u);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma<true>(d_tmem, smem_desc_sw128(b_addr + kk * 32),
-                           smem_desc_sw128(a_addr + kk * 32), idesc_t, kk > 0 ? 1u : 0u);
+                umma_lo<true>(d_tmem, blo + 2 * kk, alo + 2 * kk, idesc_t, kk > 0 ? 1u : 0u);
             } else {
+              const uint32_t alo2 = smem_desc_lo(a_addr + SK * kATileBytes);  // second weight tile
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t acc = kFP8 ? (kk > 0) : (i > 0 || kb > 0 || kk > 0);
-                const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32);
-                umma<kFP8>(d_tmem, smem_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
+                umma_lo<kFP8>(d_tmem, alo + 2 * kk, blo + 2 * kk, idesc, acc);
                 if constexpr (C::kPair)
-                  umma<kFP8>(d_tmem + BM, smem_desc_sw128(a_addr + SK * kATileBytes + kk * 32),
-                             bdesc, idesc, acc);
+                  umma_lo<kFP8>(d_tmem + BM, alo2 + 2 * kk, blo + 2 * kk, idesc, acc);
               }
             }
             if constexpr (kFP8) {
-              umma_commit(smem_u32(&bar_tfull[buf]));
+              if constexpr (kCta2) umma_commit_pair(smem_u32(&bar_tfull[buf]), 3);
+              else umma_commit(smem_u32(&bar_tfull[buf]));
               ++acc_n;
             }
           }
           if (!ok) break;
-          umma_commit(smem_u32(&bar_empty[stage]));
-          if (!kFP8 && i + nk >= d.nkb) {
-            umma_commit(smem_u32(&bar_tfull[buf]));
-            ++acc_n;
+          if constexpr (kCta2) umma_commit_pair(smem_u32(&bar_empty[stage]), 3);
+          else umma_commit(smem_u32(&bar_empty[stage]));
+          if constexpr (!kFP8) {
+            if (i + nk >= d.nkb) {
+              umma_commit(smem_u32(&bar_tfull[buf]));
+              ++acc_n;
+            }
           }
           if (++stage == NST) { stage = 0; phase ^= 1u; }
         }
@@ -690,7 +762,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
         s_abort = 1;
       }
       // drain: every MMA issued above has completed before TMEM is freed
-      umma_commit(smem_u32(&bar_drain));
+      if constexpr (kCta2) umma_commit_pair(smem_u32(&bar_drain), 1);
+      else umma_commit(smem_u32(&bar_drain));
       mbar_wait(smem_u32(&bar_drain), 0u, &s_abort, tmo);
     }
   } else if (warp == kMetaWarp) {
@@ -708,7 +781,10 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
         float* sc = reinterpret_cast<float*>(s_meta + ds * meta_bytes);
         int* tok = reinterpret_cast<int*>(sc + tok_off);
         float* wt = reinterpret_cast<float*>(tok + BM);
-        meta_fill<BM, kFP8, kEpi, kGather, C::kPair, kWide>(p, d, lane, s_rows + ds * BM, sc, tok,
+        // CTA pairs: this CTA's 128-row weight block of the 256-row tile
+        TileDesc dm = d;
+        if constexpr (kCta2) dm.n_tile = 2 * d.n_tile + static_cast<int>(rank);
+        meta_fill<BM, kFP8, kEpi, kGather, C::kPair, kWide>(p, dm, lane, s_rows + ds * BM, sc, tok,
                                                             wt);
       }
       __syncwarp();
@@ -741,7 +817,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
       const float* sc = reinterpret_cast<const float*>(s_meta + ds * meta_bytes);
       const int* tok = reinterpret_cast<const int*>(sc + tok_off);
       const float* wt = reinterpret_cast<const float*>(tok + BM);
-      const int col = d.n_tile * kWRows + row;  // output column (of the first weight tile)
+      // output column (of the first weight tile; CTA pairs: of this CTA's half)
+      const int col = d.n_tile * kWRows + (kCta2 ? static_cast<int>(rank) * kTileN : 0) + row;
 
       if constexpr (C::kTok) {
         // Token-major pair tile: TMEM lane = routed row s of the tile, 256
@@ -1064,9 +1141,15 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
                 tmem_ld16(base + (ch + 1) * kCh + 16, *reinterpret_cast<float(*)[16]>(nxt + 16));
               } else {
                 // every chunk of this K block is in registers: hand the buffer back
+                // (CTA pairs: to the even CTA, which issues the MMAs)
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[a % C::kNumAcc]));
+                if (lane == 0) {
+                  if constexpr (kCta2)
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&bar_tempty[a % C::kNumAcc]), 0));
+                  else
+                    mbar_arrive(smem_u32(&bar_tempty[a % C::kNumAcc]));
+                }
               }
 #pragma unroll
               for (int j = 0; j < kCh; j += 4) {
@@ -1251,9 +1334,13 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide>::kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
+  // CTA pairs: neither CTA frees its TMEM or leaves (its shared memory and
+  // mbarriers) until the other is done with them
+  if constexpr (kCta2) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (kCta2) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
   }
   if (threadIdx.x == 0) {
     __threadfence();
@@ -1277,11 +1364,11 @@ struct GemmVariant {
   int threads;
 };
 
-template <int BM, bool kFP8, int kEpi, bool kGather, bool kWide = false>
+template <int BM, bool kFP8, int kEpi, bool kGather, bool kWide = false, bool kCta2 = false>
 GemmVariant variant() {
-  using C = Cfg<BM, kFP8, kEpi, kWide>;
+  using C = Cfg<BM, kFP8, kEpi, kWide, kCta2>;
   return GemmVariant{
-      reinterpret_cast<const void*>(&grouped_gemm_kernel<BM, kFP8, kEpi, kGather, kWide>),
+      reinterpret_cast<const void*>(&grouped_gemm_kernel<BM, kFP8, kEpi, kGather, kWide, kCta2>),
       C::kStageBytes, C::kThreads};
 }
 
@@ -1314,7 +1401,13 @@ bool pick_bm(int bm, GemmVariant& v) {
 
 // Gathered rows are built for the FP8 GEMM (every epilogue) and the BF16
 // gated up projection (the first GEMM of the BF16 forward).
-bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, bool wide, GemmVariant& v) {
+bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, bool wide, bool cta2,
+                         GemmVariant& v) {
+  if (cta2) {
+    if (!gemm_cta2_supported(fp8, epi, bm) || gather || wide) return false;
+    v = variant<128, true, MOE_EPI_SCATTER, false, false, true>();
+    return true;
+  }
   if (wide) {
     if (gather) return false;
     if (epi == MOE_EPI_SCATTER) return pick_wide<MOE_EPI_SCATTER>(fp8, bm, v);
@@ -1361,10 +1454,45 @@ bool gemm_wide_supported(bool fp8, int epi, int bm) {
   return epi != MOE_EPI_SWIGLU && (fp8 ? bm == 128 : (bm == 128 || bm == 256));
 }
 
-int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide) {
+bool gemm_cta2_supported(bool fp8, int epi, int bm) {
+  return fp8 && epi == MOE_EPI_SCATTER && bm == 128;
+}
+
+int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide, bool cta2) {
   GemmVariant v;
-  if (!select_gemm_variant(fp8, epi, bm, false, wide, v)) return 0;
+  if (!select_gemm_variant(fp8, epi, bm, false, wide, cta2, v)) return 0;
   return v.stage_bytes;
+}
+
+// Clusters of two CTAs of the CTA-pair kernel (at one CTA per SM) that can be
+// resident at once; 0 if unknown.  Cached per device: the first call sets the
+// kernel's shared-memory limit and asks the occupancy calculator.
+int gemm_cta2_max_clusters() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  const GemmVariant v = variant<128, true, MOE_EPI_SCATTER, false, false, true>();
+  // more than half of an SM's shared memory (one CTA per SM), leaving the
+  // per-block limit room for the kernel's static shared memory
+  constexpr int kSmem = 160 * 1024;
+  if (cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(v.threads);
+  cfg.dynamicSmemBytes = kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, v.fn, &cfg) != cudaSuccess) return 0;
+  cached[dev] = n;
+  return n;
 }
 
 int gemm_table_bytes(int E) { return (2 * (E + 1) * 4 + 15) & ~15; }
@@ -1385,7 +1513,9 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
                                 const GemmParams& p, bool fp8, int epi, int bm, int num_ctas,
                                 cudaStream_t stream, bool pdl) {
   GemmVariant v;
-  if (!select_gemm_variant(fp8, epi, bm, p.gather != 0, p.wide != 0, v)) return cudaErrorInvalidValue;
+  if (!select_gemm_variant(fp8, epi, bm, p.gather != 0, p.wide != 0, p.cta2 != 0, v))
+    return cudaErrorInvalidValue;
+  if (p.cta2 && (num_ctas < 2 || num_ctas % 2 != 0)) return cudaErrorInvalidValue;
   if (p.sk != 1 && p.sk != 2 && p.sk != 4) return cudaErrorInvalidValue;
   const bool pair = fp8 && (p.wide != 0 || epi == MOE_EPI_SWIGLU);
   const size_t smem = 1024 + static_cast<size_t>(p.num_stages) * p.sk * v.stage_bytes +
@@ -1402,11 +1532,18 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tm
   cfg.blockDim = dim3(v.threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.cta2) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   void* args[] = {const_cast<CUtensorMap*>(&tmap_w), const_cast<CUtensorMap*>(&tmap_a),
                   const_cast<GemmParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, v.fn, args);

@@ -198,12 +198,25 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   // tiles per tile (a stage then carries two MMAs per K block)
   p.wide = (gemm_wide_supported(fp8, a->epilogue, a->block_m) && a->gather_rows == 0 &&
             a->N % 256 == 0) ? 1 : 0;
-  p.n_tiles = (a->epilogue == MOE_EPI_SWIGLU ? a->N / 2 : a->N) / (p.wide ? 256 : 128);
+  // FP8 scatter at 128 routed rows: the same 256-row tiles, each computed by a
+  // cluster of two CTAs (one 128-row half each); an even grid of at most the
+  // clusters that fit at once
+  int ctas = a->num_ctas > 0 ? a->num_ctas : sms;
+  if (p.wide && gemm_cta2_supported(fp8, a->epilogue, a->block_m)) {
+    const int max_cl = gemm_cta2_max_clusters();
+    const int pairs = (ctas < 2 * max_cl ? ctas : 2 * max_cl) / 2;
+    if (pairs >= 1) {
+      p.cta2 = 1;
+      p.wide = 0;
+      ctas = 2 * pairs;
+    }
+  }
+  p.n_tiles = (a->epilogue == MOE_EPI_SWIGLU ? a->N / 2 : a->N) / ((p.wide || p.cta2) ? 256 : 128);
   p.sched = a->sched;
   p.w_reuse = 2LL * a->R >= static_cast<long long>(a->block_m) * a->E ? 1 : 0;
   p.drop_producer = g_drop_producer;
   p.timeout_ns = g_timeout_ns;
-  const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m, p.wide != 0);
+  const int stage_bytes = gemm_stage_bytes(fp8, a->epilogue, a->block_m, p.wide != 0, p.cta2 != 0);
   if (stage_bytes <= 0) return MOE_ERR_UNSUPPORTED;
   const bool pair = fp8 && (p.wide != 0 || a->epilogue == MOE_EPI_SWIGLU);
   const int meta_bytes = gemm_meta_bytes(fp8, a->block_m, p.kb_per_split, pair);
@@ -211,7 +224,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   p.M = a->M;
   // FP8 weights read once per expert (no row-tile reuse) through the queue:
   // warm L2 with each CTA's likely first weight tile before the layout is known
-  p.warm_first = (fp8 && !p.w_reuse && a->sched == MOE_SCHED_QUEUE) ? 1 : 0;
+  p.warm_first = (fp8 && !p.w_reuse && a->sched == MOE_SCHED_QUEUE && !p.cta2) ? 1 : 0;
   const int rows_bytes = gemm_extra_bytes(fp8, a->epilogue, a->block_m, p.gather != 0);
   // Several K blocks per stage (more bytes per copy instruction, and 128 *
   // sk contiguous bytes of every weight row per copy): the largest of 4, 2, 1
@@ -231,7 +244,6 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   // FP8 scatter through the queue: split the last wave (one tile per CTA) in
   // K parts, so CTAs finish within a part of a tile of one another — quarters
   // where tiles are narrow (block_m <= 32: a cheap epilogue per part), else halves
-  const int ctas = a->num_ctas > 0 ? a->num_ctas : sms;
   p.tail_parts = 2;
   for (int parts = a->block_m <= 32 ? 4 : 2; parts >= 2; parts /= 2) {
     const int partkb = (p.KB / parts) / p.sk * p.sk;
@@ -241,9 +253,10 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
       break;
     }
   }
-  if (fp8 && a->epilogue == MOE_EPI_SCATTER && p.k_splits == 1 && a->sched == MOE_SCHED_QUEUE &&
-      p.tail_partkb > 0)
-    p.tail_tiles = ctas;
+  // (CTA pairs walk a fixed round-robin list, one tile per pair at a time)
+  if (fp8 && a->epilogue == MOE_EPI_SCATTER && p.k_splits == 1 &&
+      (a->sched == MOE_SCHED_QUEUE || p.cta2) && p.tail_partkb > 0)
+    p.tail_tiles = p.cta2 ? ctas / 2 : ctas;
   CUtensorMap tw, ta;
   if (!make_tmap(&tw, a->w, fp8, static_cast<uint64_t>(a->K),
                  static_cast<uint64_t>(a->E) * a->N, 128u, static_cast<uint32_t>(p.sk)))
@@ -252,7 +265,8 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
     if (!make_tmap_rows(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->M)))
       return MOE_ERR_CUDA;
   } else if (!make_tmap(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->R),
-                        static_cast<uint32_t>(a->block_m), static_cast<uint32_t>(p.sk))) {
+                        static_cast<uint32_t>(p.cta2 ? a->block_m / 2 : a->block_m),
+                        static_cast<uint32_t>(p.sk))) {
     return MOE_ERR_CUDA;
   }
   return cuda_status(launch_grouped_gemm(tw, ta, p, fp8, a->epilogue, a->block_m, ctas, stream,
@@ -585,6 +599,8 @@ moe_status_t forward_impl(const moe_forward_args* f, const float* logits, const 
     if (same_entry(g_graphs[i], f, logits, x, out, ws, dev))
       return cuda_status(cudaGraphLaunch(g_graphs[i].exec, stream));
   }
+  // host-side queries the launches make once per device, kept out of the capture
+  if (f->dtype == MOE_DTYPE_FP8_E4M3) gemm_cta2_max_clusters();
   // The launch sequence is recorded on a private stream (the caller's may be
   // the legacy default stream, which cannot be captured); the graph itself
   // is then launched on the caller's stream.
@@ -652,7 +668,12 @@ const char* moe_status_string(moe_status_t s) {
   return "unknown status";
 }
 
-int moe_num_sms(void) { return device_sms(); }
+int moe_num_sms(void) {
+  gemm_cta2_max_clusters();   // cached per device, outside any capture
+  return device_sms();
+}
+
+int moe_gemm_cta_pairs(void) { return gemm_cta2_max_clusters(); }
 
 const char* moe_last_cuda_error(void) { return g_last_error; }
 

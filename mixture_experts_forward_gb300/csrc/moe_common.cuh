@@ -199,25 +199,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, both operands K-major.
-template <bool kFP8>
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                     uint32_t idesc, uint32_t accumulate) {
-  if constexpr (kFP8) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread completes.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
@@ -225,16 +206,51 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
-// Shared-memory matrix descriptor: K-major tile whose rows are 128 bytes,
-// 128-byte swizzle, 8-row groups 1024 bytes apart, tile base 1024-aligned.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);           // start address
-  d |= static_cast<uint64_t>(1) << 16;                          // leading offset (unused)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;                  // stride offset: 8 rows
-  d |= static_cast<uint64_t>(1) << 46;                          // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                          // 128-byte swizzle
-  return d;
+// Shared-memory matrix descriptor of a K-major tile whose rows are 128 bytes
+// (128-byte swizzle, 8-row groups 1024 bytes apart, tile base 1024-aligned),
+// as two 32-bit words.  High word: stride offset 1024 >> 4 (bits 32..45),
+// descriptor version 1 (bit 46), swizzle mode 2 = 128 bytes (bits 61..63), one
+// constant.  Low word: start address >> 4 (bits 0..13) and the leading offset
+// (bit 16; unused by swizzled K-major tiles).  Advancing the
+// operand by a K step of 32 bytes adds 2 to the low word: a shared address is
+// below 2^18, so the 14-bit address field does not carry into the rest and the
+// issuing thread spends one add per operand instead of rebuilding 64 bits.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr) {
+  return ((saddr & 0x3FFFF) >> 4) | (1u << 16);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, both operands K-major, from descriptor low
+// words (high word kDescHi): cta_group::1 kind::f8f6f4 (kFP8) or kind::f16;
+// kPair: cta_group::2 kind::f8f6f4, issued by the even CTA of a pair, with A
+// spanning both CTAs (M/2 rows each) and B split likewise (N/2 rows each), D in
+// both CTAs' TMEM.
+template <bool kFP8, bool kPair = false>
+__device__ __forceinline__ void umma_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                        uint32_t idesc, uint32_t accumulate) {
+  static_assert(!kPair || kFP8, "pair MMAs are FP8 here");
+  if constexpr (kPair) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 ad, {%1, %5};\n\tmov.b64 bd, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+        : "memory");
+  } else if constexpr (kFP8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 ad, {%1, %5};\n\tmov.b64 bd, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 ad, {%1, %5};\n\tmov.b64 bd, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+        : "memory");
+  }
 }
 
 // Instruction descriptor: fp32 accumulator, A/B K-major, shape M x N.
@@ -340,6 +356,75 @@ __device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, f
       "mov.b64 {%0, %1}, pd;\n\t}"
       : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// ----------------------------------------------------------------------------
+// CTA pairs (cluster of two; tcgen05 .cta_group::2).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of both CTAs of the cluster: arrive (release) and wait (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+               "memory");
+}
+
+// The shared::cluster address of the same shared-memory location in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address, without memory
+// ordering (relaxed): for handing back a TMEM buffer whose loads this thread
+// has already waited for (tcgen05.wait::ld), where a release at cluster scope
+// would first wait for every earlier global write of the thread (such as the
+// previous tile's reductions) to become visible to the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// 3-D tiled load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (its shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2),
+      "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Arrive on the mbarrier at the same shared-memory offset in each CTA of
+// `mask` once every pair MMA issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
 }
 
 // Named barrier among `count` threads (multiple of 32).

@@ -58,6 +58,8 @@ struct GemmParams {
   int warm_first;               // before the wait for the layout: L2-prefetch the weight tiles
                                 // of this CTA's likely first warm_first tiles (0 = off)
   int wide;                     // BF16 store / scatter: tiles of 256 output columns
+  int cta2;                     // FP8 scatter at block_m 128: tiles of 256 weight rows over a
+                                // cluster of two CTAs (n_tiles counts 256-row tiles)
   int gather;                   // A rows gathered from token-major rows (see moe_gemm_args)
   int M;                        // gather: rows of the token-major A (tokens)
   int drop_producer;
@@ -127,9 +129,12 @@ cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, int32_t*
 cudaError_t launch_grouped_gemm(const CUtensorMap& tmap_w, const CUtensorMap& tmap_a,
                                 const GemmParams& p, bool fp8, int epi, int bm, int num_ctas,
                                 cudaStream_t stream, bool pdl);
-int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide = false);
+int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide = false, bool cta2 = false);
 // BF16 store / scatter tiles of two adjacent weight tiles (256 output columns)
 bool gemm_wide_supported(bool fp8, int epi, int bm);
+// FP8 scatter tiles of 256 weight rows computed by a cluster of two CTAs
+bool gemm_cta2_supported(bool fp8, int epi, int bm);
+int gemm_cta2_max_clusters();
 int gemm_meta_bytes(bool fp8, int bm, int kb_per_split, bool pair = false);
 int gemm_rows_bytes(bool fp8, int bm);   // the route-id ring of the gathered-rows mode
 // shared memory after the tables: the gathered-rows ring, or the FP8 SwiGLU

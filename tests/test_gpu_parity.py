@@ -199,6 +199,22 @@ def test_gemm_fp8_wide_tiles(epi, sched, ks, ctas):
                    k_splits=ks, skew=1.5, num_ctas=ctas)
 
 
+@pytest.mark.parametrize("M,E,k,N,ctas,skew", [
+    (2000, 4, 2, 1024, 4, 1.0),   # two pairs loop over many tiles; the last tiles in K halves
+    (3, 8, 2, 512, 0, 0.0),       # fewer tiles than pairs, most experts empty
+    (700, 8, 3, 512, 3, 1.5),     # an odd grid: one pair
+    (700, 8, 3, 512, 1, 1.5),     # one CTA: the single-CTA form of the 256-row tile
+])
+def test_gemm_fp8_scatter_cta_pairs(M, E, k, N, ctas, skew):
+    """FP8 scatter at 128 routed rows with N a multiple of 256: a cluster of two
+    CTAs computes each 256-row weight tile (one M = 256 MMA per K step, each
+    CTA holding its 128 weight rows, half of the routed rows and its own
+    accumulator); checked element by element against the oracle."""
+    assert L.gemm_cta_pairs() > 0, "the CTA-pair form is not in use on this device"
+    _fp8_gemm_case(M=M, K=2048, N=N, E=E, k=k, bm=128, epilogue=L.EPI_SCATTER, skew=skew,
+                   num_ctas=ctas)
+
+
 def _e4m3_order(c: np.ndarray) -> np.ndarray:
     """Signed position of an E4M3 code on the number line; 0x00 and 0x80 both 0."""
     c = c.astype(np.int32)
