@@ -82,15 +82,20 @@ struct TileDesc {
 // per epilogue thread, and run one TMA producer warp so that four epilogue
 // warps per TMEM lane quadrant fit the register file at 128 routed rows.
 //
-// CTA pairs (kCta2; FP8 scatter at 128 routed rows): a cluster of two CTAs on
-// two SMs computes one tile of 256 weight rows x 128 routed rows with
-// tcgen05.mma.cta_group::2 (M = 256).  Each CTA stages its own 128 weight rows
-// and half of the routed rows (64) and holds its weight rows' 128 x 128
-// accumulator in its own TMEM, so a K block's buffer is 128 columns (four in
-// TMEM) and a stage 24 KB per K block: twice the K blocks in flight per SM of
-// the single-CTA pair tile, for the same tensor work per SM.  The even CTA
+// CTA pairs (kCta2; FP8 at 128 routed rows per CTA): a cluster of two CTAs on
+// two SMs shares each MMA (tcgen05.mma.cta_group::2, M = 256).  The even CTA
 // issues every MMA; its mbarriers count both CTAs' copies and both CTAs'
 // epilogue releases.
+//   scatter: a tile of 256 weight rows x 128 routed rows; each CTA stages its
+//     own 128 weight rows and half of the routed rows (64) and holds its weight
+//     rows' 128 x 128 accumulator in its own TMEM, so a K block's buffer is 128
+//     columns (four in TMEM) and a stage 24 KB per K block.
+//   SwiGLU (token-major): a tile of 256 routed rows x the gate and up rows of
+//     128 h columns; each CTA stages 128 routed rows and one weight tile (the
+//     even CTA the gate rows, the odd one the up rows), 32 KB per K block
+//     against 48 KB for the single-CTA tile, and its TMEM holds gate and up
+//     (256 columns) for its own routed rows, so the SwiGLU and the 1x128
+//     re-quantisation stay within the CTA.
 template <int BM, bool kFP8, int kEpi, bool kWide = false, bool kCta2 = false>
 struct Cfg {
   static constexpr bool kSwiglu = kEpi == MOE_EPI_SWIGLU;
@@ -113,7 +118,8 @@ struct Cfg {
   static constexpr int kTmemNeed = kNumAcc * kAccCols;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
-  static constexpr int kATiles = kPair ? 2 : 1;
+  // weight tiles a CTA stages per K block (CTA pairs: one each, gate or up)
+  static constexpr int kATiles = (kPair && !kCta2) ? 2 : 1;
   static constexpr int kRing = ring_slots(kFP8, BM);
   // TMA producer warps (warp 0 plus warps 7..): two measured best (four were
   // no faster on any workload and slower on the BF16 FFN); FP8 pair tiles: one
@@ -137,8 +143,10 @@ struct Cfg {
   static constexpr int kThreads = 32 * kWarps;
   // bytes of one K block of a stage; a stage holds p.sk K blocks laid out as
   // [kATiles][sk] weight tiles, then [sk] activation tiles
-  // routed rows of a stage (CTA pairs: this CTA's half)
-  static constexpr int kBRows = kCta2 ? BM / 2 : BM;
+  // routed rows of a stage (CTA-pair scatter: this CTA's half of the tile's)
+  static constexpr int kBRows = (kCta2 && !kSwiglu) ? BM / 2 : BM;
+  // routed rows of one tile (CTA-pair SwiGLU: BM per CTA, so 2 * BM per pair)
+  static constexpr int kTileRows = (kCta2 && kSwiglu) ? 2 * BM : BM;
   static constexpr int kStageBytes = kATiles * kATileBytes + kBRows * kRowBytes;
   // FP8 epilogue: K blocks whose partials are loaded before one wait (<= 64 columns)
   static constexpr int kKbGroup = BM <= 64 ? 64 / BM : 1;
@@ -146,7 +154,9 @@ struct Cfg {
   static_assert(BM % 16 == 0 && BM >= 16 && BM <= 256, "block_m");
   static_assert(!kFP8 || BM <= 128, "FP8 block_m <= 128");
   static_assert(kTmemNeed <= 512, "TMEM");
-  static_assert(!kCta2 || (kFP8 && BM == 128 && !kPair && kEpi == MOE_EPI_SCATTER), "CTA pairs");
+  static_assert(!kCta2 || (kFP8 && BM == 128 && !kWide &&
+                            ((!kPair && kEpi == MOE_EPI_SCATTER) || kSwiglu)),
+                "CTA pairs");
 };
 
 // Bytes of one metadata slot.  FP8 single tiles: [kb_per_split][BM] scale
@@ -328,7 +338,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
   static_assert(!(kWide && (C::kSwiglu || kGather)), "wide tiles: store / scatter, compact rows");
   static_assert(!(C::kFP8Pair && kGather), "FP8 pair tiles read compact rows");
   // weight rows of a tile (two weight tiles when wide or split over a CTA pair)
-  constexpr int kWRows = (kWide || kCta2) ? 2 * kTileN : kTileN;
+  constexpr int kWRows = (kWide || (kCta2 && !C::kSwiglu)) ? 2 * kTileN : kTileN;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ __align__(8) uint64_t bar_tfull[C::kNumAcc], bar_tempty[C::kNumAcc];
@@ -423,6 +433,31 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
   cp_async_wait_all();
   tc_fence_before();
   __syncthreads();
+  if constexpr (C::kTileRows != BM) {
+    // CTA-pair SwiGLU: tiles of 2 * BM routed rows, so the tile offsets are
+    // the prefix of ceil(count / (2 * BM)) over the experts, from the row
+    // offsets (one warp: a run of experts per lane, then a warp scan)
+    if (warp == 0) {
+      const int per = (p.E + 31) / 32;
+      const int e0 = min(p.E, lane * per), e1 = min(p.E, e0 + per);
+      int local = 0;
+      for (int e = e0; e < e1; ++e)
+        local += (s_off[e + 1] - s_off[e] + C::kTileRows - 1) / C::kTileRows;
+      int inc = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      int run = inc - local;
+      for (int e = e0; e < e1; ++e) {
+        s_tile_off[e] = run;
+        run += (s_off[e + 1] - s_off[e] + C::kTileRows - 1) / C::kTileRows;
+      }
+      if (lane == 31) s_tile_off[p.E] = inc;
+    }
+    __syncthreads();
+  }
   // CTA pairs: both CTAs' mbarriers are initialised (and their TMEM
   // allocated) before either CTA signals the other's
   if constexpr (kCta2) cluster_sync();
@@ -515,7 +550,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
           }
           t = __shfl_sync(0xffffffffu, t, 0);
           if (t >= 0) {
-            decode_tile(t, p, s_tile_off, s_off, BM, d);
+            decode_tile(t, p, s_tile_off, s_off, C::kTileRows, d);
             if (d.rows <= 0 || d.nkb <= 0) {
               if (lane == 0 && claim) {
                 queued = G + static_cast<int>(atomicAdd(p.queue_ctr, 1u));
@@ -561,7 +596,10 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
       const int* rr = s_rows + ds * BM;   // this tile's route ids (gathered rows)
       if (++ds == C::kRing) { ds = 0; dphase ^= 1u; }
       if (d.nkb < 0) break;
-      const int w_row = d.e * p.N + d.n_tile * kWRows + (kCta2 ? static_cast<int>(rank) * kTileN : 0);
+      // CTA pairs: the odd CTA's weight tile is the scatter tile's second
+      // 128 rows, or the SwiGLU tile's up rows (N / 2 on)
+      const int w_row = d.e * p.N + d.n_tile * kWRows +
+                        (kCta2 ? static_cast<int>(rank) * (C::kSwiglu ? p.N / 2 : kTileN) : 0);
       const int w_pair = C::kSwiglu ? p.N / 2 : kTileN;  // row offset of the second weight tile
       for (int i = 0; i < d.nkb; i += SK) {
         if (q % nprod == pw) {
@@ -627,7 +665,7 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
           // stall this warp on the atomic's round trip)
           const int nt = __shfl_sync(0xffffffffu, queued, 0);
           if (nt < total_tiles) {
-            decode_tile(nt, p, s_tile_off, s_off, BM, dn);
+            decode_tile(nt, p, s_tile_off, s_off, C::kTileRows, dn);
             if (dn.rows > 0 && dn.nkb > 0) {
               {
 #pragma unroll
@@ -715,7 +753,14 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
             const uint32_t d_tmem = tmem_base + buf * C::kAccCols;
             // descriptor low words of this K block's operands (a K step adds 2)
             const uint32_t alo = smem_desc_lo(a_addr), blo = smem_desc_lo(b_addr);
-            if constexpr (kCta2) {
+            if constexpr (kCta2 && C::kSwiglu) {
+              // M = 256 routed rows (128 per CTA), N = the gate rows (even CTA)
+              // and the up rows (odd CTA) of 128 h columns
+              constexpr uint32_t idesc_p = make_idesc(0u, 256u, 256u);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_lo<true, true>(d_tmem, blo + 2 * kk, alo + 2 * kk, idesc_p, kk > 0 ? 1u : 0u);
+            } else if constexpr (kCta2) {
               // M = 256 weight rows (128 per CTA), N = 128 routed rows (64 per CTA)
               constexpr uint32_t idesc_p = make_idesc(0u, 256u, 128u);
 #pragma unroll
@@ -783,7 +828,11 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
         float* wt = reinterpret_cast<float*>(tok + BM);
         // CTA pairs: this CTA's 128-row weight block of the 256-row tile
         TileDesc dm = d;
-        if constexpr (kCta2) dm.n_tile = 2 * d.n_tile + static_cast<int>(rank);
+        if constexpr (kCta2 && !C::kSwiglu) dm.n_tile = 2 * d.n_tile + static_cast<int>(rank);
+        if constexpr (kCta2 && C::kSwiglu) {   // this CTA's routed rows of the pair tile
+          dm.m0 = d.m0 + static_cast<int>(rank) * BM;
+          dm.rows = max(0, min(BM, d.rows - static_cast<int>(rank) * BM));
+        }
         meta_fill<BM, kFP8, kEpi, kGather, C::kPair, kWide>(p, dm, lane, s_rows + ds * BM, sc, tok,
                                                             wt);
       }
@@ -812,13 +861,18 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
         ok = false;
         break;
       }
-      const TileDesc d = s_desc[ds];
+      TileDesc d = s_desc[ds];
       if (d.nkb < 0) break;
+      if constexpr (kCta2 && C::kSwiglu) {   // this CTA's routed rows of the pair tile
+        d.m0 += static_cast<int>(rank) * BM;
+        d.rows = max(0, min(BM, d.rows - static_cast<int>(rank) * BM));
+      }
       const float* sc = reinterpret_cast<const float*>(s_meta + ds * meta_bytes);
       const int* tok = reinterpret_cast<const int*>(sc + tok_off);
       const float* wt = reinterpret_cast<const float*>(tok + BM);
       // output column (of the first weight tile; CTA pairs: of this CTA's half)
-      const int col = d.n_tile * kWRows + (kCta2 ? static_cast<int>(rank) * kTileN : 0) + row;
+      const int col =
+          d.n_tile * kWRows + ((kCta2 && !C::kSwiglu) ? static_cast<int>(rank) * kTileN : 0) + row;
 
       if constexpr (C::kTok) {
         // Token-major pair tile: TMEM lane = routed row s of the tile, 256
@@ -854,9 +908,14 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
             tmem_ld16(base + c0, v);
             tmem_ld_wait(v);
             if (u == 3) {                              // the K block is in registers: release it
-              tc_fence_before();
+              tc_fence_before();                       // (CTA pairs: to the even CTA)
               __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[a % C::kNumAcc]));
+              if (lane == 0) {
+                if constexpr (kCta2)
+                  mbar_arrive_cluster(mapa_shared(smem_u32(&bar_tempty[a % C::kNumAcc]), 0));
+                else
+                  mbar_arrive(smem_u32(&bar_tempty[a % C::kNumAcc]));
+              }
             }
 #pragma unroll
             for (int j = 0; j < 16; j += 2)
@@ -1405,7 +1464,10 @@ bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, bool wide, bool
                          GemmVariant& v) {
   if (cta2) {
     if (!gemm_cta2_supported(fp8, epi, bm) || gather || wide) return false;
-    v = variant<128, true, MOE_EPI_SCATTER, false, false, true>();
+    if (epi == MOE_EPI_SWIGLU)
+      v = variant<128, true, MOE_EPI_SWIGLU, false, false, true>();
+    else
+      v = variant<128, true, MOE_EPI_SCATTER, false, false, true>();
     return true;
   }
   if (wide) {
@@ -1455,7 +1517,7 @@ bool gemm_wide_supported(bool fp8, int epi, int bm) {
 }
 
 bool gemm_cta2_supported(bool fp8, int epi, int bm) {
-  return fp8 && epi == MOE_EPI_SCATTER && bm == 128;
+  return fp8 && bm == 128 && (epi == MOE_EPI_SCATTER || epi == MOE_EPI_SWIGLU);
 }
 
 int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide, bool cta2) {
@@ -1464,8 +1526,9 @@ int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide, bool cta2) {
   return v.stage_bytes;
 }
 
-// Clusters of two CTAs of the CTA-pair kernel (at one CTA per SM) that can be
-// resident at once; 0 if unknown.  Cached per device: the first call sets the
+// Clusters of two CTAs of the CTA-pair kernels (one CTA per SM, 608 threads,
+// the same for the scatter and SwiGLU forms) that can be resident at once; 0
+// if unknown.  Cached per device: the first call sets the
 // kernel's shared-memory limit and asks the occupancy calculator.
 int gemm_cta2_max_clusters() {
   static int cached[64] = {0};

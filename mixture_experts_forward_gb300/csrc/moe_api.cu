@@ -198,11 +198,14 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   // tiles per tile (a stage then carries two MMAs per K block)
   p.wide = (gemm_wide_supported(fp8, a->epilogue, a->block_m) && a->gather_rows == 0 &&
             a->N % 256 == 0) ? 1 : 0;
-  // FP8 scatter at 128 routed rows: the same 256-row tiles, each computed by a
-  // cluster of two CTAs (one 128-row half each); an even grid of at most the
-  // clusters that fit at once
+  // FP8 at 128 routed rows, scatter (the same 256-row tiles, a 128-row half on
+  // each CTA) and SwiGLU (tiles of 2 x 128 routed rows, 128 on each CTA): a
+  // cluster of two CTAs per tile; an even grid of at most the clusters that
+  // fit at once
   int ctas = a->num_ctas > 0 ? a->num_ctas : sms;
-  if (p.wide && gemm_cta2_supported(fp8, a->epilogue, a->block_m)) {
+  const bool swiglu = a->epilogue == MOE_EPI_SWIGLU;
+  if ((p.wide || swiglu) && a->gather_rows == 0 &&
+      gemm_cta2_supported(fp8, a->epilogue, a->block_m)) {
     const int max_cl = gemm_cta2_max_clusters();
     const int pairs = (ctas < 2 * max_cl ? ctas : 2 * max_cl) / 2;
     if (pairs >= 1) {
@@ -211,7 +214,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
       ctas = 2 * pairs;
     }
   }
-  p.n_tiles = (a->epilogue == MOE_EPI_SWIGLU ? a->N / 2 : a->N) / ((p.wide || p.cta2) ? 256 : 128);
+  p.n_tiles = (swiglu ? a->N / 2 : a->N) / ((p.wide || (p.cta2 && !swiglu)) ? 256 : 128);
   p.sched = a->sched;
   p.w_reuse = 2LL * a->R >= static_cast<long long>(a->block_m) * a->E ? 1 : 0;
   p.drop_producer = g_drop_producer;
@@ -236,7 +239,8 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   // FP8 pair tiles of 128 routed rows that store their results feed both
   // weight tiles to one MMA as a single 256-row operand, so a stage holds one
   // K block (the tiles adjacent)
-  if (pair && a->block_m == 128 && a->epilogue != MOE_EPI_SCATTER) p.sk = 1;
+  // (CTA pairs stage one weight tile per CTA, so their stages may be deeper)
+  if (pair && a->block_m == 128 && a->epilogue != MOE_EPI_SCATTER && !p.cta2) p.sk = 1;
   int stages = avail / (p.sk * stage_bytes);
   if (stages > 16) stages = 16;
   if (stages < 2) return MOE_ERR_UNSUPPORTED;
@@ -265,7 +269,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
     if (!make_tmap_rows(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->M)))
       return MOE_ERR_CUDA;
   } else if (!make_tmap(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->R),
-                        static_cast<uint32_t>(p.cta2 ? a->block_m / 2 : a->block_m),
+                        static_cast<uint32_t>((p.cta2 && !swiglu) ? a->block_m / 2 : a->block_m),
                         static_cast<uint32_t>(p.sk))) {
     return MOE_ERR_CUDA;
   }

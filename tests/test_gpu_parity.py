@@ -266,8 +266,25 @@ def test_gemm_fp8_swiglu_epilogue(bm):
 
 @pytest.mark.parametrize("sched,ctas", [(L.SCHED_STATIC, 0), (L.SCHED_QUEUE, 6)])
 def test_gemm_fp8_swiglu_schedules(sched, ctas):
-    """Static partition, and six CTAs looping over many 128-row tiles."""
+    """Static partition, and six CTAs looping over many tiles (at 128 routed
+    rows both run CTA pairs, which walk a fixed round-robin order)."""
     _fp8_swiglu_case(M=900, K=1024, I=256, E=6, k=2, bm=128, sched=sched, num_ctas=ctas, skew=2.0)
+
+
+@pytest.mark.parametrize("M,E,k,I,ctas,skew", [
+    (1500, 4, 2, 512, 4, 1.0),    # two pairs loop over many 256-row tiles
+    (200, 16, 3, 256, 0, 2.0),    # experts of 1..255 rows: half-empty and odd-CTA-empty tiles
+    (700, 8, 3, 256, 5, 1.5),     # an odd grid: two pairs
+    (700, 8, 3, 256, 1, 1.5),     # one CTA: the single-CTA token-major tile
+])
+def test_gemm_fp8_swiglu_cta_pairs(M, E, k, I, ctas, skew):
+    """FP8 SWIGLU at 128 routed rows: a cluster of two CTAs computes tiles of
+    256 routed rows (128 per CTA, the M = 256 side of each MMA) against the gate
+    rows (even CTA) and up rows (odd CTA) of 128 h columns; each CTA applies
+    the SwiGLU and the 1x128 re-quantisation to its own rows.  Tile offsets of
+    the 256-row tiles come from the row offsets inside the kernel."""
+    assert L.gemm_cta_pairs() > 0, "the CTA-pair form is not in use on this device"
+    _fp8_swiglu_case(M=M, K=1024, I=I, E=E, k=k, bm=128, num_ctas=ctas, skew=skew)
 
 
 def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, seed=0):
