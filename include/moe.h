@@ -79,11 +79,14 @@ const char* moe_status_string(moe_status_t s);
 int moe_num_sms(void);
 
 /* Clusters of two CTAs that can be resident at once on the current device
- * for the FP8 scatter GEMM at block_m 128 with N a multiple of 256, whose
- * 256-row weight tiles are each computed by a CTA pair (tcgen05 MMAs with
- * M = 256 spanning both SMs).  0: that form is unavailable (or on error) and
- * those GEMMs run the single-CTA form.  The grid of such a GEMM is the even
- * number of CTAs min(num_ctas or the SM count, 2 x this). */
+ * for the grouped GEMMs whose tiles are each computed by a CTA pair (tcgen05
+ * MMAs with M = 256 spanning both SMs): FP8 SCATTER at block_m 128 with N a
+ * multiple of 256 (256 weight rows x 128 routed rows per tile), FP8 SWIGLU at
+ * block_m 128 (256 routed rows x the gate and up rows of 128 h columns), BF16
+ * SCATTER and STORE_BF16 at block_m 256 with N a multiple of 256 (256 weight
+ * rows x 256 routed rows).  0: that form is unavailable (or on error) and those
+ * GEMMs run the single-CTA form.  The grid of such a GEMM is the even number of
+ * CTAs min(num_ctas or the SM count, 2 x this). */
 int moe_gemm_cta_pairs(void);
 
 /* Name and text of the CUDA error behind the calling thread's most recent
@@ -152,12 +155,14 @@ typedef struct {
   const float* route_weights; /* SCATTER: [M*top_k] */
   void* out;                  /* see moe_epilogue_t */
   int k_splits;               /* FP8 SCATTER: K split into this many tiles (0 = auto) */
-  int num_ctas;               /* persistent CTAs (0 = one per SM).  FP8 SCATTER with
-                                 block_m 128, N a multiple of 256 and gather_rows 0 runs
-                                 clusters of two CTAs (moe_gemm_cta_pairs), each pair
-                                 walking every (G/2)-th 256-row tile in a fixed order: the
-                                 grid G is then num_ctas rounded down to even and capped
-                                 at twice the resident pairs (num_ctas 1: single CTAs) */
+  int num_ctas;               /* persistent CTAs (0 = one per SM).  With gather_rows 0,
+                                 FP8 SCATTER (block_m 128, N a multiple of 256), FP8
+                                 SWIGLU (block_m 128) and BF16 SCATTER / STORE_BF16
+                                 (block_m 256, N a multiple of 256) run clusters of two
+                                 CTAs (moe_gemm_cta_pairs), each pair walking every
+                                 (G/2)-th tile in a fixed order: the grid G is then
+                                 num_ctas rounded down to even and capped at twice the
+                                 resident pairs (num_ctas 1: single CTAs) */
   int gather_rows;            /* 0: `a` holds the expert-compact rows [R, K] (FP8 a_scales
                                  [K/128, R]).  1: `a` is token-major [M, K] and the kernel
                                  gathers compact slot s from row sorted_route_ids[s] / top_k

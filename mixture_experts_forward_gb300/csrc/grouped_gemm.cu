@@ -90,6 +90,11 @@ struct TileDesc {
 //     own 128 weight rows and half of the routed rows (64) and holds its weight
 //     rows' 128 x 128 accumulator in its own TMEM, so a K block's buffer is 128
 //     columns (four in TMEM) and a stage 24 KB per K block.
+//   BF16 scatter / bf16 rows at block_m 256: a tile of 256 weight rows x 256
+//     routed rows; each CTA stages its 128 weight rows and half of the routed
+//     rows and holds its weight rows' 128 x 256 accumulator, so TMEM takes two
+//     tiles (the single-CTA 256 x 256 tile fills it) and a tile's reductions or
+//     stores overlap the next tile's MMAs.
 //   SwiGLU (token-major): a tile of 256 routed rows x the gate and up rows of
 //     128 h columns; each CTA stages 128 routed rows and one weight tile (the
 //     even CTA the gate rows, the odd one the up rows), 32 KB per K block
@@ -155,7 +160,9 @@ struct Cfg {
   static_assert(!kFP8 || BM <= 128, "FP8 block_m <= 128");
   static_assert(kTmemNeed <= 512, "TMEM");
   static_assert(!kCta2 || (kFP8 && BM == 128 && !kWide &&
-                            ((!kPair && kEpi == MOE_EPI_SCATTER) || kSwiglu)),
+                            ((!kPair && kEpi == MOE_EPI_SCATTER) || kSwiglu)) ||
+                    (!kFP8 && BM == 256 && !kPair &&
+                     (kEpi == MOE_EPI_SCATTER || kEpi == MOE_EPI_STORE_BF16)),
                 "CTA pairs");
 };
 
@@ -760,6 +767,14 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 umma_lo<true, true>(d_tmem, blo + 2 * kk, alo + 2 * kk, idesc_p, kk > 0 ? 1u : 0u);
+            } else if constexpr (kCta2 && !kFP8) {
+              // BF16: M = 256 weight rows (128 per CTA), N = 256 routed rows (128
+              // per CTA), accumulated over all of K
+              constexpr uint32_t idesc_p = make_idesc(1u, 256u, static_cast<uint32_t>(BM));
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_lo<false, true>(d_tmem, alo + 2 * kk, blo + 2 * kk, idesc_p,
+                                     (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
             } else if constexpr (kCta2) {
               // M = 256 weight rows (128 per CTA), N = 128 routed rows (64 per CTA)
               constexpr uint32_t idesc_p = make_idesc(0u, 256u, 128u);
@@ -794,7 +809,8 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
           else umma_commit(smem_u32(&bar_empty[stage]));
           if constexpr (!kFP8) {
             if (i + nk >= d.nkb) {
-              umma_commit(smem_u32(&bar_tfull[buf]));
+              if constexpr (kCta2) umma_commit_pair(smem_u32(&bar_tfull[buf]), 3);
+              else umma_commit(smem_u32(&bar_tfull[buf]));
               ++acc_n;
             }
           }
@@ -1376,7 +1392,10 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bar_tempty[buf]));
+        if (lane == 0) {   // (CTA pairs: to the even CTA)
+          if constexpr (kCta2) mbar_arrive_cluster(mapa_shared(smem_u32(&bar_tempty[buf]), 0));
+          else mbar_arrive(smem_u32(&bar_tempty[buf]));
+        }
         ++acc_n;
       }
       // this tile's descriptor and metadata slot may now be reused
@@ -1464,7 +1483,10 @@ bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, bool wide, bool
                          GemmVariant& v) {
   if (cta2) {
     if (!gemm_cta2_supported(fp8, epi, bm) || gather || wide) return false;
-    if (epi == MOE_EPI_SWIGLU)
+    if (!fp8)
+      v = epi == MOE_EPI_SCATTER ? variant<256, false, MOE_EPI_SCATTER, false, false, true>()
+                                 : variant<256, false, MOE_EPI_STORE_BF16, false, false, true>();
+    else if (epi == MOE_EPI_SWIGLU)
       v = variant<128, true, MOE_EPI_SWIGLU, false, false, true>();
     else
       v = variant<128, true, MOE_EPI_SCATTER, false, false, true>();
@@ -1517,7 +1539,8 @@ bool gemm_wide_supported(bool fp8, int epi, int bm) {
 }
 
 bool gemm_cta2_supported(bool fp8, int epi, int bm) {
-  return fp8 && bm == 128 && (epi == MOE_EPI_SCATTER || epi == MOE_EPI_SWIGLU);
+  if (fp8) return bm == 128 && (epi == MOE_EPI_SCATTER || epi == MOE_EPI_SWIGLU);
+  return bm == 256 && (epi == MOE_EPI_SCATTER || epi == MOE_EPI_STORE_BF16);
 }
 
 int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide, bool cta2) {

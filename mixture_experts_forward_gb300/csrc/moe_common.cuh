@@ -222,14 +222,20 @@ __device__ __forceinline__ uint32_t smem_desc_lo(uint32_t saddr) {
 
 // D[tmem] (+)= A[smem] * B[smem]^T, both operands K-major, from descriptor low
 // words (high word kDescHi): cta_group::1 kind::f8f6f4 (kFP8) or kind::f16;
-// kPair: cta_group::2 kind::f8f6f4, issued by the even CTA of a pair, with A
+// kPair: the cta_group::2 forms, issued by the even CTA of a pair, with A
 // spanning both CTAs (M/2 rows each) and B split likewise (N/2 rows each), D in
 // both CTAs' TMEM.
 template <bool kFP8, bool kPair = false>
 __device__ __forceinline__ void umma_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                         uint32_t idesc, uint32_t accumulate) {
-  static_assert(!kPair || kFP8, "pair MMAs are FP8 here");
-  if constexpr (kPair) {
+  if constexpr (kPair && !kFP8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 ad, {%1, %5};\n\tmov.b64 bd, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHi)
+        : "memory");
+  } else if constexpr (kPair) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "mov.b64 ad, {%1, %5};\n\tmov.b64 bd, {%2, %5};\n\t"

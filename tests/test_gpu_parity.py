@@ -287,7 +287,7 @@ def test_gemm_fp8_swiglu_cta_pairs(M, E, k, I, ctas, skew):
     _fp8_swiglu_case(M=M, K=1024, I=I, E=E, k=k, bm=128, num_ctas=ctas, skew=skew)
 
 
-def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, seed=0):
+def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, seed=0, num_ctas=0):
     g = torch.Generator().manual_seed(seed)
     M = R_tokens
     logits = torch.randn(M, E, generator=g)
@@ -318,7 +318,7 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
         L.grouped_gemm(dtype=L.DTYPE_BF16, epilogue=epilogue, a=a.cuda(), w=w.cuda(),
                        offsets=cu(lay["offsets"]), tile_offsets=cu(lay["tile_offsets"]), out=out,
                        ws=ws, block_m=bm, sorted_route_ids=cu(lay["sorted_route_ids"]),
-                       route_weights=cu(rw), M=M, top_k=k, sched=sched)
+                       route_weights=cu(rw), M=M, top_k=k, sched=sched, num_ctas=num_ctas)
         torch.cuda.synchronize()
         assert_close(out, oracle.scatter(Y, lay["route_slot"], rw), "bf16 scatter")
     else:
@@ -326,10 +326,25 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
         out = torch.zeros(M * k, N, dtype=dt, device="cuda")
         L.grouped_gemm(dtype=L.DTYPE_BF16, epilogue=epilogue, a=a.cuda(), w=w.cuda(),
                        offsets=cu(lay["offsets"]), tile_offsets=cu(lay["tile_offsets"]), out=out,
-                       ws=ws, block_m=bm, sched=sched)
+                       ws=ws, block_m=bm, sched=sched, num_ctas=num_ctas)
         torch.cuda.synchronize()
         assert_close(out, Y, "bf16 store")
     assert L.get_error(ws) == L.MOE_OK
+
+
+@pytest.mark.parametrize("R,K,N,E,k,epi,ctas", [
+    (1200, 1024, 1024, 4, 2, L.EPI_SCATTER, 4),      # two pairs loop over many tiles
+    (1200, 1024, 1024, 4, 2, L.EPI_STORE_BF16, 5),   # an odd grid: two pairs
+    (90, 640, 512, 16, 3, L.EPI_SCATTER, 0),         # tiles of 1..127 rows: the odd CTA's half empty
+    (600, 512, 512, 8, 2, L.EPI_STORE_BF16, 1),      # one CTA: the single-CTA 256-row tile
+])
+def test_gemm_bf16_cta_pairs(R, K, N, E, k, epi, ctas):
+    """BF16 scatter / bf16-rows store at block_m 256 with N a multiple of 256:
+    a cluster of two CTAs computes each 256 x 256 tile (M = 256 weight rows,
+    N = 256 routed rows, 128 of each staged per CTA) and each CTA holds its
+    weight rows' 128 x 256 accumulator, double-buffered in TMEM."""
+    assert L.gemm_cta_pairs() > 0, "the CTA-pair form is not in use on this device"
+    _bf16_gemm_case(R_tokens=R, K=K, N=N, E=E, k=k, bm=256, epilogue=epi, num_ctas=ctas)
 
 
 @pytest.mark.parametrize("bm", [16, 64, 128, 256])
