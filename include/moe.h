@@ -84,7 +84,8 @@ int moe_num_sms(void);
  * multiple of 256 (256 weight rows x 128 routed rows per tile), FP8 SWIGLU at
  * block_m 128 (256 routed rows x the gate and up rows of 128 h columns), BF16
  * SCATTER and STORE_BF16 at block_m 256 with N a multiple of 256 (256 weight
- * rows x 256 routed rows).  0: that form is unavailable (or on error) and those
+ * rows x 256 routed rows), BF16 SWIGLU at block_m 256 (as the FP8 SWIGLU
+ * form, accumulated over all of K).  0: that form is unavailable (or on error) and those
  * GEMMs run the single-CTA form.  The grid of such a GEMM is the even number of
  * CTAs min(num_ctas or the SM count, 2 x this). */
 int moe_gemm_cta_pairs(void);
@@ -157,8 +158,9 @@ typedef struct {
   int k_splits;               /* FP8 SCATTER: K split into this many tiles (0 = auto) */
   int num_ctas;               /* persistent CTAs (0 = one per SM).  With gather_rows 0,
                                  FP8 SCATTER (block_m 128, N a multiple of 256), FP8
-                                 SWIGLU (block_m 128) and BF16 SCATTER / STORE_BF16
-                                 (block_m 256, N a multiple of 256) run clusters of two
+                                 SWIGLU (block_m 128), BF16 SWIGLU (block_m 256) and BF16
+                                 SCATTER / STORE_BF16 (block_m 256, N a multiple of 256)
+                                 run clusters of two
                                  CTAs (moe_gemm_cta_pairs), each pair walking every
                                  (G/2)-th tile in a fixed order: the grid G is then
                                  num_ctas rounded down to even and capped at twice the

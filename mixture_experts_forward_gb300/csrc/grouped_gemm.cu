@@ -95,12 +95,14 @@ struct TileDesc {
 //     rows and holds its weight rows' 128 x 256 accumulator, so TMEM takes two
 //     tiles (the single-CTA 256 x 256 tile fills it) and a tile's reductions or
 //     stores overlap the next tile's MMAs.
-//   SwiGLU (token-major): a tile of 256 routed rows x the gate and up rows of
-//     128 h columns; each CTA stages 128 routed rows and one weight tile (the
-//     even CTA the gate rows, the odd one the up rows), 32 KB per K block
-//     against 48 KB for the single-CTA tile, and its TMEM holds gate and up
-//     (256 columns) for its own routed rows, so the SwiGLU and the 1x128
-//     re-quantisation stay within the CTA.
+//   SwiGLU (token-major; FP8 at block_m 128, BF16 at block_m 256): a tile of
+//     256 routed rows x the gate and up rows of 128 h columns; each CTA stages
+//     128 routed rows and one weight tile (the even CTA the gate rows, the odd
+//     one the up rows) and its TMEM holds gate and up (256 columns) for its
+//     own routed rows, so the SwiGLU (and the FP8 1x128 re-quantisation) stay
+//     within the CTA.  FP8: 32 KB per K block against 48 KB for the
+//     single-CTA tile; BF16: two accumulators in TMEM where the single-CTA
+//     gate + up tile fills it.
 template <int BM, bool kFP8, int kEpi, bool kWide = false, bool kCta2 = false>
 struct Cfg {
   static constexpr bool kSwiglu = kEpi == MOE_EPI_SWIGLU;
@@ -159,8 +161,8 @@ struct Cfg {
   static_assert(BM % 16 == 0 && BM >= 16 && BM <= 256, "block_m");
   static_assert(!kFP8 || BM <= 128, "FP8 block_m <= 128");
   static_assert(kTmemNeed <= 512, "TMEM");
-  static_assert(!kCta2 || (kFP8 && BM == 128 && !kWide &&
-                            ((!kPair && kEpi == MOE_EPI_SCATTER) || kSwiglu)) ||
+  static_assert(!kCta2 || (BM == 128 && !kWide && kSwiglu) ||
+                    (kFP8 && BM == 128 && !kPair && kEpi == MOE_EPI_SCATTER) ||
                     (!kFP8 && BM == 256 && !kPair &&
                      (kEpi == MOE_EPI_SCATTER || kEpi == MOE_EPI_STORE_BF16)),
                 "CTA pairs");
@@ -762,11 +764,13 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
             const uint32_t alo = smem_desc_lo(a_addr), blo = smem_desc_lo(b_addr);
             if constexpr (kCta2 && C::kSwiglu) {
               // M = 256 routed rows (128 per CTA), N = the gate rows (even CTA)
-              // and the up rows (odd CTA) of 128 h columns
-              constexpr uint32_t idesc_p = make_idesc(0u, 256u, 256u);
+              // and the up rows (odd CTA) of 128 h columns (FP8: one K block
+              // per buffer; BF16: accumulated over all of K)
+              constexpr uint32_t idesc_p = make_idesc(kFP8 ? 0u : 1u, 256u, 256u);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_lo<true, true>(d_tmem, blo + 2 * kk, alo + 2 * kk, idesc_p, kk > 0 ? 1u : 0u);
+                umma_lo<kFP8, true>(d_tmem, blo + 2 * kk, alo + 2 * kk, idesc_p,
+                                    (kFP8 ? kk > 0 : (i > 0 || kb > 0 || kk > 0)) ? 1u : 0u);
             } else if constexpr (kCta2 && !kFP8) {
               // BF16: M = 256 weight rows (128 per CTA), N = 256 routed rows (128
               // per CTA), accumulated over all of K
@@ -890,7 +894,54 @@ __global__ void __launch_bounds__(Cfg<BM, kFP8, kEpi, kWide, kCta2>::kThreads, 1
       const int col =
           d.n_tile * kWRows + ((kCta2 && !C::kSwiglu) ? static_cast<int>(rank) * kTileN : 0) + row;
 
-      if constexpr (C::kTok) {
+      if constexpr (kCta2 && C::kSwiglu && !kFP8) {
+        // Token-major BF16 SwiGLU pair tile: TMEM lane = routed row s of this
+        // CTA's half, columns [0, 128) the gate rows and [128, 256) the up rows
+        // of h columns n_tile * 128 + [0, 128), accumulated over all of K.  This
+        // warp: h columns [32 grp, +32) of its quadrant's 32 rows.
+        const int s = row;
+        const int buf = acc_n % C::kNumAcc;
+        const uint32_t use = static_cast<uint32_t>(acc_n / C::kNumAcc);
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&bar_tfull[buf]), use & 1u, &s_abort, tmo))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t base = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                              buf * C::kAccCols + 32 * grp;
+        float g[32], u[32];
+        tmem_ld16(base, *reinterpret_cast<float(*)[16]>(&g[0]));
+        tmem_ld16(base + 16, *reinterpret_cast<float(*)[16]>(&g[16]));
+        tmem_ld16(base + kTileN, *reinterpret_cast<float(*)[16]>(&u[0]));
+        tmem_ld16(base + kTileN + 16, *reinterpret_cast<float(*)[16]>(&u[16]));
+        tmem_ld_wait(*reinterpret_cast<float(*)[16]>(&g[0]));
+        tmem_ld_wait(*reinterpret_cast<float(*)[16]>(&g[16]));
+        tmem_ld_wait(*reinterpret_cast<float(*)[16]>(&u[0]));
+        tmem_ld_wait(*reinterpret_cast<float(*)[16]>(&u[16]));
+        tc_fence_before();                             // the tile is in registers: release it
+        __syncwarp();                                  // to the even CTA
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bar_tempty[buf]), 0));
+        ++acc_n;
+        if (s < d.rows) {
+          // silu(g) * u with the fast exponential and division, as the
+          // single-CTA BF16 SwiGLU epilogue; 32 bf16 = four 16-byte stores
+          const int I = p.N / 2;
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float h0 = __fdividef(g[j], 1.0f + __expf(-g[j])) * u[j];
+            const float h1 = __fdividef(g[j + 1], 1.0f + __expf(-g[j + 1])) * u[j + 1];
+            const __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+            w[j / 2] = *reinterpret_cast<const uint32_t*>(&b);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                static_cast<size_t>(d.m0 + s) * I +
+                                                d.n_tile * kTileN + 32 * grp);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+      } else if constexpr (C::kTok) {
         // Token-major pair tile: TMEM lane = routed row s of the tile, 256
         // accumulator columns = the two weight tiles' rows.  This warp's 64
         // columns: store / scatter [64 grp, +64) of tile grp / 2; SwiGLU the
@@ -1483,7 +1534,9 @@ bool select_gemm_variant(bool fp8, int epi, int bm, bool gather, bool wide, bool
                          GemmVariant& v) {
   if (cta2) {
     if (!gemm_cta2_supported(fp8, epi, bm) || gather || wide) return false;
-    if (!fp8)
+    if (!fp8 && epi == MOE_EPI_SWIGLU)   // 128 routed rows per CTA: block_m 256 per pair
+      v = variant<128, false, MOE_EPI_SWIGLU, false, false, true>();
+    else if (!fp8)
       v = epi == MOE_EPI_SCATTER ? variant<256, false, MOE_EPI_SCATTER, false, false, true>()
                                  : variant<256, false, MOE_EPI_STORE_BF16, false, false, true>();
     else if (epi == MOE_EPI_SWIGLU)
@@ -1540,7 +1593,8 @@ bool gemm_wide_supported(bool fp8, int epi, int bm) {
 
 bool gemm_cta2_supported(bool fp8, int epi, int bm) {
   if (fp8) return bm == 128 && (epi == MOE_EPI_SCATTER || epi == MOE_EPI_SWIGLU);
-  return bm == 256 && (epi == MOE_EPI_SCATTER || epi == MOE_EPI_STORE_BF16);
+  return bm == 256 && (epi == MOE_EPI_SCATTER || epi == MOE_EPI_STORE_BF16 ||
+                       epi == MOE_EPI_SWIGLU);
 }
 
 int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide, bool cta2) {

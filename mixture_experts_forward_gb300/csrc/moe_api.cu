@@ -269,7 +269,8 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
     if (!make_tmap_rows(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->M)))
       return MOE_ERR_CUDA;
   } else if (!make_tmap(&ta, a->a, fp8, static_cast<uint64_t>(a->K), static_cast<uint64_t>(a->R),
-                        static_cast<uint32_t>((p.cta2 && !swiglu) ? a->block_m / 2 : a->block_m),
+                        static_cast<uint32_t>((p.cta2 && !(fp8 && swiglu)) ? a->block_m / 2
+                                                                           : a->block_m),
                         static_cast<uint32_t>(p.sk))) {
     return MOE_ERR_CUDA;
   }

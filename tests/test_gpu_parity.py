@@ -308,7 +308,7 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
         out = torch.zeros(M * k, N // 2, dtype=torch.bfloat16, device="cuda")
         L.grouped_gemm(dtype=L.DTYPE_BF16, epilogue=epilogue, a=a.cuda(), w=w.cuda(),
                        offsets=cu(lay["offsets"]), tile_offsets=cu(lay["tile_offsets"]), out=out,
-                       ws=ws, block_m=bm, sched=sched)
+                       ws=ws, block_m=bm, sched=sched, num_ctas=num_ctas)
         torch.cuda.synchronize()
         gate, up = Y[:, :N // 2], Y[:, N // 2:]
         ref = gate / (1.0 + np.exp(-gate)) * up
@@ -337,12 +337,17 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
     (1200, 1024, 1024, 4, 2, L.EPI_STORE_BF16, 5),   # an odd grid: two pairs
     (90, 640, 512, 16, 3, L.EPI_SCATTER, 0),         # tiles of 1..127 rows: the odd CTA's half empty
     (600, 512, 512, 8, 2, L.EPI_STORE_BF16, 1),      # one CTA: the single-CTA 256-row tile
+    (1200, 1024, 1024, 4, 2, L.EPI_SWIGLU, 4),       # SwiGLU: two pairs, many tiles
+    (90, 640, 512, 16, 3, L.EPI_SWIGLU, 0),          # SwiGLU: the odd CTA's 128 rows empty
+    (700, 512, 512, 8, 3, L.EPI_SWIGLU, 3),          # SwiGLU: an odd grid
+    (600, 512, 512, 8, 2, L.EPI_SWIGLU, 1),          # SwiGLU: one CTA
 ])
 def test_gemm_bf16_cta_pairs(R, K, N, E, k, epi, ctas):
-    """BF16 scatter / bf16-rows store at block_m 256 with N a multiple of 256:
-    a cluster of two CTAs computes each 256 x 256 tile (M = 256 weight rows,
-    N = 256 routed rows, 128 of each staged per CTA) and each CTA holds its
-    weight rows' 128 x 256 accumulator, double-buffered in TMEM."""
+    """BF16 at block_m 256 on CTA pairs, each CTA's accumulator double-buffered
+    in TMEM.  Scatter / bf16-rows store (N a multiple of 256): each 256 x 256
+    tile has M = 256 weight rows and N = 256 routed rows, 128 of each staged per
+    CTA.  SwiGLU: token-major, M = 256 routed rows (128 per CTA) and N = the
+    gate rows (even CTA) and up rows (odd CTA) of 128 h columns."""
     assert L.gemm_cta_pairs() > 0, "the CTA-pair form is not in use on this device"
     _bf16_gemm_case(R_tokens=R, K=K, N=N, E=E, k=k, bm=256, epilogue=epi, num_ctas=ctas)
 
