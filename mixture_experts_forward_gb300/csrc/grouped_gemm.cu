@@ -1603,15 +1603,16 @@ int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide, bool cta2) {
   return v.stage_bytes;
 }
 
-// Clusters of two CTAs of the CTA-pair kernels (one CTA per SM, 608 threads,
-// the same for the scatter and SwiGLU forms) that can be resident at once; 0
-// if unknown.  Cached per device: the first call sets the
-// kernel's shared-memory limit and asks the occupancy calculator.
-int gemm_cta2_max_clusters() {
+// Clusters of two CTAs of the CTA-pair kernels (one CTA per SM, at most 608
+// threads) that can be resident at once; 0 if unknown.  Cached per device: the
+// first call sets the kernel's shared-memory limit and asks the occupancy
+// calculator — unless `query` is false (a caller inside a stream capture),
+// which then gets 0 and the single-CTA form.
+int gemm_cta2_max_clusters(bool query) {
   static int cached[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] > 0) return cached[dev];
+  if (cached[dev] > 0 || !query) return cached[dev];
   const GemmVariant v = variant<128, true, MOE_EPI_SCATTER, false, false, true>();
   // more than half of an SM's shared memory (one CTA per SM), leaving the
   // per-block limit room for the kernel's static shared memory

@@ -206,7 +206,11 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   const bool swiglu = a->epilogue == MOE_EPI_SWIGLU;
   if ((p.wide || swiglu) && a->gather_rows == 0 &&
       gemm_cta2_supported(fp8, a->epilogue, a->block_m)) {
-    const int max_cl = gemm_cta2_max_clusters();
+    // (the first query per device is kept out of stream captures)
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const bool capturing =
+        cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone;
+    const int max_cl = gemm_cta2_max_clusters(!capturing);
     const int pairs = (ctas < 2 * max_cl ? ctas : 2 * max_cl) / 2;
     if (pairs >= 1) {
       p.cta2 = 1;
@@ -605,7 +609,7 @@ moe_status_t forward_impl(const moe_forward_args* f, const float* logits, const 
       return cuda_status(cudaGraphLaunch(g_graphs[i].exec, stream));
   }
   // host-side queries the launches make once per device, kept out of the capture
-  if (f->dtype == MOE_DTYPE_FP8_E4M3) gemm_cta2_max_clusters();
+  gemm_cta2_max_clusters();
   // The launch sequence is recorded on a private stream (the caller's may be
   // the legacy default stream, which cannot be captured); the graph itself
   // is then launched on the caller's stream.

@@ -134,7 +134,7 @@ int gemm_stage_bytes(bool fp8, int epi, int bm, bool wide = false, bool cta2 = f
 bool gemm_wide_supported(bool fp8, int epi, int bm);
 // FP8 scatter tiles of 256 weight rows computed by a cluster of two CTAs
 bool gemm_cta2_supported(bool fp8, int epi, int bm);
-int gemm_cta2_max_clusters();
+int gemm_cta2_max_clusters(bool query = true);
 int gemm_meta_bytes(bool fp8, int bm, int kb_per_split, bool pair = false);
 int gemm_rows_bytes(bool fp8, int bm);   // the route-id ring of the gathered-rows mode
 // shared memory after the tables: the gathered-rows ring, or the FP8 SwiGLU
