@@ -88,6 +88,9 @@ def parse():
     ap.add_argument("--block-m", type=int, default=0)
     ap.add_argument("--k-splits", type=int, default=0)
     ap.add_argument("--sched", choices=["queue", "static"], default="queue")
+    ap.add_argument("--cta-pairs", choices=["on", "off"], default="on",
+                    help="grouped GEMMs on clusters of two CTAs where that form exists (on), "
+                         "or single CTAs only (off)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -259,13 +262,14 @@ def bench_ours(args, rank, world, local):
     kind, d, desc = workload(args.config, args, args.seed + rank)
     c = d["cfg"]
     sched = L.SCHED_QUEUE if args.sched == "queue" else L.SCHED_STATIC
+    pairs = 0 if args.cta_pairs == "on" else -1
     if kind == "fp8":
         logits, x = d["logits"].to(dev), d["x"].to(dev)
         w, ws_ = d["w_q"].to(dev), d["w_scales"].to(dev)
         M, K, N, E, k = c["M"], c["K"], c["N"], c["E"], c["k"]
         fa = L.forward_args(dtype=L.DTYPE_FP8, M=M, K=K, N=N, E=E, top_k=k, softcap=c["softcap"],
                             logits=logits, x=x, w=w, w_scales=ws_, block_m=args.block_m,
-                            sched=sched, k_splits=args.k_splits, use_graph=1)
+                            sched=sched, k_splits=args.k_splits, use_graph=1, cta_pairs=pairs)
         out_cols = N
     elif kind == "fp8ffn":
         logits, x = d["logits"].to(dev), d["x"].to(dev)
@@ -275,7 +279,7 @@ def bench_ours(args, rank, world, local):
         fa = L.forward_args(dtype=L.DTYPE_FP8, gated=1, M=M, K=K, N=N, E=E, top_k=k, softcap=0.0,
                             logits=logits, x=x, w=wu, w_scales=wus, w2=wd, w2_scales=wds,
                             block_m=args.block_m, sched=sched, k_splits=args.k_splits,
-                            use_graph=1)
+                            use_graph=1, cta_pairs=pairs)
         out_cols = K
     else:
         logits, x = d["logits"].to(dev), d["x"].to(dev)
@@ -283,7 +287,7 @@ def bench_ours(args, rank, world, local):
         M, K, N, E, k = c["T"], c["H"], c["I"], c["E"], c["k"]
         fa = L.forward_args(dtype=L.DTYPE_BF16, M=M, K=K, N=N, E=E, top_k=k, softcap=0.0,
                             logits=logits, x=x, w=w, w2=w2, block_m=args.block_m, sched=sched,
-                            use_graph=1)
+                            use_graph=1, cta_pairs=pairs)
         out_cols = K
     ws = L.new_workspace(L.workspace_size(fa), device=dev)
     out = torch.empty(M, out_cols, dtype=torch.bfloat16, device=dev)
@@ -333,7 +337,7 @@ def bench_ours(args, rank, world, local):
     pk = peaks()
 
     roof = dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, flush,
-                           touched, pk, cfg_name=args.config)
+                           touched, pk, cfg_name=args.config, cta_pairs=pairs)
     if kind == "fp8":
         alg_bytes = touched * (N * K + (N // 128) * (K // 128) * 4) + M * E * 4 + M * K * 2 + M * N * 2
         t_roof = max(fl / (pk["fp8"] * 1e12), alg_bytes / (pk["hbm"] * 1e9))
@@ -364,6 +368,7 @@ def bench_ours(args, rank, world, local):
         "dtype": "bf16" if kind == "bf16" else "fp8_e4m3", "data": "synthetic (seeded)",
         "config": {"workload": desc, "l2": "flushed between steps (256 MiB write, then 256 MiB read)",
                    "block_m": block_m, "k_splits": k_splits, "sched": args.sched,
+                   "cta_pairs": args.cta_pairs,
                    "touched_experts": touched, "compact_rows": int(M * k),
                    "parallelism": f"replicas x{world} (token data-parallel, no collective)"},
         "forward_roofline": {"bound": "hbm" if t_roof == alg_bytes / (pk["hbm"] * 1e9) else "tensor",
@@ -382,7 +387,7 @@ def bench_ours(args, rank, world, local):
 
 
 def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, flush, touched, pk,
-                    cfg_name=""):
+                    cfg_name="", cta_pairs=0):
     """Time the grouped GEMM alone (same inputs and tiling as the forward) with
     CUDA events on its stream and report it against its roofline."""
     stream = torch.cuda.current_stream(dev)
@@ -405,7 +410,8 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
                            a=a_q, a_scales=a_s, w=w,
                            w_scales=w_s, offsets=lay["offsets"], tile_offsets=lay["tile_offsets"],
                            out=acc, ws=ws, block_m=block_m, sorted_route_ids=lay["sorted_route_ids"],
-                           route_weights=wts, M=M, top_k=k, sched=sched, k_splits=k_splits)
+                           route_weights=wts, M=M, top_k=k, sched=sched, k_splits=k_splits,
+                           cta_pairs=cta_pairs)
         out_bytes = M * N * 4 if small else R * N * 2
         alg = touched * (N * K + (N // 128) * (K // 128) * 4) + R * K + (K // 128) * R * 4 + out_bytes
         fl = 2.0 * R * N * K
@@ -425,7 +431,7 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
             L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_SWIGLU, a=a_q, a_scales=a_s, w=w,
                            w_scales=w_s, offsets=lay["offsets"], tile_offsets=lay["tile_offsets"],
                            out=h_q, out_scales=h_s, ws=ws, block_m=block_m, M=T, top_k=k,
-                           sched=sched, k_splits=1)
+                           sched=sched, k_splits=1, cta_pairs=cta_pairs)
         alg = touched * (2 * I * H + (2 * I // 128) * (H // 128) * 4) + R * H + (H // 128) * R * 4 \
             + R * I + (I // 128) * R * 4
         fl = 2.0 * R * (2 * I) * H
@@ -444,7 +450,7 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
         def launch():
             L.grouped_gemm(dtype=L.DTYPE_BF16, epilogue=L.EPI_SWIGLU, a=a, w=w,
                            offsets=lay["offsets"], tile_offsets=lay["tile_offsets"], out=h,
-                           ws=ws, block_m=block_m, M=T, top_k=k, sched=sched)
+                           ws=ws, block_m=block_m, M=T, top_k=k, sched=sched, cta_pairs=cta_pairs)
         alg = touched * (2 * I) * H * 2 + R * H * 2 + R * I * 2
         fl = 2.0 * R * (2 * I) * H
         name = "grouped_gemm_kernel<bf16, swiglu>"
@@ -476,7 +482,8 @@ def dominant_kernel(L, kind, c, fa, d, dev, block_m, k_splits, sched, lay, ids, 
     t_hbm = alg / (pk["hbm"] * 1e9)
     fp8 = kind in ("fp8", "fp8ffn")
     t_tc = fl / ((pk["fp8"] if fp8 else pk["bf16"]) * 1e12)
-    traffic = stored_traffic(src, name, cfg_name)
+    # (the committed captures are of the default build: CTA pairs on)
+    traffic = stored_traffic(src, name, cfg_name) if cta_pairs == 0 else None
     if t_hbm >= t_tc:
         achieved = alg / avg_s / 1e9
         return {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1),

@@ -175,6 +175,9 @@ typedef struct {
                                  SWIGLU epilogue; others: MOE_ERR_UNSUPPORTED */
   float* out_scales;          /* FP8 SWIGLU only: f32 [N/256, R] block scales of h (see
                                  moe_epilogue_t); ignored otherwise */
+  int cta_pairs;              /* 0: tiles on clusters of two CTAs wherever that form
+                                 exists (see num_ctas and moe_gemm_cta_pairs); -1: single
+                                 CTAs only.  Other values: MOE_ERR_INVALID_ARG */
 } moe_gemm_args;
 
 /* Grouped GEMM — "Fused MoE FP8" section "Baseline: 7 kernels" item 6, with
@@ -253,6 +256,8 @@ typedef struct {
                              projection's epilogue (MOE_EPI_SWIGLU, FP8); output [M,K].  0 = the single FP8 GEMM.  BF16:
                              must be 0 or 1 (its forward is always the gated FFN) */
   const float* w2_scales; /* FP8 with gated = 1: [E,K/128,N/128] */
+  int cta_pairs;          /* the grouped GEMMs' cta_pairs (see moe_gemm_args): 0 = CTA
+                             pairs wherever that form exists, -1 = single CTAs only */
 } moe_forward_args;
 
 /* Workspace bytes needed by moe_forward / moe_forward_host for these

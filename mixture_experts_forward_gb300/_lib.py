@@ -46,7 +46,8 @@ class GemmArgs(ctypes.Structure):
                 ("offsets", ctypes.c_void_p), ("tile_offsets", ctypes.c_void_p),
                 ("sorted_route_ids", ctypes.c_void_p), ("route_weights", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("k_splits", ctypes.c_int), ("num_ctas", ctypes.c_int),
-                ("gather_rows", ctypes.c_int), ("out_scales", ctypes.c_void_p)]
+                ("gather_rows", ctypes.c_int), ("out_scales", ctypes.c_void_p),
+                ("cta_pairs", ctypes.c_int)]
 
 
 class ForwardArgs(ctypes.Structure):
@@ -57,7 +58,8 @@ class ForwardArgs(ctypes.Structure):
                 ("w_scales", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("block_m", ctypes.c_int), ("sched", ctypes.c_int), ("k_splits", ctypes.c_int),
                 ("use_graph", ctypes.c_int), ("gather_rows", ctypes.c_int),
-                ("gated", ctypes.c_int), ("w2_scales", ctypes.c_void_p)]
+                ("gated", ctypes.c_int), ("w2_scales", ctypes.c_void_p),
+                ("cta_pairs", ctypes.c_int)]
 
 
 class WorkspaceMap(ctypes.Structure):
@@ -174,10 +176,11 @@ def quant_gather(x: torch.Tensor, k: int, route_slot: torch.Tensor, zero_acc=Non
 def grouped_gemm(*, dtype, epilogue, a, w, offsets, tile_offsets, out, ws, block_m,
                  a_scales=None, w_scales=None, sorted_route_ids=None, route_weights=None,
                  M=0, top_k=0, sched=SCHED_QUEUE, k_splits=0, num_ctas=0, gather_rows=0,
-                 out_scales=None, stream=None):
+                 out_scales=None, cta_pairs=0, stream=None):
     """moe_grouped_gemm.  gather_rows=1: `a` (and FP8 a_scales) are token-major
     and compact slot s reads row sorted_route_ids[s] // top_k.  FP8 SWIGLU:
-    out = u8 [R, N/2] codes of h, out_scales = f32 [N/256, R]."""
+    out = u8 [R, N/2] codes of h, out_scales = f32 [N/256, R].  cta_pairs=-1:
+    single CTAs only (0: CTA pairs wherever that form exists)."""
     E, N, K = w.shape
     R = sorted_route_ids.numel() if gather_rows else a.shape[0]
     g = GemmArgs(dtype=dtype, epilogue=epilogue, sched=sched, block_m=block_m, E=E, N=N, K=K,
@@ -189,7 +192,8 @@ def grouped_gemm(*, dtype, epilogue, a, w, offsets, tile_offsets, out, ws, block
                  route_weights=None if route_weights is None else route_weights.data_ptr(),
                  out=out.data_ptr(), k_splits=k_splits, num_ctas=num_ctas,
                  gather_rows=gather_rows,
-                 out_scales=None if out_scales is None else out_scales.data_ptr())
+                 out_scales=None if out_scales is None else out_scales.data_ptr(),
+                 cta_pairs=cta_pairs)
     _check(lib().moe_grouped_gemm(ctypes.byref(g), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_grouped_gemm")
     return out
@@ -198,7 +202,7 @@ def grouped_gemm(*, dtype, epilogue, a, w, offsets, tile_offsets, out, ws, block
 def grouped_gemm_noalloc(*, dtype, epilogue, a, w, offsets, tile_offsets, out, block_m,
                          a_scales=None, w_scales=None, sorted_route_ids=None, route_weights=None,
                          M=0, top_k=0, sched=SCHED_QUEUE, k_splits=0, num_ctas=0,
-                         out_scales=None, stream=None):
+                         out_scales=None, cta_pairs=0, stream=None):
     """moe_grouped_gemm_noalloc: the same GEMM with the library's own static
     scratch instead of a workspace (for callers that cannot allocate)."""
     E, N, K = w.shape
@@ -210,7 +214,8 @@ def grouped_gemm_noalloc(*, dtype, epilogue, a, w, offsets, tile_offsets, out, b
                  sorted_route_ids=None if sorted_route_ids is None else sorted_route_ids.data_ptr(),
                  route_weights=None if route_weights is None else route_weights.data_ptr(),
                  out=out.data_ptr(), k_splits=k_splits, num_ctas=num_ctas,
-                 out_scales=None if out_scales is None else out_scales.data_ptr())
+                 out_scales=None if out_scales is None else out_scales.data_ptr(),
+                 cta_pairs=cta_pairs)
     _check(lib().moe_grouped_gemm_noalloc(ctypes.byref(g), _stream(stream)),
            "moe_grouped_gemm_noalloc")
     return out
@@ -240,9 +245,10 @@ def swiglu_quant(gu: torch.Tensor, stream=None):
 # ------------------------------------------------------------------ forward
 def forward_args(*, dtype, M, K, N, E, top_k, softcap=0.0, renorm=1, logits=None, x=None, w=None,
                  w_scales=None, w2=None, block_m=0, sched=SCHED_QUEUE, k_splits=0,
-                 use_graph=1, gather_rows=0, gated=0, w2_scales=None) -> ForwardArgs:
+                 use_graph=1, gather_rows=0, gated=0, w2_scales=None, cta_pairs=0) -> ForwardArgs:
     """Arguments of moe_forward.  gated=1 with dtype FP8: the FP8 gated FFN
-    (w = w_up codes [E,2N,K] + w_scales, w2 = w_down codes [E,K,N] + w2_scales)."""
+    (w = w_up codes [E,2N,K] + w_scales, w2 = w_down codes [E,K,N] + w2_scales).
+    cta_pairs=-1: the grouped GEMMs on single CTAs only."""
     return ForwardArgs(dtype=dtype, M=M, K=K, N=N, E=E, top_k=top_k, softcap=float(softcap),
                        renorm=int(renorm), logits=None if logits is None else logits.data_ptr(),
                        x=None if x is None else x.data_ptr(),
@@ -251,7 +257,8 @@ def forward_args(*, dtype, M, K, N, E, top_k, softcap=0.0, renorm=1, logits=None
                        w2=None if w2 is None else w2.data_ptr(), block_m=block_m, sched=sched,
                        k_splits=k_splits, use_graph=use_graph, gather_rows=gather_rows,
                        gated=gated,
-                       w2_scales=None if w2_scales is None else w2_scales.data_ptr())
+                       w2_scales=None if w2_scales is None else w2_scales.data_ptr(),
+                       cta_pairs=cta_pairs)
 
 
 def workspace_size(args: ForwardArgs) -> int:

@@ -119,6 +119,7 @@ moe_status_t check_gemm(const moe_gemm_args* a) {
   if (a->dtype != MOE_DTYPE_FP8_E4M3 && a->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (a->epilogue < MOE_EPI_SCATTER || a->epilogue > MOE_EPI_STORE_BF16) return MOE_ERR_INVALID_ARG;
   if (a->sched != MOE_SCHED_QUEUE && a->sched != MOE_SCHED_STATIC) return MOE_ERR_INVALID_ARG;
+  if (a->cta_pairs != 0 && a->cta_pairs != -1) return MOE_ERR_INVALID_ARG;
   if (a->E <= 0 || a->N <= 0 || a->K <= 0 || a->R <= 0) return MOE_ERR_INVALID_ARG;
   if (a->a == nullptr || a->w == nullptr || a->offsets == nullptr || a->tile_offsets == nullptr ||
       a->out == nullptr)
@@ -204,7 +205,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   // fit at once
   int ctas = a->num_ctas > 0 ? a->num_ctas : sms;
   const bool swiglu = a->epilogue == MOE_EPI_SWIGLU;
-  if ((p.wide || swiglu) && a->gather_rows == 0 &&
+  if (a->cta_pairs == 0 && (p.wide || swiglu) && a->gather_rows == 0 &&
       gemm_cta2_supported(fp8, a->epilogue, a->block_m)) {
     // (the first query per device is kept out of stream captures)
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -383,6 +384,7 @@ moe_status_t check_forward(const moe_forward_args* f) {
   if (!forward_shape_ok(f)) return MOE_ERR_INVALID_ARG;
   if (f->dtype != MOE_DTYPE_FP8_E4M3 && f->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
   if (f->sched != MOE_SCHED_QUEUE && f->sched != MOE_SCHED_STATIC) return MOE_ERR_INVALID_ARG;
+  if (f->cta_pairs != 0 && f->cta_pairs != -1) return MOE_ERR_INVALID_ARG;
   if (f->w == nullptr) return MOE_ERR_INVALID_ARG;
   if (f->E > 1024 || f->top_k > 32 || f->top_k > f->E) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(f->M) * f->top_k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
@@ -462,6 +464,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
     std::memset(&g, 0, sizeof(g));
     g.dtype = MOE_DTYPE_FP8_E4M3;
     g.sched = f->sched;
+    g.cta_pairs = f->cta_pairs;
     g.block_m = bm;
     g.E = E;
     g.K = K;
@@ -527,6 +530,7 @@ moe_status_t enqueue_forward(const moe_forward_args* f, const float* logits, con
   g.dtype = MOE_DTYPE_BF16;
   g.epilogue = MOE_EPI_SWIGLU;
   g.sched = f->sched;
+  g.cta_pairs = f->cta_pairs;
   g.block_m = bm;
   g.E = E;
   g.N = 2 * N;

@@ -92,6 +92,7 @@ def _gemm(**kw):
     (dict(dtype=L.DTYPE_BF16, epilogue=L.EPI_SWIGLU, N=384), L.MOE_ERR_UNSUPPORTED),
     (dict(epilogue=4), L.MOE_ERR_INVALID_ARG), (dict(epilogue=-1), L.MOE_ERR_INVALID_ARG),
     (dict(epilogue=L.EPI_STORE_BF16, k_splits=2), L.MOE_ERR_UNSUPPORTED),
+    (dict(cta_pairs=1), L.MOE_ERR_INVALID_ARG), (dict(cta_pairs=-2), L.MOE_ERR_INVALID_ARG),
 ])
 def test_gemm_argument_errors(lib, kw, code):
     g = _gemm(**kw)
@@ -144,6 +145,17 @@ def test_forward_gather_rows_workspace(lib):
             L.workspace_size(_fwd(dtype=L.DTYPE_FP8, **small)))
     for bad in (2, -1):
         assert lib.moe_workspace_size(ctypes.byref(_fwd(dtype=L.DTYPE_FP8, gather_rows=bad,
+                                                        **big))) == 0
+
+
+def test_forward_cta_pairs_argument(lib):
+    """cta_pairs is 0 (CTA pairs where that form exists) or -1 (single CTAs);
+    it does not change the workspace."""
+    big = dict(M=4096, K=2048, N=512, E=256, top_k=8)
+    on = L.workspace_size(_fwd(dtype=L.DTYPE_FP8, **big))
+    assert on > 0 and L.workspace_size(_fwd(dtype=L.DTYPE_FP8, cta_pairs=-1, **big)) == on
+    for bad in (1, -2):
+        assert lib.moe_workspace_size(ctypes.byref(_fwd(dtype=L.DTYPE_FP8, cta_pairs=bad,
                                                         **big))) == 0
 
 

@@ -49,14 +49,14 @@ def test_swiglu_quant_bit_exact(R, I):
     assert np.array_equal(np_(h_s).view(np.uint32), rs.view(np.uint32))
 
 
-def _run_ffn_fp8(d, block_m=0, sched=L.SCHED_QUEUE, use_graph=1, gather_rows=0):
+def _run_ffn_fp8(d, block_m=0, sched=L.SCHED_QUEUE, use_graph=1, gather_rows=0, cta_pairs=0):
     c = d["cfg"]
     dev = {k: d[k].cuda() for k in ("logits", "x", "wup_q", "wup_s", "wdn_q", "wdn_s")}
     args = L.forward_args(dtype=L.DTYPE_FP8, gated=1, M=c["T"], K=c["H"], N=c["I"], E=c["E"],
                           top_k=c["k"], softcap=0.0, logits=dev["logits"], x=dev["x"],
                           w=dev["wup_q"], w_scales=dev["wup_s"], w2=dev["wdn_q"],
                           w2_scales=dev["wdn_s"], block_m=block_m, sched=sched,
-                          use_graph=use_graph, gather_rows=gather_rows)
+                          use_graph=use_graph, gather_rows=gather_rows, cta_pairs=cta_pairs)
     ws = L.new_workspace(L.workspace_size(args))
     out = torch.empty(c["T"], c["H"], dtype=torch.bfloat16, device="cuda")
     L.forward(args, out, ws)
@@ -84,14 +84,16 @@ def test_forward_ffn_fp8_small_batch_all_rows(use_graph):
     _check_ffn_fp8(d, out, 10**9, f"ffn fp8 small graph={use_graph}")
 
 
-@pytest.mark.parametrize("bm,gather", [(64, 0), (128, 0), (128, 1)])
-def test_forward_ffn_fp8_large_batch_all_rows(bm, gather):
+@pytest.mark.parametrize("bm,gather,pairs", [(64, 0, 0), (128, 0, 0), (128, 1, 0), (128, 0, -1)])
+def test_forward_ffn_fp8_large_batch_all_rows(bm, gather, pairs):
     """6000 routes (ragged expert tiles, three blocks of I): route + rank,
-    quantise + gather (or token-major codes gathered by the up projection)."""
+    quantise + gather (or token-major codes gathered by the up projection);
+    at block_m 128 both projections on CTA pairs, or (pairs = -1) on single
+    CTAs."""
     d = inputs.make_fp8_ffn_inputs("ffn_fp8", routing="zipf1.2", T=1500, H=512, I=384, E=16,
                                    k=4, seed=2)
-    out = _run_ffn_fp8(d, block_m=bm, gather_rows=gather)
-    _check_ffn_fp8(d, out, 10**9, f"ffn fp8 large bm={bm} gather={gather}")
+    out = _run_ffn_fp8(d, block_m=bm, gather_rows=gather, cta_pairs=pairs)
+    _check_ffn_fp8(d, out, 10**9, f"ffn fp8 large bm={bm} gather={gather} pairs={pairs}")
 
 
 def test_forward_ffn_fp8_bf16_rows_path_sampled():

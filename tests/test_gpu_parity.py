@@ -121,7 +121,7 @@ def test_quant_gather_bit_exact(M, K, k):
 
 # ------------------------------------------------------------------ grouped GEMM
 def _fp8_gemm_case(M, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, k_splits=0, seed=0,
-                   skew=0.0, num_ctas=0):
+                   skew=0.0, num_ctas=0, cta_pairs=0):
     d = inputs.make_fp8_inputs(dict(M=M, K=K, N=N, E=E, k=k, softcap=0.0, zipf_bias=skew),
                                seed=seed)
     rid, rw = oracle.route(d["logits"].numpy(), k)
@@ -156,7 +156,8 @@ def _fp8_gemm_case(M, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, k_splits=0,
                        w=d["w_q"].cuda(), w_scales=d["w_scales"].cuda(), offsets=cu(lay["offsets"]),
                        tile_offsets=cu(lay["tile_offsets"]), out=out, ws=ws, block_m=bm,
                        sorted_route_ids=cu(lay["sorted_route_ids"]), route_weights=cu(rw),
-                       M=M, top_k=k, sched=sched, k_splits=k_splits, num_ctas=num_ctas)
+                       M=M, top_k=k, sched=sched, k_splits=k_splits, num_ctas=num_ctas,
+                       cta_pairs=cta_pairs)
         torch.cuda.synchronize()
         assert L.get_error(ws) == L.MOE_OK
         ref = oracle.scatter(Y, lay["route_slot"], rw)
@@ -215,6 +216,20 @@ def test_gemm_fp8_scatter_cta_pairs(M, E, k, N, ctas, skew):
                    num_ctas=ctas)
 
 
+@pytest.mark.parametrize("form", ["fp8_scatter", "fp8_swiglu", "bf16_scatter", "bf16_swiglu"])
+def test_gemm_cta_pairs_off(form):
+    """cta_pairs = -1: shapes that have a CTA-pair form run single CTAs."""
+    if form == "fp8_scatter":
+        _fp8_gemm_case(M=700, K=1024, N=512, E=8, k=3, bm=128, epilogue=L.EPI_SCATTER, skew=1.5,
+                       cta_pairs=-1)
+    elif form == "fp8_swiglu":
+        _fp8_swiglu_case(M=700, K=1024, I=256, E=8, k=3, bm=128, skew=1.5, cta_pairs=-1)
+    else:
+        _bf16_gemm_case(R_tokens=600, K=512, N=512, E=8, k=2, bm=256,
+                        epilogue=L.EPI_SCATTER if form == "bf16_scatter" else L.EPI_SWIGLU,
+                        cta_pairs=-1)
+
+
 def _e4m3_order(c: np.ndarray) -> np.ndarray:
     """Signed position of an E4M3 code on the number line; 0x00 and 0x80 both 0."""
     c = c.astype(np.int32)
@@ -222,7 +237,8 @@ def _e4m3_order(c: np.ndarray) -> np.ndarray:
     return np.where(c & 0x80, -mag, mag)
 
 
-def _fp8_swiglu_case(M, K, I, E, k, bm, sched=L.SCHED_QUEUE, num_ctas=0, skew=1.0, seed=0):
+def _fp8_swiglu_case(M, K, I, E, k, bm, sched=L.SCHED_QUEUE, num_ctas=0, skew=1.0, seed=0,
+                     cta_pairs=0):
     """The FP8 SWIGLU epilogue (gate rows [0, I), up rows [I, 2I) of [E, 2I, K])
     against the oracle's pipeline: binary64 up projection of the same codes
     rounded to binary32, then its SwiGLU + 1x128 rule.  The device accumulates
@@ -245,7 +261,7 @@ def _fp8_swiglu_case(M, K, I, E, k, bm, sched=L.SCHED_QUEUE, num_ctas=0, skew=1.
     L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_SWIGLU, a=cu(a_q), a_scales=cu(a_s),
                    w=d["w_q"].cuda(), w_scales=d["w_scales"].cuda(), offsets=cu(lay["offsets"]),
                    tile_offsets=cu(lay["tile_offsets"]), out=h_q, out_scales=h_s, ws=ws,
-                   block_m=bm, sched=sched, num_ctas=num_ctas)
+                   block_m=bm, sched=sched, num_ctas=num_ctas, cta_pairs=cta_pairs)
     torch.cuda.synchronize()
     assert L.get_error(ws) == L.MOE_OK
     hq, hs = np_(h_q), np_(h_s)
@@ -287,7 +303,8 @@ def test_gemm_fp8_swiglu_cta_pairs(M, E, k, I, ctas, skew):
     _fp8_swiglu_case(M=M, K=1024, I=I, E=E, k=k, bm=128, num_ctas=ctas, skew=skew)
 
 
-def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, seed=0, num_ctas=0):
+def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, seed=0, num_ctas=0,
+                    cta_pairs=0):
     g = torch.Generator().manual_seed(seed)
     M = R_tokens
     logits = torch.randn(M, E, generator=g)
@@ -308,7 +325,8 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
         out = torch.zeros(M * k, N // 2, dtype=torch.bfloat16, device="cuda")
         L.grouped_gemm(dtype=L.DTYPE_BF16, epilogue=epilogue, a=a.cuda(), w=w.cuda(),
                        offsets=cu(lay["offsets"]), tile_offsets=cu(lay["tile_offsets"]), out=out,
-                       ws=ws, block_m=bm, sched=sched, num_ctas=num_ctas)
+                       ws=ws, block_m=bm, sched=sched, num_ctas=num_ctas,
+                       cta_pairs=cta_pairs)
         torch.cuda.synchronize()
         gate, up = Y[:, :N // 2], Y[:, N // 2:]
         ref = gate / (1.0 + np.exp(-gate)) * up
@@ -318,7 +336,8 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
         L.grouped_gemm(dtype=L.DTYPE_BF16, epilogue=epilogue, a=a.cuda(), w=w.cuda(),
                        offsets=cu(lay["offsets"]), tile_offsets=cu(lay["tile_offsets"]), out=out,
                        ws=ws, block_m=bm, sorted_route_ids=cu(lay["sorted_route_ids"]),
-                       route_weights=cu(rw), M=M, top_k=k, sched=sched, num_ctas=num_ctas)
+                       route_weights=cu(rw), M=M, top_k=k, sched=sched, num_ctas=num_ctas,
+                       cta_pairs=cta_pairs)
         torch.cuda.synchronize()
         assert_close(out, oracle.scatter(Y, lay["route_slot"], rw), "bf16 scatter")
     else:
@@ -326,7 +345,8 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
         out = torch.zeros(M * k, N, dtype=dt, device="cuda")
         L.grouped_gemm(dtype=L.DTYPE_BF16, epilogue=epilogue, a=a.cuda(), w=w.cuda(),
                        offsets=cu(lay["offsets"]), tile_offsets=cu(lay["tile_offsets"]), out=out,
-                       ws=ws, block_m=bm, sched=sched, num_ctas=num_ctas)
+                       ws=ws, block_m=bm, sched=sched, num_ctas=num_ctas,
+                       cta_pairs=cta_pairs)
         torch.cuda.synchronize()
         assert_close(out, Y, "bf16 store")
     assert L.get_error(ws) == L.MOE_OK
