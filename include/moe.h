@@ -197,9 +197,13 @@ moe_status_t moe_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_byt
 
 /* Standalone weighted scatter (unfused form of "Baseline: 7 kernels" item 7):
  * out[t,n] = bf16( sum_j weights[t*top_k+j] * rows[route_slot[t*top_k+j], n] )
- * with the sum in j order in fp32.  rows: f32 [M*top_k, N]; out: bf16 [M,N]. */
+ * with the sum in j order in fp32.  rows: f32 [M*top_k, N]; out: bf16 [M,N].
+ * ws: workspace of at least MOE_CTRL_BYTES, 256-byte aligned (else
+ * MOE_ERR_WORKSPACE): a route whose slot lies outside [0, M*top_k) adds nothing
+ * and records MOE_ERR_DEVICE_FAULT in its status word (read with
+ * moe_get_error). */
 moe_status_t moe_scatter(const float* rows, const int32_t* route_slot, const float* weights,
-                         int M, int N, int top_k, void* out, void* stream);
+                         int M, int N, int top_k, void* out, void* ws, void* stream);
 
 /* SwiGLU + re-quantisation between the projections of the FP8 gated FFN (the
  * two-layer expert MLP — gate+up projection, SiLU, down projection — of "Fused

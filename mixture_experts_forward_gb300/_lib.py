@@ -91,7 +91,7 @@ def lib():
         L.moe_quant_gather.argtypes = [P, I, I, I, P, P, P, P, I, P]
         L.moe_grouped_gemm.argtypes = [ctypes.POINTER(GemmArgs), P, ctypes.c_size_t, P]
         L.moe_grouped_gemm_noalloc.argtypes = [ctypes.POINTER(GemmArgs), P]
-        L.moe_scatter.argtypes = [P, P, P, I, I, I, P, P]
+        L.moe_scatter.argtypes = [P, P, P, I, I, I, P, P, P]
         L.moe_swiglu_quant.argtypes = [P, I, I, P, P, P]
         L.moe_workspace_size.argtypes = [ctypes.POINTER(ForwardArgs)]
         L.moe_workspace_size.restype = ctypes.c_size_t
@@ -221,12 +221,15 @@ def grouped_gemm_noalloc(*, dtype, epilogue, a, w, offsets, tile_offsets, out, b
     return out
 
 
-def scatter(rows: torch.Tensor, route_slot: torch.Tensor, weights: torch.Tensor, stream=None):
+def scatter(rows: torch.Tensor, route_slot: torch.Tensor, weights: torch.Tensor,
+            ws: torch.Tensor, stream=None):
+    """moe_scatter: out bf16 [M, N]; a route with an out-of-range slot records
+    MOE_ERR_DEVICE_FAULT in ws's status word (get_error)."""
     M, k = weights.shape
     N = rows.shape[1]
     out = torch.empty(M, N, dtype=torch.bfloat16, device=rows.device)
     _check(lib().moe_scatter(_ptr(rows), _ptr(route_slot), _ptr(weights), M, N, k, _ptr(out),
-                             _stream(stream)), "moe_scatter")
+                             _ptr(ws), _stream(stream)), "moe_scatter")
     return out
 
 

@@ -750,13 +750,15 @@ moe_status_t moe_grouped_gemm(const moe_gemm_args* args, void* ws, size_t ws_byt
 }
 
 moe_status_t moe_scatter(const float* rows, const int32_t* route_slot, const float* weights, int M,
-                         int N, int top_k, void* out, void* stream) {
+                         int N, int top_k, void* out, void* ws, void* stream) {
   if (rows == nullptr || route_slot == nullptr || weights == nullptr || out == nullptr)
     return MOE_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || top_k <= 0) return MOE_ERR_INVALID_ARG;
   if (top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(M) * top_k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_WORKSPACE;
   return cuda_status(launch_scatter(rows, route_slot, weights, M, N, top_k, out,
-                                    static_cast<cudaStream_t>(stream)));
+                                    static_cast<Ctrl*>(ws), static_cast<cudaStream_t>(stream)));
 }
 
 size_t moe_workspace_size(const moe_forward_args* args) {

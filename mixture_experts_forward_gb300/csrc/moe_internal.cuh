@@ -122,7 +122,7 @@ cudaError_t launch_reduce_rows(const void* rows, const int32_t* route_slot, cons
                                int M, int N, int k, void* out, int num_sms, cudaStream_t stream,
                                bool pdl);
 cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const float* weights,
-                           int M, int N, int k, void* out, cudaStream_t stream);
+                           int M, int N, int k, void* out, Ctrl* ctrl, cudaStream_t stream);
 cudaError_t launch_gather_rows_bf16(const void* x, int M, int K, int k, int32_t* route_slot,
                                     void* a, float* zero_acc, int zero_cols, const Placement& pl,
                                     cudaStream_t stream, bool pdl);

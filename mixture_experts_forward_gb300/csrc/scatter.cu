@@ -53,12 +53,17 @@ __global__ void __launch_bounds__(256) scatter_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ route_slot,
                                                       const float* __restrict__ weights, int M,
                                                       int N, int k,
-                                                      __nv_bfloat16* __restrict__ out) {
+                                                      __nv_bfloat16* __restrict__ out, Ctrl* ctrl) {
   pdl_wait();
   pdl_launch_dependents();
   const int t = blockIdx.x;
   if (t >= M) return;
   const int R = M * k;
+  // a route whose slot is out of range adds nothing and is reported once per token
+  if (threadIdx.x < k) {
+    const int slot = __ldg(route_slot + static_cast<size_t>(t) * k + threadIdx.x);
+    if (slot < 0 || slot >= R) set_error(ctrl, MOE_ERR_DEVICE_FAULT, 3);
+  }
   for (int n = threadIdx.x; n < N; n += blockDim.x) {
     float acc = 0.0f;
     for (int j = 0; j < k; ++j) {
@@ -223,11 +228,11 @@ cudaError_t launch_reduce_rows(const void* rows, const int32_t* route_slot, cons
 }
 
 cudaError_t launch_scatter(const float* rows, const int32_t* route_slot, const float* weights,
-                           int M, int N, int k, void* out, cudaStream_t stream) {
+                           int M, int N, int k, void* out, Ctrl* ctrl, cudaStream_t stream) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(M), dim3(256), stream, false, attr);
   return cudaLaunchKernelEx(&cfg, scatter_kernel, rows, route_slot, weights, M, N, k,
-                            static_cast<__nv_bfloat16*>(out));
+                            static_cast<__nv_bfloat16*>(out), ctrl);
 }
 
 cudaError_t launch_place_routes(int M, int k, int32_t* route_slot, float* zero_acc, int zero_cols,

@@ -76,6 +76,7 @@ def lib():
         L.oracle_quant_gather.argtypes = [P, i, i, i, P, P, P]
         L.oracle_grouped_gemm_fp8.argtypes = [P, P, i, i, P, P, i, i, P, P, i, P]
         L.oracle_scatter.argtypes = [P, P, P, i, i, P, i, P]
+        L.oracle_grouped_gemm_bf16.argtypes = [P, i, i, P, i, i, P, i, P]
         L.oracle_forward_fp8.argtypes = [P, P, P, P, i, i, i, i, i, f, i, i, P, i, i,
                                          P, P, P, P, P, P, P, P, P, P]
         L.oracle_dense_fp8.argtypes = [P, P, P, P, P, i, i, i, i, i, P, i, i, P]
@@ -193,6 +194,19 @@ def grouped_gemm_fp8(a_q, a_scales, w_q, w_scales, offsets, row_mask=None, threa
     mask = None if row_mask is None else _c(row_mask, np.uint8)
     lib().oracle_grouped_gemm_fp8(_p(a_q), _p(a_scales), R, K, _p(w_q), _p(w_scales), E, N,
                                   _p(_c(offsets, np.int32)), _p(mask), threads, _p(Y))
+    return Y
+
+
+def grouped_gemm_bf16(a_bits, w_bits, offsets, threads=1):
+    """BF16 grouped GEMM on expert-compact rows: a u16 bf16 bits [R, K], w u16
+    bf16 bits [E, N, K] -> Y f64 [R, N] (slots outside every expert: 0)."""
+    a = _c(a_bits, np.uint16)
+    w = _c(w_bits, np.uint16)
+    R, K = a.shape
+    E, N, _ = w.shape
+    Y = np.zeros((R, N), np.float64)
+    lib().oracle_grouped_gemm_bf16(_p(a), R, K, _p(w), E, N, _p(_c(offsets, np.int32)),
+                                   int(threads), _p(Y))
     return Y
 
 

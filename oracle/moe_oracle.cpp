@@ -273,6 +273,30 @@ void oracle_grouped_gemm_fp8(const uint8_t* a_q, const float* a_scales, int R, i
   });
 }
 
+// BF16 grouped GEMM ("H200 MoE Grouped GEMM", section 4: compact routed rows;
+// the gated up and down projections of its config-tuning benchmark design):
+// for every slot s of expert e (offsets[e] <= s < offsets[e+1]) and output n,
+// Y[s,n] = sum_k a[s,k] * w[e,n,k], the bf16 values widened exactly and the
+// products and sum in binary64.
+void oracle_grouped_gemm_bf16(const uint16_t* a_bf16, int R, int K, const uint16_t* w_bf16,
+                              int E, int N, const int32_t* offsets, int threads, double* Y) {
+  std::vector<int> expert_of(R, -1);
+  for (int e = 0; e < E; ++e)
+    for (int s = offsets[e]; s < offsets[e + 1]; ++s) expert_of[s] = e;
+  parallel_for(R, threads, [&](int s) {
+    int e = expert_of[s];
+    if (e < 0) return;
+    std::vector<double> a(K);
+    for (int i = 0; i < K; ++i) a[i] = bf16_to_f32(a_bf16[(size_t)s * K + i]);
+    for (int n = 0; n < N; ++n) {
+      const uint16_t* w = w_bf16 + ((size_t)e * N + n) * K;
+      double acc = 0.0;
+      for (int i = 0; i < K; ++i) acc += a[i] * double(bf16_to_f32(w[i]));
+      Y[(size_t)s * N + n] = acc;
+    }
+  });
+}
+
 void oracle_scatter(const double* Y, const int32_t* route_slot, const float* weights,
                     int N, int k, const int32_t* tokens, int n_tokens, double* out) {
   for (int i = 0; i < n_tokens; ++i) {

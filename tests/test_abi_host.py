@@ -159,6 +159,16 @@ def test_forward_cta_pairs_argument(lib):
                                                         **big))) == 0
 
 
+def test_scatter_argument_errors(lib):
+    P = ctypes.c_void_p
+    f = P(FAKE)
+    assert lib.moe_scatter(f, f, f, 4, 256, 2, f, None, None) == L.MOE_ERR_WORKSPACE
+    assert lib.moe_scatter(f, f, f, 4, 256, 2, f, P(FAKE + 16), None) == L.MOE_ERR_WORKSPACE
+    assert lib.moe_scatter(None, f, f, 4, 256, 2, f, f, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_scatter(f, f, f, 0, 256, 2, f, f, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_scatter(f, f, f, 4, 256, 33, f, f, None) == L.MOE_ERR_UNSUPPORTED
+
+
 def test_swiglu_quant_argument_errors(lib):
     P = ctypes.c_void_p
     f = P(FAKE)

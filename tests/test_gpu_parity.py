@@ -313,12 +313,7 @@ def _bf16_gemm_case(R_tokens, K, N, E, k, bm, epilogue, sched=L.SCHED_QUEUE, see
     x = torch.randn(M, K, generator=g).to(torch.bfloat16)
     w = (torch.randn(E, N, K, generator=g) / np.sqrt(K)).to(torch.bfloat16)
     a = x[torch.from_numpy(lay["sorted_route_ids"] // k).long()]  # expert-compact rows
-    A = a.double().numpy()
-    W = w.double().numpy()
-    Y = np.zeros((M * k, N))
-    for e in range(E):
-        s0, s1 = lay["offsets"][e], lay["offsets"][e + 1]
-        Y[s0:s1] = A[s0:s1] @ W[e].T
+    Y = oracle.grouped_gemm_bf16(bits(a), bits(w), lay["offsets"], threads=THREADS)
     cu = lambda t: torch.from_numpy(np.ascontiguousarray(t)).cuda()
     ws = L.new_workspace(L.CTRL_BYTES)
     if epilogue == L.EPI_SWIGLU:
@@ -648,9 +643,33 @@ def test_scatter_standalone():
     rows = torch.randn(M * k, N, generator=g)
     w = torch.rand(M, k, generator=g)
     slot = torch.randperm(M * k, generator=g).to(torch.int32)
-    out = L.scatter(rows.cuda(), slot.cuda(), w.cuda())
+    ws = L.new_workspace(L.CTRL_BYTES)
+    out = L.scatter(rows.cuda(), slot.cuda(), w.cuda(), ws)
     ref = oracle.scatter(rows.double().numpy(), slot.numpy(), w.numpy())
     assert_close(out, ref, "scatter")
+    assert L.get_error(ws) == L.MOE_OK
+
+
+def test_scatter_reports_bad_slots():
+    """A route whose slot is outside [0, M*top_k) adds nothing and records
+    MOE_ERR_DEVICE_FAULT; reading the status clears it."""
+    g = torch.Generator().manual_seed(4)
+    M, N, k = 9, 256, 2
+    rows = torch.randn(M * k, N, generator=g)
+    w = torch.rand(M, k, generator=g)
+    slot = torch.randperm(M * k, generator=g).to(torch.int32)
+    ws = L.new_workspace(L.CTRL_BYTES)
+    bad = slot.clone()
+    bad[5] = M * k                       # token 2, route 1
+    bad[8] = -3                          # token 4, route 0
+    out = L.scatter(rows.cuda(), bad.cuda(), w.cuda(), ws)
+    assert L.get_error(ws) == L.MOE_ERR_DEVICE_FAULT
+    w0 = w.clone()
+    w0[2, 1] = 0.0
+    w0[4, 0] = 0.0
+    ref = oracle.scatter(rows.double().numpy(), slot.numpy(), w0.numpy())
+    assert_close(out, ref, "scatter without the bad routes")
+    assert L.get_error(ws) == L.MOE_OK
 
 
 # ------------------------------------------------------------------ failure detection

@@ -219,6 +219,38 @@ def test_gemm_identity_weights_return_dequantised_rows():
     assert np.array_equal(Y, 0.5 * deq.reshape(M, K)[:, :N])
 
 
+def test_gemm_bf16_single_expert_is_textbook_matmul():
+    """E=1: Y = A W^T of the bf16 values, against numpy's matmul in binary64."""
+    g = torch.Generator().manual_seed(12)
+    R, K, N = 19, 320, 96
+    a = torch.randn(R, K, generator=g).to(torch.bfloat16)
+    w = (torch.randn(1, N, K, generator=g) / 16).to(torch.bfloat16)
+    Y = oracle.grouped_gemm_bf16(inputs.bf16_bits(a), inputs.bf16_bits(w),
+                                 np.array([0, R], np.int32), threads=2)
+    ref = a.double().numpy() @ w[0].double().numpy().T
+    assert np.allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gemm_bf16_scaled_identity_per_expert():
+    """Expert e's weights are (e + 1) * I: every slot's row comes back scaled by
+    its own expert's factor, exactly (a wrong expert index or row fails)."""
+    g = torch.Generator().manual_seed(13)
+    E, K = 3, 64
+    counts = [5, 0, 7]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    R = int(offsets[-1])
+    a = torch.randn(R, K, generator=g).to(torch.bfloat16)
+    w = torch.zeros(E, K, K)
+    for e in range(E):
+        w[e] = (e + 1) * torch.eye(K)
+    w = w.to(torch.bfloat16)
+    Y = oracle.grouped_gemm_bf16(inputs.bf16_bits(a), inputs.bf16_bits(w), offsets)
+    A = a.double().numpy()
+    for e in range(E):
+        s0, s1 = offsets[e], offsets[e + 1]
+        assert np.array_equal(Y[s0:s1], (e + 1) * A[s0:s1])
+
+
 def test_forward_token_subset_equals_full():
     d = inputs.make_fp8_inputs("tiny_fp8", seed=3)
     args = (d["logits"].numpy(), inputs.bf16_bits(d["x"]), d["w_q"].numpy(), d["w_scales"].numpy())
