@@ -188,21 +188,30 @@ __host__ __device__ inline int meta_slot_bytes(bool fp8, int bm, int kb_per_spli
 // group, two tile buffers of [4 quadrants][32 routed rows] floats.
 __host__ __device__ constexpr int swiglu_red_bytes(int groups) { return groups * 2 * 4 * 32 * 4; }
 
-// Work items of the queue: with a split tail (p.tail_tiles > 0, one K split)
-// the last tail_tiles output tiles are handed out as tail_parts K parts each
-// (halves or quarters), so the final wave of work is that much shorter; the
-// other items are whole tiles.
+// Output tiles handed out as tail_parts K parts each (halves or quarters) at
+// the end of the work list, one K split only: p.tail_tiles of them for the
+// queue (one per CTA: the last wave), or, for the fixed round-robin order of
+// G = -p.tail_tiles CTA pairs, the remainder of an even split plus one round
+// (every tile when T < 2G), so that every pair gets the same number of whole
+// tiles and the parts spread the rest.
+__device__ __forceinline__ int tail_count(const GemmParams& p, int T) {
+  if (p.tail_tiles >= 0) return min(p.tail_tiles, T);
+  const int G = -p.tail_tiles;
+  return T >= 2 * G ? T % G + G : T;
+}
+
+// Work items: whole tiles, then the split tail's parts.
 __device__ __forceinline__ int work_items(const GemmParams& p, const int* s_tile_off) {
   const int T = s_tile_off[p.E] * p.n_tiles * p.k_splits;
-  return T + min(p.tail_tiles, T) * (p.tail_parts - 1);
+  return T + tail_count(p, T) * (p.tail_parts - 1);
 }
 
 __device__ __forceinline__ void decode_tile(int t, const GemmParams& p, const int* s_tile_off,
                                             const int* s_off, int BM, TileDesc& d) {
   int part = -1;  // >= 0: K part of a split tail tile
-  if (p.tail_tiles > 0) {
+  if (p.tail_tiles != 0) {
     const int T = s_tile_off[p.E] * p.n_tiles;
-    const int F = T - min(p.tail_tiles, T);
+    const int F = T - tail_count(p, T);
     if (t >= F) {
       part = (t - F) % p.tail_parts;
       t = F + (t - F) / p.tail_parts;

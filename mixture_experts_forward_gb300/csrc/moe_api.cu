@@ -265,7 +265,7 @@ moe_status_t run_gemm(const moe_gemm_args* a, Ctrl* ctrl, bool second, cudaStrea
   // (CTA pairs walk a fixed round-robin list, one tile per pair at a time)
   if (fp8 && a->epilogue == MOE_EPI_SCATTER && p.k_splits == 1 &&
       (a->sched == MOE_SCHED_QUEUE || p.cta2) && p.tail_partkb > 0)
-    p.tail_tiles = p.cta2 ? ctas / 2 : ctas;
+    p.tail_tiles = p.cta2 ? -(ctas / 2) : ctas;   // (negative: the pairs' balanced tail)
   CUtensorMap tw, ta;
   if (!make_tmap(&tw, a->w, fp8, static_cast<uint64_t>(a->K),
                  static_cast<uint64_t>(a->E) * a->N, 128u, static_cast<uint32_t>(p.sk)))

@@ -52,7 +52,8 @@ struct GemmParams {
   int num_stages;
   int sk;                       // K blocks per pipeline stage (1, 2 or 4)
   int w_reuse;                  // experts average more than one row tile: keep weights in L2
-  int tail_tiles;               // queue, FP8 scatter, one K split: last tiles split in K parts
+  int tail_tiles;               // FP8 scatter, one K split: last tiles split in K parts (the
+                                // queue: this many; -G: balanced for G CTA pairs' fixed order)
   int tail_parts;               // 2 or 4 parts per split tile
   int tail_partkb;              // K blocks of each part but the last (a multiple of sk)
   int warm_first;               // before the wait for the layout: L2-prefetch the weight tiles
