@@ -693,3 +693,58 @@ def test_pipeline_timeout_reports_status_and_recovers():
     r = oracle.forward_fp8(d["logits"].numpy(), bits(d["x"]), d["w_q"].numpy(),
                            d["w_scales"].numpy(), k=2)
     assert_close(out, r["out"], "after timeout")
+
+
+@pytest.mark.parametrize("form", ["fp8_scatter", "fp8_swiglu", "bf16_scatter"])
+def test_cta_pair_timeout_reports_status_and_recovers(form):
+    """The same fault on the CTA-pair kernels: neither CTA of a pair receives
+    any copy, the even CTA's MMA thread and both CTAs' other roles run into
+    their time limits, both CTAs still meet at the closing cluster barrier,
+    the launch ends with MOE_ERR_TIMEOUT, and the next call is correct."""
+    assert L.gemm_cta_pairs() > 0, "the CTA-pair form is not in use on this device"
+    M, k, E, K = 256, 2, 4, 256
+    ids = np.stack([np.arange(M) % E, (np.arange(M) + 1) % E], axis=1).astype(np.int32)
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    fp8 = form != "bf16_scatter"
+    bm = 128 if fp8 else 256
+    lay = oracle.layout(ids, E, block_m=bm)
+    R = M * k
+    ws = L.new_workspace(L.CTRL_BYTES)
+    common = dict(offsets=cu(lay["offsets"]), tile_offsets=cu(lay["tile_offsets"]), ws=ws,
+                  block_m=bm, M=M, top_k=k)
+    try:
+        L.debug_set_pipeline_fault(True, 20_000_000)   # 20 ms
+        if form == "fp8_scatter":
+            L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_SCATTER,
+                           a=torch.zeros(R, K, dtype=torch.uint8, device="cuda"),
+                           a_scales=torch.zeros(K // 128, R, device="cuda"),
+                           w=torch.zeros(E, 512, K, dtype=torch.uint8, device="cuda"),
+                           w_scales=torch.zeros(E, 4, K // 128, device="cuda"),
+                           out=torch.zeros(M, 512, device="cuda"),
+                           sorted_route_ids=cu(lay["sorted_route_ids"]),
+                           route_weights=torch.ones(M, k, device="cuda"), **common)
+        elif form == "fp8_swiglu":
+            L.grouped_gemm(dtype=L.DTYPE_FP8, epilogue=L.EPI_SWIGLU,
+                           a=torch.zeros(R, K, dtype=torch.uint8, device="cuda"),
+                           a_scales=torch.zeros(K // 128, R, device="cuda"),
+                           w=torch.zeros(E, 512, K, dtype=torch.uint8, device="cuda"),
+                           w_scales=torch.zeros(E, 4, K // 128, device="cuda"),
+                           out=torch.zeros(R, 256, dtype=torch.uint8, device="cuda"),
+                           out_scales=torch.zeros(2, R, device="cuda"), **common)
+        else:
+            L.grouped_gemm(dtype=L.DTYPE_BF16, epilogue=L.EPI_SCATTER,
+                           a=torch.zeros(R, K, dtype=torch.bfloat16, device="cuda"),
+                           w=torch.zeros(E, 512, K, dtype=torch.bfloat16, device="cuda"),
+                           out=torch.zeros(M, 512, device="cuda"),
+                           sorted_route_ids=cu(lay["sorted_route_ids"]),
+                           route_weights=torch.ones(M, k, device="cuda"), **common)
+        torch.cuda.synchronize()
+        assert L.get_error(ws) == L.MOE_ERR_TIMEOUT
+    finally:
+        L.debug_set_pipeline_fault(False, 0)
+    if form == "fp8_scatter":
+        _fp8_gemm_case(M=700, K=1024, N=512, E=8, k=3, bm=128, epilogue=L.EPI_SCATTER, skew=1.5)
+    elif form == "fp8_swiglu":
+        _fp8_swiglu_case(M=700, K=1024, I=256, E=8, k=3, bm=128, skew=1.5)
+    else:
+        _bf16_gemm_case(R_tokens=600, K=512, N=512, E=8, k=2, bm=256, epilogue=L.EPI_SCATTER)
