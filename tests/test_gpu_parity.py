@@ -216,6 +216,26 @@ def test_gemm_fp8_scatter_cta_pairs(M, E, k, N, ctas, skew):
                    num_ctas=ctas)
 
 
+@pytest.mark.parametrize("case", ["fp8_scatter_one_weight_tile", "fp8_scatter_one_expert",
+                                  "fp8_swiglu_one_h_tile", "bf16_scatter_one_k_block",
+                                  "bf16_swiglu_exact_tile"])
+def test_gemm_cta_pairs_edges(case):
+    """CTA pairs at the edges of their tilings: a single 256-row weight tile
+    (N = 256), every route on one expert, a single 128-column h tile, a single
+    64-deep BF16 K block, and a pair tile filled exactly (256 routed rows)."""
+    assert L.gemm_cta_pairs() > 0, "the CTA-pair form is not in use on this device"
+    if case == "fp8_scatter_one_weight_tile":
+        _fp8_gemm_case(M=300, K=512, N=256, E=8, k=2, bm=128, epilogue=L.EPI_SCATTER, skew=1.0)
+    elif case == "fp8_scatter_one_expert":
+        _fp8_gemm_case(M=400, K=384, N=512, E=1, k=1, bm=128, epilogue=L.EPI_SCATTER)
+    elif case == "fp8_swiglu_one_h_tile":
+        _fp8_swiglu_case(M=300, K=512, I=128, E=4, k=2, bm=128, skew=1.0)
+    elif case == "bf16_scatter_one_k_block":
+        _bf16_gemm_case(R_tokens=300, K=64, N=512, E=4, k=2, bm=256, epilogue=L.EPI_SCATTER)
+    else:
+        _bf16_gemm_case(R_tokens=128, K=256, N=256, E=1, k=2, bm=256, epilogue=L.EPI_SWIGLU)
+
+
 @pytest.mark.parametrize("form", ["fp8_scatter", "fp8_swiglu", "bf16_scatter", "bf16_swiglu"])
 def test_gemm_cta_pairs_off(form):
     """cta_pairs = -1: shapes that have a CTA-pair form run single CTAs."""
