@@ -82,14 +82,14 @@ struct TileDesc {
 // per epilogue thread, and run one TMA producer warp so that four epilogue
 // warps per TMEM lane quadrant fit the register file at 128 routed rows.
 //
-// CTA pairs (kCta2; FP8 at 128 routed rows per CTA): a cluster of two CTAs on
-// two SMs shares each MMA (tcgen05.mma.cta_group::2, M = 256).  The even CTA
-// issues every MMA; its mbarriers count both CTAs' copies and both CTAs'
-// epilogue releases.
-//   scatter: a tile of 256 weight rows x 128 routed rows; each CTA stages its
-//     own 128 weight rows and half of the routed rows (64) and holds its weight
-//     rows' 128 x 128 accumulator in its own TMEM, so a K block's buffer is 128
-//     columns (four in TMEM) and a stage 24 KB per K block.
+// CTA pairs (kCta2): a cluster of two CTAs on two SMs shares each MMA
+// (tcgen05.mma.cta_group::2, M = 256).  The even CTA issues every MMA; its
+// mbarriers count both CTAs' copies and both CTAs' epilogue releases.
+//   FP8 scatter at block_m 128: a tile of 256 weight rows x 128 routed rows;
+//     each CTA stages its own 128 weight rows and half of the routed rows (64)
+//     and holds its weight rows' 128 x 128 accumulator in its own TMEM, so a
+//     K block's buffer is 128 columns (four in TMEM) and a stage 24 KB per K
+//     block.
 //   BF16 scatter / bf16 rows at block_m 256: a tile of 256 weight rows x 256
 //     routed rows; each CTA stages its 128 weight rows and half of the routed
 //     rows and holds its weight rows' 128 x 256 accumulator, so TMEM takes two
@@ -129,7 +129,8 @@ struct Cfg {
   static constexpr int kATiles = (kPair && !kCta2) ? 2 : 1;
   static constexpr int kRing = ring_slots(kFP8, BM);
   // TMA producer warps (warp 0 plus warps 7..): two measured best (four were
-  // no faster on any workload and slower on the BF16 FFN); FP8 pair tiles: one
+  // no faster on any workload and slower on the BF16 FFN); FP8 pair tiles and
+  // CTA pairs: one
   static constexpr int kProducers = (kFP8Pair || kCta2) ? 1 : 2;
   // FP8 with block_m >= 64 and BF16 with block_m >= 128: two epilogue warps per
   // TMEM lane quadrant, each taking half of the tile's columns (routed rows),
@@ -137,7 +138,8 @@ struct Cfg {
   // the per-tile stores and reductions (BF16); otherwise one per quadrant
   // (BF16 with block_m 256: four, since its SwiGLU accumulator fills TMEM, so
   // the tile's epilogue is not overlapped with the next tile's MMAs).  FP8
-  // pair tiles: one warp per quadrant for every 32 routed rows.
+  // pair tiles: one warp per quadrant for every 32 routed rows; CTA pairs:
+  // four per quadrant.
   static constexpr int kEpiGroups = kFP8Pair ? (BM >= 32 ? BM / 32 : 1)
                                   : kCta2 ? 4
                                   : (!kFP8 && BM >= 256) ? 4
@@ -148,12 +150,12 @@ struct Cfg {
   static constexpr int kGroup1Warp = kFirstExtraProducer + kProducers - 1;
   static constexpr int kWarps = kGroup1Warp + 4 * (kEpiGroups - 1);
   static constexpr int kThreads = 32 * kWarps;
-  // bytes of one K block of a stage; a stage holds p.sk K blocks laid out as
-  // [kATiles][sk] weight tiles, then [sk] activation tiles
   // routed rows of a stage (CTA-pair scatter: this CTA's half of the tile's)
   static constexpr int kBRows = (kCta2 && !kSwiglu) ? BM / 2 : BM;
   // routed rows of one tile (CTA-pair SwiGLU: BM per CTA, so 2 * BM per pair)
   static constexpr int kTileRows = (kCta2 && kSwiglu) ? 2 * BM : BM;
+  // bytes of one K block of a stage; a stage holds p.sk K blocks laid out as
+  // [kATiles][sk] weight tiles, then [sk] activation tiles
   static constexpr int kStageBytes = kATiles * kATileBytes + kBRows * kRowBytes;
   // FP8 epilogue: K blocks whose partials are loaded before one wait (<= 64 columns)
   static constexpr int kKbGroup = BM <= 64 ? 64 / BM : 1;
